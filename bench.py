@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Throughput of the tree-speculative-decoding verification step on GB300.
+
+A step is the whole hot path over one batch: ancestor masks, tree-verify
+attention, greedy acceptance and KV commit (four C-ABI calls, captured once in a
+CUDA graph). Workload: the Llama-3-8B-shaped single-sequence verify — bf16,
+32 query / 8 KV heads, head dim 128, a 4096-token prefix in shuffled 16-token
+pages, a 64-node EAGLE-2-style tree (top-10, depth <= 8), fp32 target logits over
+a 128256-token vocabulary; synthetic, seeded.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead
+(the fp64 numpy restatement of the same step) on the host cores.
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the path shards by
+sequence and has no exchange step); value = all ranks' tokens / max-rank time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify attn tokens/s, TFLOP/s & GB/s (% roofline); accept+commit µs/step"
+WORKLOAD = "llama3-8b-single-verify: bf16, B1, Hq32/Hkv8, D128, prefix 4096 (16-token pages, shuffled), " \
+           "64-node EAGLE-2 tree (top-10, depth<=8), vocab 128256 fp32 logits, greedy + commit"
+CONFIG_INDEX = 2
+L2_BYTES = 256 << 20          # flush buffer, larger than the 129 MB L2
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- work counts
+
+def work_counts(inp, accept_len=None):
+    """Algorithmic FLOPs and bytes of one step's kernels (per launch)."""
+    import numpy as np
+
+    qo = inp.qo_indptr
+    # ancestors per node = depth + 1 (computed from the parent array; counting, not verifying)
+    anc = np.zeros(inp.total_nodes, np.int64)
+    for b in range(inp.batch):
+        a, e = qo[b], qo[b + 1]
+        dep = np.zeros(e - a, np.int64)
+        for i in range(1, e - a):
+            dep[i] = dep[inp.parent[a + i]] + 1
+        anc[a:e] = dep + 1
+    esz = 4 if inp.dtype == "f32" else 2
+    P = inp.prefix_len.astype(np.int64)
+    n = np.diff(qo).astype(np.int64)
+    keys = np.repeat(P, n) + anc                       # keys each tree node attends to
+    attn_flops = int(4 * keys.sum() * inp.hq * inp.d)  # QK^T and PV, 2 FLOP per MAC
+    attn_bytes = int(P.sum() * inp.hkv * inp.d * esz * 2            # prefix K and V, once per KV head
+                     + inp.total_nodes * inp.hkv * inp.d * esz * 2  # tree K and V
+                     + inp.total_nodes * inp.hq * inp.d * esz * 2   # Q in, O out
+                     + inp.total_nodes * inp.mask_words * 8)
+    accept_bytes = int(inp.total_nodes * inp.vocab * 4)   # one pass over every node's logits
+    commit_bytes = 0
+    if accept_len is not None:
+        commit_bytes = int(((np.asarray(accept_len) + 1) * inp.hkv * inp.d * esz * 2 * 2).sum())
+    return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, accept_bytes=accept_bytes, commit_bytes=commit_bytes,
+                tokens=int(inp.total_nodes))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- traffic record
+
+def _kernel_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "attention": ["speculative_decoding_tree_parent_gb300/csrc/attn_tc.cu",
+                  "speculative_decoding_tree_parent_gb300/csrc/attn_simt.cu",
+                  "speculative_decoding_tree_parent_gb300/csrc/attn_common.cuh"],
+    "accept": ["speculative_decoding_tree_parent_gb300/csrc/accept.cu"],
+}
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec or rec.get("source_digest") != _kernel_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = W.generate_index(CONFIG_INDEX, seed=CONFIG_INDEX + 1000 * rank if rank else None)
+    # R device replicas of the batch (same values, separate buffers): one graph replay runs
+    # R steps back to back, each on a replica the previous steps did not touch, so every
+    # step reads its inputs from HBM (R x ~51 MB > the 129 MB L2); L2 is also flushed
+    # before every replay. R divides K so exactly K steps are timed.
+    R = max(r for r in range(1, 9) if args.steps % r == 0)
+    reps = [DeviceBatch(inp, device=dev, mode="greedy") for _ in range(R)]
+    db = reps[0]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_BYTES, dtype=torch.uint8, device=dev)
+
+    with torch.cuda.stream(stream):
+        for rep in reps:                        # load the library, settle the workspaces
+            rep.step("greedy")
+    torch.cuda.synchronize()
+    assert all(rep.device_status() == 0 for rep in reps)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def over_reps(name):
+        def run():
+            for rep in reps:
+                getattr(rep, name)() if name != "accept" else rep.accept("greedy")
+        return run
+
+    g_step = capture(lambda: [rep.step("greedy") for rep in reps])
+    g_one = capture(lambda: db.step("greedy"))
+    g_calls = {"mask": capture(over_reps("build_mask")), "attention": capture(over_reps("attention")),
+               "accept": capture(over_reps("accept")), "commit": capture(over_reps("commit"))}
+    launches = db.launches_per_step("greedy")
+    splits, tc = db.attn_plan()
+
+    def timed_replays(graphs, n):
+        """n rounds of: flush L2, then each graph between its own pair of events."""
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in graphs]
+              for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for r in range(n):
+                for gi, g in enumerate(graphs):
+                    flush.zero_()
+                    ev[r][gi][0].record(stream)
+                    g.replay()
+                    ev[r][gi][1].record(stream)
+        return ev
+
+    # warm-up
+    timed_replays([g_step] + list(g_calls.values()), max(args.warmup, 3))
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps = K / R replays of the R-step graph --------------------
+    n_rep = args.steps // R
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev_step = timed_replays([g_step], n_rep)
+        ev_calls = timed_replays(list(g_calls.values()), n_rep)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) / R for ((a, b),) in ev_step]
+    call_ms = {name: [ev_calls[r][i][0].elapsed_time(ev_calls[r][i][1]) / R for r in range(n_rep)]
+               for i, name in enumerate(g_calls)}
+    total_ms = sum(step_ms) * R
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert all(rep.device_status() == 0 for rep in reps), [rep.device_status() for rep in reps]
+
+    # ---- end-to-end through the C ABI with host buffers ------------------------------
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {k: pin(getattr(db, k)) for k in ("q", "k_tree", "v_tree", "parent", "qo", "tokens", "target_logits",
+                                            "page_table", "prefix_len")}
+    h_out = {k: torch.empty_like(getattr(db, k), device="cpu").pin_memory()
+             for k in ("accept_len", "path", "out_tokens", "seq_len")}
+    bi = sum(t.numel() * t.element_size() for t in h_in.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_ms = []
+    for r in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a.record(stream)
+            for k, h in h_in.items():
+                getattr(db, k).copy_(h, non_blocking=True)
+            g_one.replay()
+            for k, h in h_out.items():
+                h.copy_(getattr(db, k), non_blocking=True)
+            b.record(stream)
+        b.synchronize()
+        if r >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if ws > 1:
+        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+
+    # ---- figures ------------------------------------------------------------------------
+    wc = work_counts(inp, db.accept_len.cpu().numpy())
+    hbm, tfl, tfl_sus, peak_kind = _peaks()
+    ms_step = total_ms / args.steps
+    tokens_all = wc["tokens"] * ws * args.steps
+    value = tokens_all / (total_ms / 1e3)
+    t_attn = statistics.mean(call_ms["attention"]) / 1e3
+    t_acc = statistics.mean(call_ms["accept"]) / 1e3
+    t_com = statistics.mean(call_ms["commit"]) / 1e3
+    attn_gbs = wc["attn_bytes"] / t_attn / 1e9
+    attn_tflops = wc["attn_flops"] / t_attn / 1e12
+    attn_roof = max(wc["attn_flops"] / (tfl * 1e12), wc["attn_bytes"] / (hbm * 1e9)) / t_attn
+    acc_gbs = wc["accept_bytes"] / t_acc / 1e9
+    accom_gbs = (wc["accept_bytes"] + wc["commit_bytes"]) / (t_acc + t_com) / 1e9
+    # dominant kernel = largest measured time
+    dom = "attention" if t_attn >= t_acc else "accept"
+    if dom == "attention":
+        bound = "tensor" if wc["attn_flops"] / (tfl * 1e12) > wc["attn_bytes"] / (hbm * 1e9) else "hbm"
+        if bound == "hbm":
+            roof = {"bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm}
+        else:
+            roof = {"bound": "tensor", "achieved": attn_tflops, "peak": tfl, "unit": "TFLOP/s",
+                    "frac": attn_tflops / tfl}
+    else:
+        roof = {"bound": "hbm", "achieved": acc_gbs, "peak": hbm, "unit": "GB/s", "frac": acc_gbs / hbm}
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} (burst)"
+    roof["traffic"] = recorded_traffic(dom)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": inp.batch, "tree_nodes": inp.total_nodes,
+                   "prefix": int(inp.max_prefix), "hq": inp.hq, "hkv": inp.hkv, "head_dim": inp.d,
+                   "vocab": inp.vocab,
+                   "l2": f"inputs larger than L2: {R} device replicas rotated inside each replay "
+                         f"({R} x {wc['attn_bytes'] + wc['accept_bytes'] >> 20} MB); L2 also flushed before each replay",
+                   "timing": f"CUDA-graph replay of {R} steps, CUDA events on the launching stream",
+                   "parallelism": "replicas" if ws > 1 else "single-gpu"},
+        "attn": {"tokens_per_s": wc["tokens"] / t_attn, "tflops": attn_tflops, "gbs": attn_gbs,
+                 "roofline_frac": attn_roof, "us": t_attn * 1e6, "flops": wc["attn_flops"],
+                 "bytes": wc["attn_bytes"], "splits": splits, "tensor_cores": bool(tc)},
+        "accept_commit": {"us_per_step": (t_acc + t_com) * 1e6, "accept_us": t_acc * 1e6,
+                          "commit_us": t_com * 1e6, "gbs": accom_gbs, "hbm_frac": accom_gbs / hbm,
+                          "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
+        "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
+        "roofline": roof,
+        "e2e": {"value": tokens_all / (e2e_total / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_total / args.steps},
+        # launches in the timed region: full-step replays + per-call replays (each call's kernels once)
+        "gpu_launches": 2 * launches * args.steps,   # step replays + per-call replays, R steps each
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def _oracle_step(inp, oracle):
+    mask, _ = oracle.ancestor_mask_batch(inp.parent, inp.qo_indptr, inp.max_nodes)
+    oracle.tree_verify_attention(inp.q, inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree,
+                                 inp.v_tree, mask, inp.qo_indptr, inp.hq, inp.hkv)
+    acc = oracle.greedy_accept(inp.parent, inp.draft_tokens, inp.target_logits, inp.qo_indptr, inp.path_cap)
+    oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree, inp.v_tree, acc.path,
+                     acc.accept_len, inp.qo_indptr, inp.page_size)
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, seconds):
+    """The oracle, as it stands, on the host cores: whole config steps for about `seconds`."""
+    import oracle
+
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(inp, oracle)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * inp.total_nodes / dt, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{n} full verification steps of the same workload (fp64 numpy; BLAS threads = host cores)",
+            "seconds": dt}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    import oracle
+
+    inp = W.generate_index(CONFIG_INDEX)
+    for _ in range(args.warmup):
+        _oracle_step(inp, oracle)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step(inp, oracle)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = inp.total_nodes * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "parallelism": "host cores (rank 0 only)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                             "sample": "whole verification steps of the same workload, one per timed step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * spec_verify.h — C ABI of the tree-speculative-decoding verification path
+ * (library: libspecverify.so, sm_103a / GB300).
+ *
+ * Four operations, in the order a verification step runs them:
+ *
+ *   spec_build_tree_mask   draft tree (parent array) -> ancestor bitmasks + depths
+ *   spec_tree_verify_attn  one attention pass of every tree node over the paged
+ *                          prefix and the tree's own K/V, ancestors only
+ *   spec_accept            longest accepted path + bonus token (greedy / stochastic)
+ *   spec_kv_commit         the accepted path's K/V written into the paged cache
+ *
+ * Sources of the operations (page title, then section):
+ *   "EAGLE-2 deep dive" (techknowgenie): architecture section (all tree tokens
+ *     verified in one target forward with a 2-D tree mask injected into
+ *     attention; target logits contrasted with draft tokens; longest accepted
+ *     path; the target KV cache must not be contaminated), core-implementation
+ *     section (tree mask = node + ancestors up to the root; node ids in
+ *     creation order), production section (paged tree attention indexing the
+ *     mask over paged KV), benchmark section (rejection sampling, lossless).
+ *   "Accelerating Sonar through speculation" (Perplexity): speculative-decoding
+ *     section (n drafts -> up to n+1 tokens; the extra token from the target's
+ *     logits at the stop position), draft-target section (acceptance compares
+ *     full draft and target distributions; KV filled for accepted tokens),
+ *     EAGLE section (a custom mask over the whole sequence slows attention by
+ *     up to 50% — so the prefix here is never masked), MTP-schedule section (a
+ *     kernel inserts the next token after the shift, no CPU-GPU sync — so
+ *     every length stays on the device here).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer. No call allocates, frees or synchronises with the host:
+ *     each enqueues its kernels on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream) and returns.
+ *   - Layouts are row-major, C order. Tree node ids are sequence-local:
+ *     sequence b owns global rows [qo_indptr[b], qo_indptr[b+1]) of every
+ *     per-node array; its node i is global row qo_indptr[b] + i.
+ *   - Errors the host can see (null pointer, bad size, unsupported shape,
+ *     workspace too small) return a negative spec_status at once and enqueue
+ *     nothing. Errors that depend on device data (bad parent, page id outside
+ *     the pool, path longer than its buffer, timeout of a bounded wait) are
+ *     written to *dev_status with first-error-wins semantics (the word is
+ *     only changed while it holds SPEC_OK); the kernels then skip the bad
+ *     item and finish cleanly — no trap, assert or unbounded wait. dev_status
+ *     may be NULL (device errors are then not reported). The caller zeroes
+ *     it when it wants a fresh report.
+ *   - Workspace: `ws` is scratch of at least spec_workspace_size(...) bytes,
+ *     256-byte aligned. It must be zero-filled before its first use with
+ *     spec_accept; every call leaves the counters it uses at zero again. One
+ *     workspace must not serve two calls that may run concurrently.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_ARG = -1,         /* host: null pointer, negative or inconsistent size            */
+  SPEC_ERR_PARENT = -2,      /* device: parent array is not a tree (root != -1, parent >= i) */
+  SPEC_ERR_PAGE = -3,        /* device: page table entry outside [0, num_pages)              */
+  SPEC_ERR_CAPACITY = -4,    /* device: a sequence needs more nodes/pages/path slots than given */
+  SPEC_ERR_WORKSPACE = -5,   /* host: ws_bytes smaller than spec_workspace_size()            */
+  SPEC_ERR_UNSUPPORTED = -6, /* host: dtype / head dim / group size not implemented          */
+  SPEC_ERR_CUDA = -7,        /* host: a CUDA runtime call or kernel launch failed            */
+  SPEC_ERR_TIMEOUT = -8,     /* device: a bounded wait inside a kernel gave up               */
+  SPEC_ERR_INDEX = -9        /* device: token id / path node id out of range                 */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+typedef enum { SPEC_GREEDY = 0, SPEC_STOCHASTIC = 1 } spec_mode;
+typedef enum { SPEC_OP_MASK = 0, SPEC_OP_ATTN = 1, SPEC_OP_ACCEPT = 2, SPEC_OP_COMMIT = 3 } spec_op;
+
+/* Bytes of workspace `op` needs for these sizes (0 when it needs none).
+ * For SPEC_OP_ATTN the result depends on (batch, max_nodes, hq, hkv, d,
+ * max_prefix, total_nodes); for SPEC_OP_ACCEPT on (batch, total_nodes, vocab).
+ * Unused arguments may be 0. Returns 0 for invalid sizes. */
+size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, int hq, int hkv,
+                           int d, int max_prefix, int vocab);
+
+/* Launch plan spec_tree_verify_attn uses for these sizes (informational; the pages
+ * have no counterpart): *splits = number of key splits (> 1 adds a merge kernel),
+ * *tensor_cores = 1 when the tcgen05 kernel runs, 0 for the CUDA-core kernel.
+ * Returns SPEC_OK or SPEC_ERR_ARG / SPEC_ERR_UNSUPPORTED like the call would. */
+int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, int page_size,
+                   int max_prefix, int* splits, int* tensor_cores);
+
+/* Static, NUL-terminated description of a spec_status value. */
+const char* spec_status_string(int status);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+int spec_version(void);
+
+/*
+ * spec_build_tree_mask — ancestor bitmask of every draft-tree node.
+ *   ("EAGLE-2 deep dive", core-implementation section: a node's row of the tree
+ *   mask marks the node itself and every ancestor, walking parent links to the
+ *   root; nodes are numbered after their parents.)
+ *
+ *   parent     int32 [total_nodes]  sequence-local parent id; the root (node 0 of
+ *                                   each sequence) holds -1; node i > 0 needs
+ *                                   0 <= parent[i] < i.
+ *   qo_indptr  int32 [batch+1]      node ranges; qo_indptr[0] = 0, non-decreasing,
+ *                                   qo_indptr[batch] = total_nodes.
+ *   max_nodes  >= every sequence's node count; fixes the mask row width
+ *              W = ceil(max_nodes / 64) words.
+ *   mask       uint64 [total_nodes][W] (out)  bit (j & 63) of word (j >> 6) of row
+ *              t = node j of t's sequence is t itself or an ancestor of t. Bits of
+ *              node ids >= the sequence's node count are 0.
+ *   depth      int32 [total_nodes] (out, nullable)  parent links to the root (root 0).
+ *   Device errors: SPEC_ERR_PARENT (row left all-zero), SPEC_ERR_CAPACITY
+ *   (sequence longer than max_nodes; its rows are not written).
+ */
+int spec_build_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch,
+                         int total_nodes, int max_nodes, uint64_t* mask, int32_t* depth,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * spec_tree_verify_attn — tree-verify attention with GQA over a paged prefix.
+ *   ("EAGLE-2 deep dive", architecture and production sections: one target
+ *   forward over all tree tokens, 2-D tree mask inside attention, mask indexed
+ *   over paged KV. "Accelerating Sonar", EAGLE section: a mask over the whole
+ *   sequence costs up to 50% — here the prefix is never masked.)
+ *
+ *   For sequence b, node i, query head h (KV head g = h / (hq / hkv)):
+ *     keys  = prefix slots 0 .. prefix_len[b]-1  (read through page_table)
+ *             ++ tree nodes j of b with mask bit j of row i set
+ *     out[t][h] = softmax(sm_scale * q[t][h] . K^T) V,  lse[t][h] = ln sum exp(scores)
+ *
+ *   dtype      SPEC_F32 or SPEC_BF16: element type of q, k_pool, v_pool, k_tree,
+ *              v_tree and out (accumulation is fp32 in both cases).
+ *   q          [total_nodes][hq][d]
+ *   k_pool, v_pool  [num_pages][hkv][page_size][d]  the paged KV cache ("HND" pages)
+ *   page_table int32 [batch][max_pages]  page id of logical page p of sequence b;
+ *              entries past ceil(prefix_len[b] / page_size) are not read.
+ *   prefix_len int32 [batch]   verified prefix length per sequence (>= 0).
+ *   max_prefix >= every prefix_len[b]; used on the host to size the key split.
+ *   k_tree, v_tree  [total_nodes][hkv][d]  K/V of the tree tokens themselves.
+ *   mask       uint64 [total_nodes][ceil(max_nodes/64)]  from spec_build_tree_mask.
+ *   qo_indptr  int32 [batch+1]; max_nodes >= every sequence's node count.
+ *   hq % hkv == 0; d in {64, 128}; page_size a multiple of 8 (16 for the bf16
+ *   tensor-core path); sm_scale <= 0 selects 1/sqrt(d).
+ *   out        [total_nodes][hq][d] (out)
+ *   lse        float [total_nodes][hq] (out, nullable)  natural-log log-sum-exp.
+ *   ws         workspace of spec_workspace_size(SPEC_OP_ATTN, ...) bytes (key-split
+ *              partial results).
+ *   Device errors: SPEC_ERR_PAGE (page id outside [0, num_pages): the page is read
+ *   as zeros), SPEC_ERR_TIMEOUT.
+ */
+int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const void* v_pool,
+                          int num_pages, int page_size, const int32_t* page_table, int max_pages,
+                          const int32_t* prefix_len, int max_prefix, const void* k_tree,
+                          const void* v_tree, const uint64_t* mask, const int32_t* qo_indptr,
+                          int batch, int total_nodes, int max_nodes, int hq, int hkv, int d,
+                          float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
+
+/*
+ * spec_accept — longest accepted root-to-node path of each tree + the bonus token.
+ *   Greedy ("EAGLE-2 deep dive", architecture section; "Accelerating Sonar",
+ *   speculative-decoding section): a[v] = argmax of target_logits[v] (lowest
+ *   token id on ties); from the root, move to the first child (lowest node id)
+ *   whose draft token equals a[v]; stop when none does; bonus = a[stop node].
+ *   Stochastic ("EAGLE-2 deep dive", benchmark section; "Accelerating Sonar",
+ *   draft-target section; rule of the speculative-sampling works they cite):
+ *   p_v = softmax(target_logits[v] / T), q_v = softmax(draft_logits[v] / T);
+ *   at node v, r = p_v; each child c (increasing id, token x) is accepted iff
+ *   uniforms[c][0] < r(x) / q_v(x); a rejection replaces r by
+ *   max(r - q_v, 0) normalised; if no child is accepted the bonus is the
+ *   inverse-CDF draw from r with uniforms[v][1].
+ *
+ *   parent, draft_tokens  int32 [total_nodes]  (root's token = last accepted token)
+ *   target_logits  float [total_nodes][vocab]
+ *   draft_logits   float [total_nodes][vocab]  (stochastic only; NULL for greedy)
+ *   uniforms       float [total_nodes][2]      (stochastic only) (u_accept, u_bonus) in [0,1)
+ *   temperature    > 0 (stochastic only)
+ *   path_cap       row length of path / out_tokens (>= deepest accepted path + 1).
+ *   accept_len int32 [batch] (out)  L = accepted draft nodes (root excluded).
+ *   path       int32 [batch][path_cap] (out)  root (0) then the accepted node ids; -1 after.
+ *   out_tokens int32 [batch][path_cap] (out)  the L accepted tokens, then the bonus; -1 after.
+ *   flags      uint8 [batch] (out, nullable)  stochastic near-ties seen by the GPU:
+ *              bit 0 a ratio test with |u - ratio| <= 1e-6, bit 1 a bonus draw within
+ *              1e-8 (relative to the residual's total) of a CDF boundary. Greedy writes 0.
+ *   ws         workspace of spec_workspace_size(SPEC_OP_ACCEPT, ...) bytes, zeroed
+ *              before first use (see the conventions above).
+ *   Device errors: SPEC_ERR_PARENT, SPEC_ERR_INDEX (draft token outside [0, vocab)),
+ *   SPEC_ERR_CAPACITY (accepted path longer than path_cap - 1: truncated).
+ */
+int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens,
+                const float* target_logits, const float* draft_logits, const float* uniforms,
+                float temperature, int vocab, const int32_t* qo_indptr, int batch,
+                int total_nodes, int max_nodes, int path_cap, int32_t* accept_len, int32_t* path,
+                int32_t* out_tokens, uint8_t* flags, void* ws, size_t ws_bytes,
+                int32_t* dev_status, void* stream);
+
+/*
+ * spec_kv_commit — write the accepted path's K/V into each sequence's cache.
+ *   ("EAGLE-2 deep dive", architecture section: verification must not
+ *   contaminate the target KV cache; "Accelerating Sonar", draft-target and
+ *   MTP-schedule sections: KV of accepted tokens is filled, the next token is
+ *   placed after the shift on the device with no CPU sync.)
+ *   For i = 0 .. accept_len[b]: tree row qo_indptr[b] + path[b][i] (all hkv heads)
+ *   is copied to logical slot prefix_len[b] + i of sequence b (page
+ *   page_table[b][slot / page_size], row slot % page_size). Then
+ *   seq_len_out[b] = prefix_len[b] + accept_len[b] + 1. accept_len and path are
+ *   read on the device (straight from spec_accept), so no host sync is needed.
+ *   The tree buffers must not alias the pool.
+ *
+ *   dtype       element type of k_tree, v_tree, k_pool, v_pool.
+ *   k_tree, v_tree  [total_nodes][hkv][d];  k_pool, v_pool  [num_pages][hkv][page_size][d] (in/out)
+ *   path        int32 [batch][path_cap];  accept_len int32 [batch]
+ *   seq_len_out int32 [batch] (out, nullable)
+ *   Device errors: SPEC_ERR_INDEX (path node outside the sequence's tree, or
+ *   accept_len outside [0, path_cap)), SPEC_ERR_CAPACITY (slot beyond max_pages),
+ *   SPEC_ERR_PAGE (page id outside the pool). A sequence with an error is
+ *   left unwritten.
+ */
+int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path,
+                   int path_cap, const int32_t* accept_len, const int32_t* qo_indptr,
+                   const int32_t* page_table, int max_pages, int num_pages, int page_size,
+                   const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool, void* v_pool,
+                   int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,165 @@
+"""Thin ctypes binding of libspecverify (include/spec_verify.h).
+
+Functions carry the C entry points' names and argument order; they take torch
+tensors (device memory) and only marshal pointers, sizes and the current CUDA
+stream. All computation happens in the library's kernels. A negative status
+raises SpecError; nothing here falls back to another implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SPEC_OK = 0
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_GREEDY, SPEC_STOCHASTIC = 0, 1
+SPEC_OP_MASK, SPEC_OP_ATTN, SPEC_OP_ACCEPT, SPEC_OP_COMMIT = 0, 1, 2, 3
+STATUS = {
+    0: "SPEC_OK", -1: "SPEC_ERR_ARG", -2: "SPEC_ERR_PARENT", -3: "SPEC_ERR_PAGE", -4: "SPEC_ERR_CAPACITY",
+    -5: "SPEC_ERR_WORKSPACE", -6: "SPEC_ERR_UNSUPPORTED", -7: "SPEC_ERR_CUDA", -8: "SPEC_ERR_TIMEOUT",
+    -9: "SPEC_ERR_INDEX",
+}
+EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
+           "spec_tree_verify_attn", "spec_accept", "spec_kv_commit")
+
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "spec_version": (_I, []),
+    "spec_status_string": (ctypes.c_char_p, [_I]),
+    "spec_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "spec_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "spec_build_tree_mask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "spec_tree_verify_attn": (_I, [_I, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                   _I, _F, _P, _P, _P, _Z, _P, _P]),
+    "spec_accept": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
+    "spec_kv_commit": (_I, [_I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+}
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def load(path: str | None = None):
+    """Open libspecverify.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libspecverify not found at {path}")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().spec_status_string(int(status)).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(st: int, what: str) -> int:
+    if st < 0:
+        raise SpecError(st, what)
+    return st
+
+
+def _dtype(t) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t, dtype, what):
+    if t.dtype != dtype:
+        raise ValueError(f"{what}: {dtype} expected, got {t.dtype}")
+
+
+def spec_workspace_size(op, batch=0, total_nodes=0, max_nodes=0, hq=0, hkv=0, d=0, max_prefix=0, vocab=0) -> int:
+    return int(load().spec_workspace_size(op, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, vocab))
+
+
+def spec_attn_plan(dtype, batch, max_nodes, hq, hkv, d, page_size, max_prefix):
+    """(splits, tensor_cores) the attention call uses for these sizes."""
+    s, tc = ctypes.c_int(0), ctypes.c_int(0)
+    st = load().spec_attn_plan(int(dtype), batch, max_nodes, hq, hkv, d, page_size, max_prefix,
+                               ctypes.addressof(s), ctypes.addressof(tc))
+    _check(st, "spec_attn_plan")
+    return s.value, tc.value
+
+
+def spec_build_tree_mask(parent, qo_indptr, max_nodes, mask, depth=None, dev_status=None, stream=None):
+    _need(parent, torch.int32, "parent")
+    _need(qo_indptr, torch.int32, "qo_indptr")
+    _need(mask, torch.int64, "mask (uint64 bits held in an int64 tensor)")
+    st = load().spec_build_tree_mask(_ptr(parent), _ptr(qo_indptr), qo_indptr.numel() - 1, parent.numel(),
+                                     int(max_nodes), _ptr(mask), _ptr(depth), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_build_tree_mask")
+
+
+def spec_tree_verify_attn(q, k_pool, v_pool, page_table, prefix_len, max_prefix, k_tree, v_tree, mask,
+                          qo_indptr, max_nodes, out, lse=None, ws=None, sm_scale=0.0, dev_status=None,
+                          stream=None):
+    """q [T,Hq,D]; k_pool/v_pool [pages,Hkv,PS,D]; page_table int32 [B,max_pages]; k_tree/v_tree [T,Hkv,D]."""
+    dt = _dtype(q)
+    T, hq, d = q.shape
+    num_pages, hkv, ps, _ = k_pool.shape
+    st = load().spec_tree_verify_attn(
+        dt, _ptr(q), _ptr(k_pool), _ptr(v_pool), num_pages, ps, _ptr(page_table), page_table.shape[1],
+        _ptr(prefix_len), int(max_prefix), _ptr(k_tree), _ptr(v_tree), _ptr(mask), _ptr(qo_indptr),
+        qo_indptr.numel() - 1, T, int(max_nodes), hq, hkv, d, float(sm_scale), _ptr(out), _ptr(lse),
+        _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_tree_verify_attn")
+
+
+def spec_accept(mode, parent, draft_tokens, target_logits, qo_indptr, max_nodes, accept_len, path, out_tokens,
+                ws, draft_logits=None, uniforms=None, temperature=1.0, flags=None, dev_status=None, stream=None):
+    T, V = target_logits.shape
+    st = load().spec_accept(
+        int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+        float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
+        _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_accept")
+
+
+def spec_kv_commit(k_tree, v_tree, path, accept_len, qo_indptr, page_table, prefix_len, k_pool, v_pool,
+                   seq_len_out=None, dev_status=None, stream=None):
+    dt = _dtype(k_tree)
+    T, hkv, d = k_tree.shape
+    num_pages, _, ps, _ = k_pool.shape
+    st = load().spec_kv_commit(
+        dt, _ptr(k_tree), _ptr(v_tree), _ptr(path), path.shape[1], _ptr(accept_len), _ptr(qo_indptr),
+        _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
+        _ptr(v_pool), qo_indptr.numel() - 1, T, hkv, d, _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_kv_commit")

@@ -1,0 +1,634 @@
+// K-ACCEPT: longest accepted path of every draft tree + the bonus token.
+//
+// Greedy ("EAGLE-2 deep dive", architecture section: the target's logits are
+// contrasted with the draft tokens and the longest accepted path is fixed;
+// "Accelerating Sonar through speculation", speculative-decoding section: n
+// drafts give up to n+1 tokens, the extra one from the target's logits where
+// the walk stops). Stochastic ("EAGLE-2 deep dive", benchmark section:
+// rejection sampling on the target distribution; "Accelerating Sonar",
+// draft-target section: full draft and target distributions are compared),
+// with the rule of the speculative-sampling works those pages cite applied to
+// the children of a node one after another.
+//
+// Greedy, one launch:
+//   accept_argmax_kernel   grid = chunks x nodes. Each CTA streams one chunk of one
+//                          logits row with 16-byte loads and keeps (max, first index).
+//                          The last CTA of a row (atomic counter, no waiting) merges
+//                          the chunk partials into argmax[t]; the last row of a
+//                          sequence then runs the walk in one warp.
+// Stochastic, two launches:
+//   accept_stats_kernel    grid = chunks x nodes. Per row of target and draft logits:
+//                          max and sum of exp((x - max) / T) (fp32 elements, Kahan
+//                          compensated, fp64 across threads and chunks).
+//   accept_walk_kernel     one 8-CTA cluster per sequence. The decisions at a node
+//                          need sums over the vocabulary of the residual
+//                          max(p - c q, 0) (see below); each CTA sums its eighth of the
+//                          vocabulary and the eight partials are exchanged through
+//                          distributed shared memory. Every CTA of the cluster takes
+//                          the same decisions from bitwise-identical sums.
+//
+// Residual in closed form. Starting from r_1 = p, the update
+// r <- max(r - q, 0) / sum(max(r - q, 0)) keeps r of the form
+// max(p - c q, 0) / s with scalars c and s:  c_1 = 0, s_1 = 1, and after a
+// rejection c' = c + s, s' = sum_t max(p(t) - c' q(t), 0) (if s' = 0, r is kept).
+// The test of a child with token x is then u < max(p(x) - c q(x), 0) / (s q(x)).
+// Only the scalar pair (c, s) travels between passes; each rejection costs one
+// pass over the vocabulary and the bonus draw one more (an inverse-CDF search).
+#include <cooperative_groups.h>
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace specv {
+
+constexpr int kAcceptThreads = 256;
+constexpr int kWalkThreads = 512;
+constexpr int kWalkCluster = 8;
+constexpr int kMaxTreeNodes = 1024;
+constexpr double kTieEps = 1e-6;    // ratio test near-tie band (absolute)
+constexpr double kBonusEps = 1e-8;  // bonus draw near-tie band (relative to the residual's total)
+
+struct ArgPartial {
+  float v;
+  int i;
+};
+struct StatPartial {
+  float m_p, m_q;
+  double s_p, s_q;
+};
+struct NodeStats {
+  float m_p, m_q;
+  double z_p, z_q;
+};
+
+// Workspace layout for spec_accept (offsets in bytes, each 256-aligned).
+struct AcceptWs {
+  size_t node_cnt, seq_cnt, partials, results, total;
+  static AcceptWs make(int batch, int total_nodes, int chunks) {
+    AcceptWs w;
+    size_t off = 0;
+    w.node_cnt = off; off = align_up(off + sizeof(unsigned) * (size_t)total_nodes, 256);
+    w.seq_cnt = off;  off = align_up(off + sizeof(unsigned) * (size_t)batch, 256);
+    w.partials = off; off = align_up(off + sizeof(StatPartial) * (size_t)total_nodes * chunks, 256);
+    w.results = off;  off = align_up(off + sizeof(NodeStats) * (size_t)total_nodes, 256);
+    w.total = off;
+    return w;
+  }
+};
+
+int accept_chunks(int total_nodes, int vocab) {
+  // about four CTAs per SM over all rows, chunks of at least 2048 logits
+  const int want = ceil_div(4 * 152, total_nodes > 0 ? total_nodes : 1);
+  const int maxc = ceil_div(vocab, 2048);
+  int c = want < maxc ? want : maxc;
+  if (c > 64) c = 64;
+  return c < 1 ? 1 : c;
+}
+
+size_t accept_ws_bytes(int batch, int total_nodes, int vocab) {
+  return AcceptWs::make(batch, total_nodes, accept_chunks(total_nodes, vocab)).total;
+}
+
+__device__ __forceinline__ void arg_better(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+__device__ __forceinline__ void warp_arg_reduce(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    arg_better(v, i, v2, i2);
+  }
+}
+
+// Chunk range [lo, hi) of chunk c (multiple of 4 elements except at the end of the row).
+__device__ __forceinline__ void chunk_range(int vocab, int chunks, int c, int& lo, int& hi) {
+  const int per = ((vocab + chunks - 1) / chunks + 3) & ~3;
+  lo = c * per;
+  hi = lo + per < vocab ? lo + per : vocab;
+  if (lo > vocab) lo = vocab;
+}
+
+// Greedy walk of one sequence by one warp: from the root, move to the first child
+// (lowest id) whose draft token equals the node's target argmax.
+__device__ void greedy_walk_warp(int b, int base, int n, const int32_t* __restrict__ parent,
+                                 const int32_t* __restrict__ tokens, const int* argmax, int path_cap,
+                                 int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                                 uint8_t* flags, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  int v = 0, L = 0, bonus = 0;
+  int32_t* prow = path + (size_t)b * path_cap;
+  int32_t* trow = out_tokens + (size_t)b * path_cap;
+  if (lane == 0) prow[0] = 0;
+  while (true) {
+    const int a = __ldcg(argmax + base + v);
+    int found = -1;
+    for (int c0 = v + 1; c0 < n; c0 += 32) {
+      const int c = c0 + lane;
+      const bool m = c < n && __ldg(parent + base + c) == v && __ldg(tokens + base + c) == a;
+      const unsigned bal = __ballot_sync(0xffffffffu, m);
+      if (bal) {
+        found = c0 + __ffs(bal) - 1;
+        break;
+      }
+    }
+    if (found < 0) {
+      bonus = a;
+      break;
+    }
+    if (L + 1 >= path_cap) {  // accepted path does not fit: truncate here
+      if (lane == 0) report(status, SPEC_ERR_CAPACITY);
+      bonus = a;
+      break;
+    }
+    ++L;
+    if (lane == 0) {
+      prow[L] = found;
+      trow[L - 1] = __ldg(tokens + base + found);
+    }
+    v = found;
+  }
+  if (lane == 0) {
+    trow[L] = bonus;
+    accept_len[b] = L;
+    if (flags != nullptr) flags[b] = 0;
+  }
+  for (int k = L + 1 + lane; k < path_cap; k += 32) {
+    prow[k] = -1;
+    trow[k] = -1;
+  }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(
+    const float* __restrict__ logits, int vocab, int chunks, const int32_t* __restrict__ qo,
+    int batch, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
+    int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+    unsigned* node_cnt, unsigned* seq_cnt, ArgPartial* partials, int* argmax, int32_t* status) {
+  const int t = blockIdx.x / chunks;
+  const int c = blockIdx.x - t * chunks;
+  int lo, hi;
+  chunk_range(vocab, chunks, c, lo, hi);
+  const float* row = logits + (size_t)t * vocab;
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  if (kVec) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int q0 = lo >> 2, q1 = hi >> 2;  // hi is a multiple of 4 when vocab is
+    int j = q0 + threadIdx.x;
+    for (; j + 3 * kAcceptThreads < q1; j += 4 * kAcceptThreads) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldcs(r4 + j + u * kAcceptThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = (j + u * kAcceptThreads) << 2;
+        arg_better(bv, bi, x[u].x, e);
+        arg_better(bv, bi, x[u].y, e + 1);
+        arg_better(bv, bi, x[u].z, e + 2);
+        arg_better(bv, bi, x[u].w, e + 3);
+      }
+    }
+    for (; j < q1; j += kAcceptThreads) {
+      const float4 x = __ldcs(r4 + j);
+      const int e = j << 2;
+      arg_better(bv, bi, x.x, e);
+      arg_better(bv, bi, x.y, e + 1);
+      arg_better(bv, bi, x.z, e + 2);
+      arg_better(bv, bi, x.w, e + 3);
+    }
+  } else {
+    for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) arg_better(bv, bi, __ldcs(row + e), e);
+  }
+  warp_arg_reduce(bv, bi);
+  __shared__ float sv[kAcceptThreads / 32];
+  __shared__ int si[kAcceptThreads / 32];
+  __shared__ bool s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kAcceptThreads / 32; ++w) arg_better(bv, bi, sv[w], si[w]);
+    partials[(size_t)t * chunks + c] = ArgPartial{bv, bi};
+    __threadfence();
+    const unsigned done = atomicAdd(node_cnt + t, 1u);
+    s_last = done == (unsigned)(chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // last CTA of row t: merge the chunk partials
+  if (warp == 0) {
+    float v = -INFINITY;
+    int i = INT_MAX;
+    for (int k = lane; k < chunks; k += 32) {
+      const ArgPartial* p = partials + (size_t)t * chunks + k;
+      arg_better(v, i, __ldcg(&p->v), __ldcg(&p->i));
+    }
+    warp_arg_reduce(v, i);
+    if (lane == 0) {
+      argmax[t] = i == INT_MAX ? 0 : i;
+      node_cnt[t] = 0;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  const int b = seq_of_row(qo, batch, t);
+  const int base = __ldg(qo + b);
+  const int n = __ldg(qo + b + 1) - base;
+  if (threadIdx.x == 0) {
+    const unsigned done = atomicAdd(seq_cnt + b, 1u);
+    s_last = done == (unsigned)(n - 1);
+    if (s_last) seq_cnt[b] = 0;
+    __threadfence();
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  greedy_walk_warp(b, base, n, parent, tokens, argmax, path_cap, accept_len, path, out_tokens, flags,
+                   status);
+}
+
+// ---------------------------------------------------------------- stochastic: statistics
+
+// Online max / compensated sum of exp((x - m) * invT) over a stream of values.
+struct OnlineExp {
+  float m = -INFINITY, s = 0.f, comp = 0.f;
+  __device__ __forceinline__ void add(float x, float invT) {
+    if (x > m) {
+      const float f = (m == -INFINITY) ? 0.f : expf((m - x) * invT);
+      s *= f;
+      comp *= f;
+      m = x;
+      kahan(1.f);
+    } else {
+      kahan(expf((x - m) * invT));
+    }
+  }
+  __device__ __forceinline__ void kahan(float e) {
+    const float y = e - comp;
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+  }
+};
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < nw; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+
+// Block-wide fp64 sum; every thread gets the same value (summed in a fixed order).
+__device__ __forceinline__ double block_sum(double v, double* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  double r = red[0];
+  for (int w = 1; w < nw; ++w) r += red[w];
+  return r;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
+    const float* __restrict__ tl, const float* __restrict__ dl, int vocab, int chunks, float invT,
+    unsigned* node_cnt, StatPartial* partials, NodeStats* stats) {
+  const int t = blockIdx.x / chunks;
+  const int c = blockIdx.x - t * chunks;
+  int lo, hi;
+  chunk_range(vocab, chunks, c, lo, hi);
+  OnlineExp ep, eq;
+  const float* rp = tl + (size_t)t * vocab;
+  const float* rq = dl + (size_t)t * vocab;
+  if (kVec) {
+    const float4* p4 = reinterpret_cast<const float4*>(rp);
+    const float4* q4 = reinterpret_cast<const float4*>(rq);
+    for (int j = (lo >> 2) + threadIdx.x; j < (hi >> 2); j += kAcceptThreads) {
+      const float4 a = __ldcs(p4 + j);
+      const float4 d = __ldcs(q4 + j);
+      ep.add(a.x, invT); ep.add(a.y, invT); ep.add(a.z, invT); ep.add(a.w, invT);
+      eq.add(d.x, invT); eq.add(d.y, invT); eq.add(d.z, invT); eq.add(d.w, invT);
+    }
+  } else {
+    for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) {
+      ep.add(__ldcs(rp + e), invT);
+      eq.add(__ldcs(rq + e), invT);
+    }
+  }
+  __shared__ float redf[kAcceptThreads / 32];
+  __shared__ double redd[kAcceptThreads / 32];
+  __shared__ bool s_last;
+  const float Mp = block_max(ep.m, redf);
+  const float Mq = block_max(eq.m, redf);
+  const double Sp = block_sum(ep.m == -INFINITY ? 0.0 : (double)ep.s * (double)expf((ep.m - Mp) * invT), redd);
+  const double Sq = block_sum(eq.m == -INFINITY ? 0.0 : (double)eq.s * (double)expf((eq.m - Mq) * invT), redd);
+  if (threadIdx.x == 0) {
+    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, Sp, Sq};
+    __threadfence();
+    s_last = atomicAdd(node_cnt + t, 1u) == (unsigned)(chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  const volatile StatPartial* vp = partials + (size_t)t * chunks;
+  float mp = -INFINITY, mq = -INFINITY;
+  for (int k = 0; k < chunks; ++k) {
+    mp = fmaxf(mp, vp[k].m_p);
+    mq = fmaxf(mq, vp[k].m_q);
+  }
+  double zp = 0.0, zq = 0.0;
+  for (int k = 0; k < chunks; ++k) {
+    if (vp[k].m_p != -INFINITY) zp += vp[k].s_p * (double)expf((vp[k].m_p - mp) * invT);
+    if (vp[k].m_q != -INFINITY) zq += vp[k].s_q * (double)expf((vp[k].m_q - mq) * invT);
+  }
+  stats[t] = NodeStats{mp, mq, zp, zq};
+  node_cnt[t] = 0;
+}
+
+// ---------------------------------------------------------------- stochastic: walk
+
+struct WalkShared {
+  double part[2][kWalkThreads / 32];  // block reduction scratch
+  double cta_sum[2];                  // this CTA's pass total (double-buffered by pass parity)
+  double scan[kWalkThreads];          // per-thread sums for the bonus search
+  unsigned kids[kMaxTreeNodes / 32];  // children bitmap of the current node
+  int found;                          // bonus token found by this CTA (-1 = none)
+  int found_flag;
+};
+
+// p(t) and q(t) in fp32 from the node statistics.
+struct RowEval {
+  const float* tl;
+  const float* dl;
+  float m_p, m_q, invT, inv_zp, inv_zq;
+  __device__ __forceinline__ float p(int t) const { return expf((__ldg(tl + t) - m_p) * invT) * inv_zp; }
+  __device__ __forceinline__ float q(int t) const { return expf((__ldg(dl + t) - m_q) * invT) * inv_zq; }
+  __device__ __forceinline__ float resid(int t, float c) const {
+    const float pt = p(t);
+    return c == 0.f ? pt : fmaxf(pt - c * q(t), 0.f);
+  }
+};
+
+// This thread's contiguous sub-range of the CTA's slice of the vocabulary.
+__device__ __forceinline__ void walk_range(int vocab, int rank, int& lo, int& hi) {
+  const int per_cta = (vocab + kWalkCluster - 1) / kWalkCluster;
+  const int c_lo = rank * per_cta;
+  const int c_hi = min(vocab, c_lo + per_cta);
+  const int n = max(0, c_hi - c_lo);
+  const int per_thr = (n + kWalkThreads - 1) / kWalkThreads;
+  lo = min(c_hi, c_lo + (int)threadIdx.x * per_thr);
+  hi = min(c_hi, lo + per_thr);
+}
+
+// Sum over the whole vocabulary (all CTAs of the cluster) of the residual with
+// coefficient c; identical bitwise in every CTA.
+__device__ double cluster_resid_sum(cg::cluster_group& cl, WalkShared& sh, const RowEval& ev, int vocab,
+                                    float c, int parity) {
+  int lo, hi;
+  walk_range(vocab, (int)cl.block_rank(), lo, hi);
+  float s = 0.f, comp = 0.f;
+  for (int t = lo; t < hi; ++t) {
+    const float y = ev.resid(t, c) - comp;
+    const float z = s + y;
+    comp = (z - s) - y;
+    s = z;
+  }
+  const double tot = block_sum((double)s, sh.part[parity]);
+  if (threadIdx.x == 0) sh.cta_sum[parity] = tot;
+  cl.sync();
+  double all = 0.0;
+  for (int r = 0; r < kWalkCluster; ++r) all += *cl.map_shared_rank(&sh.cta_sum[parity], r);
+  return all;
+}
+
+__global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThreads)
+    accept_walk_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
+                       const float* __restrict__ tl, const float* __restrict__ dl,
+                       const float* __restrict__ uniforms, float temperature, int vocab,
+                       const int32_t* __restrict__ qo, int path_cap, const NodeStats* stats,
+                       int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+                       int32_t* status) {
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ WalkShared sh;
+  const int b = blockIdx.y;
+  const int rank = (int)cl.block_rank();
+  const int base = __ldg(qo + b);
+  const int n = __ldg(qo + b + 1) - base;
+  const float invT = 1.0f / temperature;
+  const double invTd = 1.0 / (double)temperature;
+  int32_t* prow = path + (size_t)b * path_cap;
+  int32_t* trow = out_tokens + (size_t)b * path_cap;
+  const bool writer = rank == 0 && threadIdx.x == 0;
+  if (n < 1 || n > kMaxTreeNodes) {  // same answer in every CTA of the cluster: all leave here
+    if (writer) report(status, SPEC_ERR_CAPACITY);
+    return;
+  }
+  if (writer) prow[0] = 0;
+  int v = 0, L = 0, flag = 0, bonus = 0;
+  int parity = 0;
+  while (true) {
+    const NodeStats st = stats[base + v];
+    RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
+               (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
+    // children bitmap of v
+    for (int w = threadIdx.x; w < kMaxTreeNodes / 32; w += blockDim.x) sh.kids[w] = 0u;
+    __syncthreads();
+    for (int c = v + 1 + threadIdx.x; c < n; c += blockDim.x)
+      if (__ldg(parent + base + c) == v) atomicOr(&sh.kids[c >> 5], 1u << (c & 31));
+    __syncthreads();
+    double cc = 0.0, ss = 1.0;  // residual r = max(p - cc q, 0) / ss
+    int accepted = -1;
+    for (int w = (v + 1) >> 5; w < kMaxTreeNodes / 32 && accepted < 0; ++w) {
+      unsigned bits = sh.kids[w];
+      while (bits) {
+        const int c = (w << 5) + __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int x = __ldg(tokens + base + c);
+        if (x < 0 || x >= vocab) {
+          if (writer) report(status, SPEC_ERR_INDEX);
+          continue;
+        }
+        const double px = exp(((double)__ldg(ev.tl + x) - (double)st.m_p) * invTd) / st.z_p;
+        const double qx = exp(((double)__ldg(ev.dl + x) - (double)st.m_q) * invTd) / st.z_q;
+        const double u = (double)__ldg(uniforms + 2 * (size_t)(base + c));
+        const double rx = fmax(px - cc * qx, 0.0) / ss;
+        bool ok;
+        if (qx > 0.0) {
+          const double ratio = rx / qx;
+          if (fabs(u - ratio) <= kTieEps) flag |= 1;
+          ok = u < ratio;
+        } else {
+          ok = rx > 0.0;
+        }
+        if (ok) {
+          accepted = c;
+          break;
+        }
+        const double cn = cc + ss;
+        const double sn = cluster_resid_sum(cl, sh, ev, vocab, (float)cn, parity);
+        parity ^= 1;
+        if (sn > 0.0) {
+          cc = cn;
+          ss = sn;
+        }
+      }
+    }
+    __syncthreads();  // everyone done with sh.kids before the next node rebuilds it
+    if (accepted >= 0) {
+      if (L + 1 >= path_cap) {
+        if (writer) report(status, SPEC_ERR_CAPACITY);
+        accepted = -1;  // truncate: fall through to the bonus draw at v
+      } else {
+        ++L;
+        if (writer) {
+          prow[L] = accepted;
+          trow[L - 1] = __ldg(tokens + base + accepted);
+        }
+        v = accepted;
+        continue;
+      }
+    }
+    // bonus: inverse-CDF draw from r = max(p - cc q, 0) / ss with u_bonus of v
+    {
+      int lo, hi;
+      walk_range(vocab, rank, lo, hi);
+      const float cf = (float)cc;
+      float s = 0.f, comp = 0.f;
+      for (int t = lo; t < hi; ++t) {
+        const float y = ev.resid(t, cf) - comp;
+        const float z = s + y;
+        comp = (z - s) - y;
+        s = z;
+      }
+      sh.scan[threadIdx.x] = (double)s;
+      __syncthreads();
+      if (threadIdx.x == 0) {  // exclusive scan over threads (fixed order)
+        double acc = 0.0;
+        for (int k = 0; k < kWalkThreads; ++k) {
+          const double x = sh.scan[k];
+          sh.scan[k] = acc;
+          acc += x;
+        }
+        sh.cta_sum[parity] = acc;
+        sh.found = -1;
+        sh.found_flag = 0;
+      }
+      __syncthreads();
+      const double my_pre_local = sh.scan[threadIdx.x];
+      const double my_next_local = threadIdx.x + 1 < kWalkThreads ? sh.scan[threadIdx.x + 1] : sh.cta_sum[parity];
+      cl.sync();
+      double cta_pre = 0.0, total = 0.0;
+      for (int r = 0; r < kWalkCluster; ++r) {
+        const double x = *cl.map_shared_rank(&sh.cta_sum[parity], r);
+        if (r < rank) cta_pre += x;
+        total += x;
+      }
+      const double thr = (double)__ldg(uniforms + 2 * (size_t)(base + v) + 1) * total;
+      const double pre = cta_pre + my_pre_local;
+      const double nxt = cta_pre + my_next_local;
+      if (pre <= thr && thr < nxt && hi > lo) {
+        double acc = pre;
+        int tok = -1, last_pos = -1, fl = 0;
+        for (int t = lo; t < hi; ++t) {
+          const float rv = ev.resid(t, cf);
+          if (rv > 0.f) last_pos = t;
+          const double before = acc;
+          acc += (double)rv;
+          if (acc > thr) {
+            tok = t;
+            if (fabs(acc - thr) <= kBonusEps * total || fabs(before - thr) <= kBonusEps * total) fl = 2;
+            break;
+          }
+        }
+        if (tok < 0) {  // rounding put the crossing just past this range's last mass
+          tok = last_pos >= 0 ? last_pos : lo;
+          fl = 2;
+        }
+        sh.found = tok;
+        sh.found_flag = fl;
+      }
+      parity ^= 1;
+      cl.sync();
+      if (rank == 0 && threadIdx.x == 0) {
+        int tok = -1;
+        for (int r = 0; r < kWalkCluster && tok < 0; ++r) {
+          const int f = *cl.map_shared_rank(&sh.found, r);
+          if (f >= 0) {
+            tok = f;
+            flag |= *cl.map_shared_rank(&sh.found_flag, r);
+          }
+        }
+        bonus = tok < 0 ? 0 : tok;
+      }
+      cl.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+      break;
+    }
+  }
+  if (writer) {
+    trow[L] = bonus;
+    accept_len[b] = L;
+    for (int k = L + 1; k < path_cap; ++k) {
+      prow[k] = -1;
+      trow[k] = -1;
+    }
+    if (flags != nullptr) flags[b] = (uint8_t)flag;
+  }
+}
+
+int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl,
+                  const float* dl, const float* uniforms, float temperature, int vocab,
+                  const int32_t* qo, int batch, int total_nodes, int path_cap, int32_t* accept_len,
+                  int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws, int32_t* status,
+                  cudaStream_t stream) {
+  const int chunks = accept_chunks(total_nodes, vocab);
+  const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  unsigned* node_cnt = reinterpret_cast<unsigned*>(wb + w.node_cnt);
+  unsigned* seq_cnt = reinterpret_cast<unsigned*>(wb + w.seq_cnt);
+  const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
+                   (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
+  const dim3 grid((unsigned)(total_nodes * chunks));
+  if (mode == SPEC_GREEDY) {
+    ArgPartial* part = reinterpret_cast<ArgPartial*>(wb + w.partials);
+    int* am = reinterpret_cast<int*>(wb + w.results);
+    if (vec)
+      accept_argmax_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(
+          tl, vocab, chunks, qo, batch, parent, tokens, path_cap, accept_len, path, out_tokens, flags,
+          node_cnt, seq_cnt, part, am, status);
+    else
+      accept_argmax_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(
+          tl, vocab, chunks, qo, batch, parent, tokens, path_cap, accept_len, path, out_tokens, flags,
+          node_cnt, seq_cnt, part, am, status);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  StatPartial* part = reinterpret_cast<StatPartial*>(wb + w.partials);
+  NodeStats* st = reinterpret_cast<NodeStats*>(wb + w.results);
+  const float invT = 1.0f / temperature;
+  if (vec)
+    accept_stats_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, node_cnt, part, st);
+  else
+    accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, node_cnt, part, st);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  accept_walk_kernel<<<dim3(kWalkCluster, batch), kWalkThreads, 0, stream>>>(
+      parent, tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, st, accept_len, path, out_tokens,
+      flags, status);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace specv

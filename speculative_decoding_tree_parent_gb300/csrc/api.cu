@@ -1,0 +1,176 @@
+// C ABI of libspecverify: argument checks on the host, then kernel dispatch.
+// Every entry point is asynchronous on the caller's stream and allocates nothing.
+#include "attn_common.cuh"
+
+namespace specv {
+int launch_tree_mask(const int32_t* parent, const int32_t* qo, int batch, int total_nodes, int max_nodes,
+                     uint64_t* mask, int32_t* depth, int32_t* status, cudaStream_t stream);
+int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
+                     const int32_t* accept_len, const int32_t* qo, const int32_t* page_table, int max_pages,
+                     int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
+                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream);
+int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl, const float* dl,
+                  const float* uniforms, float temperature, int vocab, const int32_t* qo, int batch,
+                  int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                  uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream);
+size_t accept_ws_bytes(int batch, int total_nodes, int vocab);
+int launch_attn_simt(int dtype, const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
+                     const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
+                     const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
+                     int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
+                     void* ws, int32_t* status, cudaStream_t stream);
+bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max_nodes);
+int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
+                   const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
+                   const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
+                   int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
+                   void* ws, int32_t* status, cudaStream_t stream);
+
+constexpr int kMaxNodes = 1024;
+
+static size_t attn_ws_bytes(int batch, int total_nodes, int max_nodes, int hq, int hkv, int d, int max_prefix) {
+  const int rows = total_nodes * hq;
+  const int s1 = attn_splits_simt(batch, max_nodes, hq, hkv, max_prefix);
+  const int s2 = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
+  const size_t b1 = s1 > 1 ? AttnWs::bytes(s1, rows, d) : 0;
+  const size_t b2 = s2 > 1 ? AttnWs::bytes(s2, rows, d) : 0;
+  return b1 > b2 ? b1 : b2;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace specv
+
+using namespace specv;
+
+extern "C" {
+
+int spec_version(void) { return 100; }
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_ARG: return "invalid argument (null pointer or bad size)";
+    case SPEC_ERR_PARENT: return "parent array is not a tree (root must be -1, 0 <= parent[i] < i)";
+    case SPEC_ERR_PAGE: return "page table entry outside the KV pool";
+    case SPEC_ERR_CAPACITY: return "capacity exceeded (nodes, pages or path slots)";
+    case SPEC_ERR_WORKSPACE: return "workspace smaller than spec_workspace_size()";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported dtype / head dim / shape";
+    case SPEC_ERR_CUDA: return "CUDA runtime or launch error";
+    case SPEC_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case SPEC_ERR_INDEX: return "token or node index out of range";
+    default: return "unknown status";
+  }
+}
+
+size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, int hq, int hkv, int d,
+                           int max_prefix, int vocab) {
+  if (batch < 0 || total_nodes < 0) return 0;
+  switch (op) {
+    case SPEC_OP_ATTN:
+      if (hq <= 0 || hkv <= 0 || hq % hkv || d <= 0 || max_nodes <= 0 || max_prefix < 0) return 0;
+      return attn_ws_bytes(batch, total_nodes, max_nodes, hq, hkv, d, max_prefix);
+    case SPEC_OP_ACCEPT:
+      if (vocab <= 0) return 0;
+      return accept_ws_bytes(batch, total_nodes, vocab);
+    default:
+      return 0;
+  }
+}
+
+int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, int page_size, int max_prefix,
+                   int* splits, int* tensor_cores) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes || max_prefix < 0 || hq <= 0 || hkv <= 0 ||
+      hq % hkv != 0 || !splits || !tensor_cores)
+    return SPEC_ERR_ARG;
+  if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
+  if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+  const bool tc = attn_tc_supported(dtype, hq, hkv, d, page_size, max_nodes);
+  *tensor_cores = tc ? 1 : 0;
+  *splits = tc ? attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix)
+               : attn_splits_simt(batch, max_nodes, hq, hkv, max_prefix);
+  return SPEC_OK;
+}
+
+int spec_build_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch, int total_nodes,
+                         int max_nodes, uint64_t* mask, int32_t* depth, int32_t* dev_status, void* stream) {
+  if (batch < 0 || total_nodes < 0 || max_nodes < 1 || max_nodes > kMaxNodes) return SPEC_ERR_ARG;
+  if (batch == 0 || total_nodes == 0) return SPEC_OK;
+  if (!parent || !qo_indptr || !mask) return SPEC_ERR_ARG;
+  return launch_tree_mask(parent, qo_indptr, batch, total_nodes, max_nodes, mask, depth, dev_status,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                          int page_size, const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                          int max_prefix, const void* k_tree, const void* v_tree, const uint64_t* mask,
+                          const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int hq, int hkv,
+                          int d, float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                          int32_t* dev_status, void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (batch < 0 || total_nodes < 0 || max_nodes < 1 || max_nodes > kMaxNodes || max_prefix < 0 ||
+      num_pages < 0 || max_pages < 0)
+    return SPEC_ERR_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
+  if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
+  if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+  if (batch == 0 || total_nodes == 0) return SPEC_OK;
+  if (!q || !k_tree || !v_tree || !mask || !qo_indptr || !prefix_len || !out) return SPEC_ERR_ARG;
+  if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
+    return SPEC_ERR_ARG;
+  if ((long)max_pages * page_size < max_prefix) return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
+  if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (attn_tc_supported(dtype, hq, hkv, d, page_size, max_nodes) && aligned16(q) && aligned16(k_pool) &&
+      aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree))
+    return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
+                          k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale,
+                          out, lse, ws, dev_status, st);
+  return launch_attn_simt(dtype, q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len,
+                          max_prefix, k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d,
+                          sm_scale, out, lse, ws, dev_status, st);
+}
+
+int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws,
+                size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
+  if (batch < 0 || total_nodes < 0 || vocab <= 0 || path_cap < 1 || max_nodes < 1 || max_nodes > kMaxNodes)
+    return SPEC_ERR_ARG;
+  if (batch == 0) return SPEC_OK;
+  if (total_nodes < batch) return SPEC_ERR_ARG;  // every sequence has at least its root
+  if (!parent || !draft_tokens || !target_logits || !qo_indptr || !accept_len || !path || !out_tokens)
+    return SPEC_ERR_ARG;
+  if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_ACCEPT, batch, total_nodes, max_nodes, 0, 0, 0, 0, vocab);
+  if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return SPEC_ERR_WORKSPACE;
+  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
+                       dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
+                   const int32_t* accept_len, const int32_t* qo_indptr, const int32_t* page_table, int max_pages,
+                   int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
+                   void* v_pool, int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (batch < 0 || total_nodes < 0 || path_cap < 1 || max_pages < 0 || num_pages < 0 || page_size <= 0 ||
+      hkv <= 0 || d <= 0)
+    return SPEC_ERR_ARG;
+  const int elem = dtype == SPEC_F32 ? 4 : 2;
+  if ((d * elem) % 16 != 0) return SPEC_ERR_UNSUPPORTED;
+  if (batch == 0) return SPEC_OK;
+  if (!k_tree || !v_tree || !path || !accept_len || !qo_indptr || !page_table || !prefix_len || !k_pool || !v_pool)
+    return SPEC_ERR_ARG;
+  if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_pool) || !aligned16(v_pool)) return SPEC_ERR_ARG;
+  return launch_kv_commit(elem, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
+                          num_pages, page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
+                          static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// Shared device/host helpers of libspecverify (no kernel lives here).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace specv {
+
+// First-error-wins report into the caller's status word (nullable).
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// Sequence that owns global node row t: largest b with qo_indptr[b] <= t.
+__device__ __forceinline__ int seq_of_row(const int32_t* __restrict__ qo, int batch, int t) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(qo + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+}  // namespace specv
+
+// Host-side launch check used by the entry points.
+#define SPECV_LAUNCH_CHECK()                              \
+  do {                                                    \
+    cudaError_t e__ = cudaGetLastError();                 \
+    if (e__ != cudaSuccess) return SPEC_ERR_CUDA;         \
+  } while (0)
