@@ -125,7 +125,7 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
   if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (attn_tc_supported(dtype, hq, hkv, d, page_size, max_nodes) && aligned16(q) && aligned16(k_pool) &&
-      aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree))
+      aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree) && aligned16(out))
     return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                           k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale,
                           out, lse, ws, dev_status, st);
