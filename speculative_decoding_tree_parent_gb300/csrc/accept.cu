@@ -79,13 +79,14 @@ struct AcceptWs {
   }
 };
 
+// One CTA streams kChunk logits of one row: 8 float4 per thread, all loads issued
+// before any is used, so a CTA costs one memory round trip.
+constexpr int kVecPerThread = 8;
+constexpr int kChunk = kAcceptThreads * kVecPerThread * 4;
+
 int accept_chunks(int total_nodes, int vocab) {
-  // about four CTAs per SM over all rows, chunks of at least 2048 logits
-  const int want = ceil_div(4 * 152, total_nodes > 0 ? total_nodes : 1);
-  const int maxc = ceil_div(vocab, 2048);
-  int c = want < maxc ? want : maxc;
-  if (c > 64) c = 64;
-  return c < 1 ? 1 : c;
+  (void)total_nodes;
+  return ceil_div(vocab, kChunk);
 }
 
 size_t accept_ws_bytes(int batch, int total_nodes, int vocab) {
@@ -108,12 +109,10 @@ __device__ __forceinline__ void warp_arg_reduce(float& v, int& i) {
   }
 }
 
-// Chunk range [lo, hi) of chunk c (multiple of 4 elements except at the end of the row).
-__device__ __forceinline__ void chunk_range(int vocab, int chunks, int c, int& lo, int& hi) {
-  const int per = ((vocab + chunks - 1) / chunks + 3) & ~3;
-  lo = c * per;
-  hi = lo + per < vocab ? lo + per : vocab;
-  if (lo > vocab) lo = vocab;
+// Chunk range [lo, hi) of chunk c (lo a multiple of 4).
+__device__ __forceinline__ void chunk_range(int vocab, int c, int& lo, int& hi) {
+  lo = c * kChunk;
+  hi = lo + kChunk < vocab ? lo + kChunk : vocab;
 }
 
 // Greedy walk of one sequence by one warp: from the root, move to the first child
@@ -175,34 +174,29 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(
   const int t = blockIdx.x / chunks;
   const int c = blockIdx.x - t * chunks;
   int lo, hi;
-  chunk_range(vocab, chunks, c, lo, hi);
+
+  chunk_range(vocab, c, lo, hi);
   const float* row = logits + (size_t)t * vocab;
   float bv = -INFINITY;
   int bi = INT_MAX;
   if (kVec) {
     const float4* r4 = reinterpret_cast<const float4*>(row);
     const int q0 = lo >> 2, q1 = hi >> 2;  // hi is a multiple of 4 when vocab is
-    int j = q0 + threadIdx.x;
-    for (; j + 3 * kAcceptThreads < q1; j += 4 * kAcceptThreads) {
-      float4 x[4];
+    float4 x[kVecPerThread];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = __ldcs(r4 + j + u * kAcceptThreads);
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int j = q0 + threadIdx.x + u * kAcceptThreads;
+      x[u] = j < q1 ? __ldcs(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = (j + u * kAcceptThreads) << 2;
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int e = (q0 + threadIdx.x + u * kAcceptThreads) << 2;
+      if (e < hi) {
         arg_better(bv, bi, x[u].x, e);
         arg_better(bv, bi, x[u].y, e + 1);
         arg_better(bv, bi, x[u].z, e + 2);
         arg_better(bv, bi, x[u].w, e + 3);
       }
-    }
-    for (; j < q1; j += kAcceptThreads) {
-      const float4 x = __ldcs(r4 + j);
-      const int e = j << 2;
-      arg_better(bv, bi, x.x, e);
-      arg_better(bv, bi, x.y, e + 1);
-      arg_better(bv, bi, x.z, e + 2);
-      arg_better(bv, bi, x.w, e + 3);
     }
   } else {
     for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) arg_better(bv, bi, __ldcs(row + e), e);
@@ -220,6 +214,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(
   if (threadIdx.x == 0) {
     for (int w = 1; w < kAcceptThreads / 32; ++w) arg_better(bv, bi, sv[w], si[w]);
     partials[(size_t)t * chunks + c] = ArgPartial{bv, bi};
+    pdl_trigger();  // this CTA has streamed its chunk: the next kernel may be scheduled
     __threadfence();
     const unsigned done = atomicAdd(node_cnt + t, 1u);
     s_last = done == (unsigned)(chunks - 1);
@@ -313,18 +308,30 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
   const int t = blockIdx.x / chunks;
   const int c = blockIdx.x - t * chunks;
   int lo, hi;
-  chunk_range(vocab, chunks, c, lo, hi);
+
+  chunk_range(vocab, c, lo, hi);
   OnlineExp ep, eq;
   const float* rp = tl + (size_t)t * vocab;
   const float* rq = dl + (size_t)t * vocab;
   if (kVec) {
     const float4* p4 = reinterpret_cast<const float4*>(rp);
     const float4* q4 = reinterpret_cast<const float4*>(rq);
-    for (int j = (lo >> 2) + threadIdx.x; j < (hi >> 2); j += kAcceptThreads) {
-      const float4 a = __ldcs(p4 + j);
-      const float4 d = __ldcs(q4 + j);
-      ep.add(a.x, invT); ep.add(a.y, invT); ep.add(a.z, invT); ep.add(a.w, invT);
-      eq.add(d.x, invT); eq.add(d.y, invT); eq.add(d.z, invT); eq.add(d.w, invT);
+    const int q0 = lo >> 2, q1 = hi >> 2;
+    float4 a[kVecPerThread], d[kVecPerThread];
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int j = q0 + threadIdx.x + u * kAcceptThreads;
+      if (j < q1) {
+        a[u] = __ldcs(p4 + j);
+        d[u] = __ldcs(q4 + j);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      if (q0 + threadIdx.x + u * kAcceptThreads < q1) {
+        ep.add(a[u].x, invT); ep.add(a[u].y, invT); ep.add(a[u].z, invT); ep.add(a[u].w, invT);
+        eq.add(d[u].x, invT); eq.add(d[u].y, invT); eq.add(d[u].z, invT); eq.add(d[u].w, invT);
+      }
     }
   } else {
     for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) {
@@ -341,6 +348,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
   const double Sq = block_sum(eq.m == -INFINITY ? 0.0 : (double)eq.s * (double)expf((eq.m - Mq) * invT), redd);
   if (threadIdx.x == 0) {
     partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, Sp, Sq};
+    pdl_trigger();
     __threadfence();
     s_last = atomicAdd(node_cnt + t, 1u) == (unsigned)(chunks - 1);
   }
@@ -426,6 +434,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
                        int32_t* status) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ WalkShared sh;
+  pdl_wait();  // the statistics kernel's results
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int base = __ldg(qo + b);
@@ -625,9 +634,10 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   else
     accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, node_cnt, part, st);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  accept_walk_kernel<<<dim3(kWalkCluster, batch), kWalkThreads, 0, stream>>>(
-      parent, tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, st, accept_len, path, out_tokens,
-      flags, status);
+  if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), 0, stream, parent, tokens, tl,
+                 dl, uniforms, temperature, vocab, qo, path_cap, (const NodeStats*)st, accept_len, path, out_tokens,
+                 flags, status) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

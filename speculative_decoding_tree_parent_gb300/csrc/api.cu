@@ -20,6 +20,7 @@ int launch_attn_simt(int dtype, const void* q, const void* k_pool, const void* v
                      int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
                      void* ws, int32_t* status, cudaStream_t stream);
 bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max_nodes);
+size_t attn_tc_ws_bytes(int batch, int max_nodes, int hq, int hkv, int max_prefix);
 int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                    const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
@@ -31,9 +32,8 @@ constexpr int kMaxNodes = 1024;
 static size_t attn_ws_bytes(int batch, int total_nodes, int max_nodes, int hq, int hkv, int d, int max_prefix) {
   const int rows = total_nodes * hq;
   const int s1 = attn_splits_simt(batch, max_nodes, hq, hkv, max_prefix);
-  const int s2 = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
   const size_t b1 = s1 > 1 ? AttnWs::bytes(s1, rows, d) : 0;
-  const size_t b2 = s2 > 1 ? AttnWs::bytes(s2, rows, d) : 0;
+  const size_t b2 = d == 128 ? attn_tc_ws_bytes(batch, max_nodes, hq, hkv, max_prefix) : 0;
   return b1 > b2 ? b1 : b2;
 }
 

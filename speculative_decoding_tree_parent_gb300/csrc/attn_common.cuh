@@ -4,8 +4,9 @@
 // Key space of sequence b: blocks of kb keys; first ceil(P_b / kb) prefix blocks
 // (slots read through the page table, never masked; the last one is cut at P_b),
 // then ceil(N_b / kb) tree blocks (tree K/V, filtered by the ancestor mask bits).
-// Split s of S takes a contiguous run of that combined block list, so the tree
-// blocks fall in the last split(s) and every split gets the same amount of work.
+// Split s of S takes the contiguous run [s*total/S, (s+1)*total/S) of that combined
+// block list, so the tree blocks fall in the last split(s) and split sizes differ by
+// at most one block.
 // ("Accelerating Sonar through speculation", EAGLE section: a custom mask over the
 // whole sequence is what slows attention, so only tree blocks are masked.)
 #pragma once
@@ -23,9 +24,8 @@ __device__ __forceinline__ SplitRange split_range(int P, int N, int kb, int spli
   SplitRange r;
   r.n_prefix_blocks = (P + kb - 1) / kb;
   const int total = r.n_prefix_blocks + (N + kb - 1) / kb;
-  const int per = (total + splits - 1) / splits;
-  r.blk_lo = min(total, s * per);
-  r.blk_hi = min(total, r.blk_lo + per);
+  r.blk_lo = (int)((long)s * total / splits);        // sizes differ by at most one block
+  r.blk_hi = (int)((long)(s + 1) * total / splits);
   return r;
 }
 

@@ -21,10 +21,14 @@
 //   warps 2-5  softmax, one thread per query row (its TMEM lane): S row -> max /
 //              exp2 / row sum in registers, P row -> bf16 in shared memory
 //              (128-byte swizzle), O rescale in TMEM only when the running max
-//              grows by more than 2^8; finally O / l to global memory (or the
-//              unnormalised split partial for the LSE merge).
+//              grows by more than 2^8; finally O / l to global memory.
 // S is double-buffered in TMEM (2 x 64 columns) next to O (128 columns), so QK of
 // block j+1 runs while the softmax of block j does. Every wait is bounded.
+// When the keys are split (a single short sequence cannot fill 152 SMs otherwise),
+// the launch is cooperative: the S split CTAs of one (sequence, KV head, M-tile) group
+// publish unnormalised partials (coalesced, L2-resident), meet at a bounded
+// arrival counter, and each merges a slice of the group's rows by log-sum-exp — the
+// merge needs no second kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -65,7 +69,9 @@ struct TcParams {
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
-  AttnWs ws;
+  float4* part_o;      // split partials [group][S][32 chunks][128 rows] (unnormalised O)
+  float2* part_ml;     // [group][S][128 rows] (running max in log2 units, row sum)
+  unsigned* counters;  // [group][2] arrivals / departures (zero between calls)
   int32_t* status;
 };
 
@@ -88,6 +94,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* ptr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
@@ -106,7 +124,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int npt = kTcRows / G;  // tree nodes per M-tile
   const int node0 = mt * npt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (node0 >= N) return;  // whole CTA: this M-tile is past the sequence's tree
+  // the two exits below are taken by every split CTA of a group alike (they depend on b, g, mt)
+  if (node0 >= N) return;  // this M-tile is past the sequence's tree
   if (N > p.mask_words * 64 || P < 0 || P > p.max_pages * 16) {
     if (threadIdx.x == 0 && split == 0) report(p.status, SPEC_ERR_CAPACITY);
     return;
@@ -121,275 +140,386 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int head = g * G + (row - (row / G) * G);
   const bool row_valid = node_l < N;
   const size_t orow = (size_t)(base + node_l) * p.hq + head;
+  const int grp = mt + gridDim.y * bg;  // (sequence, KV head, M-tile) group of the key splits
 
-  if (nb == 0) {  // empty key split: an empty partial (only possible when splits > 1)
-    if (warp >= 2 && row_valid) {
-      float* dst = p.ws.o + ((size_t)split * p.total_rows + orow) * kTcD;
-      for (int d = 0; d < kTcD; d += 4) *reinterpret_cast<float4*>(dst + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-      p.ws.ml[(size_t)split * p.total_rows + orow] = make_float2(-INFINITY, 0.f);
-    }
-    return;
-  }
+  if (nb > 0) {
+    const uint32_t bar_q = tc::smem_u32(&bars.q_full);
+    const uint32_t bar_pv = tc::smem_u32(&bars.pv_done);
+    const uint32_t bar_fin = tc::smem_u32(&bars.mma_fin);
+    auto bar_kvf = [&](int s) { return tc::smem_u32(&bars.kv_full[s]); };
+    auto bar_kve = [&](int s) { return tc::smem_u32(&bars.kv_empty[s]); };
+    auto bar_sf = [&](int s) { return tc::smem_u32(&bars.s_full[s]); };
+    auto bar_pf = [&](int s) { return tc::smem_u32(&bars.p_full[s]); };
+    volatile int* abort = &bars.abort;
 
-  const uint32_t bar_q = tc::smem_u32(&bars.q_full);
-  const uint32_t bar_pv = tc::smem_u32(&bars.pv_done);
-  const uint32_t bar_fin = tc::smem_u32(&bars.mma_fin);
-  auto bar_kvf = [&](int s) { return tc::smem_u32(&bars.kv_full[s]); };
-  auto bar_kve = [&](int s) { return tc::smem_u32(&bars.kv_empty[s]); };
-  auto bar_sf = [&](int s) { return tc::smem_u32(&bars.s_full[s]); };
-  auto bar_pf = [&](int s) { return tc::smem_u32(&bars.p_full[s]); };
-  volatile int* abort = &bars.abort;
-
-  if (threadIdx.x == 0) {
-    tc::mbar_init(bar_q, 1);
-    for (int s = 0; s < kTcStages; ++s) {
-      tc::mbar_init(bar_kvf(s), 1);
-      tc::mbar_init(bar_kve(s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(bar_sf(s), 1);
-      tc::mbar_init(bar_pf(s), 128);
-    }
-    tc::mbar_init(bar_pv, 1);
-    tc::mbar_init(bar_fin, 1);
-    bars.abort = 0;
-    tc::mbar_fence_init();
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(&bars.tmem_base), kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tbase = bars.tmem_base;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    int issued = 0;
-    if (lane == 0) {
-      tc::prefetch_tmap(&tm_q);
-      tc::prefetch_tmap(&tm_kp);
-      tc::prefetch_tmap(&tm_vp);
-      tc::prefetch_tmap(&tm_kt);
-      tc::prefetch_tmap(&tm_vt);
-      tc::mbar_arrive_expect_tx(bar_q, 2 * kQSlab);
-      tc::tma_load_3d(s_base + kOffQ, &tm_q, bar_q, 0, g * G, base + node0);
-      tc::tma_load_3d(s_base + kOffQ + kQSlab, &tm_q, bar_q, 64, g * G, base + node0);
-    }
-    for (int j = 0; j < nb; ++j) {
-      const int st = j % kTcStages;
-      if (!warp_wait(bar_kve(st), ((j / kTcStages) & 1) ^ 1, abort)) {
-        if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
-        break;
+    // Page ids of the producer's next 8 blocks, one per lane (lane l: block 8k + l/4,
+    // page l%4), fetched a batch ahead so the page-table latency is paid once per 8 blocks.
+    // Pages past the prefix (and invalid ids, reported) become the out-of-range id
+    // num_pages, which TMA reads as zeros.
+    auto fetch_pages = [&](int k) -> int {
+      const int blk = sr.blk_lo + 8 * k + (lane >> 2);
+      const int lp = blk * 4 + (lane & 3);
+      int page = p.num_pages;
+      if (blk < sr.blk_hi && blk < npb && lp * 16 < P) {
+        const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + lp);
+        if (pg >= 0 && pg < p.num_pages) page = pg;
+        else report(p.status, SPEC_ERR_PAGE);
       }
+      return page;
+    };
+    int pg_cur = 0, pg_nxt = 0;
+
+    // K/V block j into ring stage j % kTcStages (the warp's lanes each issue one copy);
+    // called for j = 0, 1, 2, ... in order by the whole producer warp
+    auto load_block = [&](int j) {
+      const int st = j % kTcStages;
       const uint32_t dst0 = s_base + kOffKV + st * kStageBytes;
       const int blk = sr.blk_lo + j;
+      if ((j & 7) == 0 && j > 0) {
+        pg_cur = pg_nxt;
+        pg_nxt = fetch_pages((j >> 3) + 1);
+      }
+      const int page_here = __shfl_sync(0xffffffffu, pg_cur, ((j & 7) << 2) + ((lane >> 2) & 3));
       if (lane == 0) tc::mbar_arrive_expect_tx(bar_kvf(st), kStageBytes);
       __syncwarp();
       if (blk < npb) {
         if (lane < 16) {
           const int pp = lane >> 2, which = lane & 3;
-          const int lp = blk * 4 + pp;
-          int page = p.num_pages;  // out of range: TMA fills zeros
-          if (lp * 16 < P) {
-            const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + lp);
-            if (pg >= 0 && pg < p.num_pages) page = pg;
-            else report(p.status, SPEC_ERR_PAGE);
-          }
+          const int page = page_here;
           const int slab = which & 1, isv = which >> 1;
           const uint32_t dst = dst0 + isv * 2 * kKVSlab + slab * kKVSlab + pp * 2048;
           tc::tma_load_4d(dst, isv ? &tm_vp : &tm_kp, bar_kvf(st), slab * 64, 0, g, page);
         }
-      } else {
-        if (lane < 4) {
-          const int tb = blk - npb;
-          const int slab = lane & 1, isv = lane >> 1;
-          const uint32_t dst = dst0 + isv * 2 * kKVSlab + slab * kKVSlab;
-          tc::tma_load_3d(dst, isv ? &tm_vt : &tm_kt, bar_kvf(st), slab * 64, g, base + tb * 64);
-        }
+      } else if (lane < 4) {
+        const int tb = blk - npb;
+        const int slab = lane & 1, isv = lane >> 1;
+        const uint32_t dst = dst0 + isv * 2 * kKVSlab + slab * kKVSlab;
+        tc::tma_load_3d(dst, isv ? &tm_vt : &tm_kt, bar_kvf(st), slab * 64, g, base + tb * 64);
       }
-      issued = j + 1;
-    }
-    // leave no copy in flight: the last stages issued must have landed
-    if (lane == 0 && *abort) {
-      int zero = 0;
-      for (int j = max(0, issued - kTcStages); j < issued; ++j)
-        tc::mbar_wait(bar_kvf(j % kTcStages), (j / kTcStages) & 1, &zero, kWaitLimit);
-      tc::mbar_wait(bar_q, 0, &zero, kWaitLimit);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t t_s[2] = {tbase, tbase + 64};
-      const uint32_t t_o = tbase + 128;
-      auto pv = [&](int i) -> bool {
-        if (!tc::mbar_wait(bar_pf(i & 1), (i >> 1) & 1, abort, kWaitLimit)) return false;
-        tc::fence_after_sync();
-        const uint32_t pbuf = s_base + kOffP + (i & 1) * kPBuf;
-        const uint32_t vbuf = s_base + kOffKV + (i % kTcStages) * kStageBytes + 2 * kKVSlab;
-#pragma unroll
-        for (int k = 0; k < kTcKeys / 16; ++k) {
-          const uint64_t a = tc::sdesc_sw128(pbuf + k * 32, 16, 1024);
-          const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
-          tc::mma_bf16(t_o, a, bdesc, kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
+    };
+
+    const int first = nb < kTcStages ? nb : kTcStages;
+    if (warp == 0) {
+      // barriers, then the first loads at once: their latency overlaps the TMEM allocation
+      if (lane == 0) {
+        tc::mbar_init(bar_q, 1);
+        for (int s = 0; s < kTcStages; ++s) {
+          tc::mbar_init(bar_kvf(s), 1);
+          tc::mbar_init(bar_kve(s), 1);
         }
-        tc::mma_commit(bar_kve(i % kTcStages));
-        tc::mma_commit(bar_pv);
-        return true;
-      };
-      bool ok = tc::mbar_wait(bar_q, 0, abort, kWaitLimit);
-      int j = 0;
-      for (; ok && j < nb; ++j) {
-        const int st = j % kTcStages;
-        if (!tc::mbar_wait(bar_kvf(st), (j / kTcStages) & 1, abort, kWaitLimit)) {
+        for (int s = 0; s < 2; ++s) {
+          tc::mbar_init(bar_sf(s), 1);
+          tc::mbar_init(bar_pf(s), 128);
+        }
+        tc::mbar_init(bar_pv, 1);
+        tc::mbar_init(bar_fin, 1);
+        bars.abort = 0;
+        tc::mbar_fence_init();
+        tc::mbar_arrive_expect_tx(bar_q, 2 * kQSlab);
+        tc::tma_load_3d(s_base + kOffQ, &tm_q, bar_q, 0, g * G, base + node0);
+        tc::tma_load_3d(s_base + kOffQ + kQSlab, &tm_q, bar_q, 64, g * G, base + node0);
+      }
+      __syncwarp();
+      pg_cur = fetch_pages(0);
+      pg_nxt = fetch_pages(1);
+      for (int j = 0; j < first; ++j) load_block(j);
+    } else if (warp == 1) {
+      tc::tmem_alloc(tc::smem_u32(&bars.tmem_base), kTmemCols);
+      tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = bars.tmem_base;
+
+    if (warp == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int issued = first;
+      for (int j = first; j < nb; ++j) {
+        if (!warp_wait(bar_kve(j % kTcStages), ((j / kTcStages) & 1) ^ 1, abort)) {
+          if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
+          break;
+        }
+        load_block(j);
+        issued = j + 1;
+      }
+      // leave no copy in flight: the last stages issued must have landed
+      if (lane == 0 && *abort) {
+        int zero = 0;
+        for (int j = max(0, issued - kTcStages); j < issued; ++j)
+          tc::mbar_wait(bar_kvf(j % kTcStages), (j / kTcStages) & 1, &zero, kWaitLimit);
+        tc::mbar_wait(bar_q, 0, &zero, kWaitLimit);
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        const uint32_t t_s[2] = {tbase, tbase + 64};
+        const uint32_t t_o = tbase + 128;
+        auto pv = [&](int i) -> bool {
+          if (!tc::mbar_wait(bar_pf(i & 1), (i >> 1) & 1, abort, kWaitLimit)) return false;
+          tc::fence_after_sync();
+          const uint32_t pbuf = s_base + kOffP + (i & 1) * kPBuf;
+          const uint32_t vbuf = s_base + kOffKV + (i % kTcStages) * kStageBytes + 2 * kKVSlab;
+#pragma unroll
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint64_t a = tc::sdesc_sw128(pbuf + k * 32, 16, 1024);
+            const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
+            tc::mma_bf16(t_o, a, bdesc, kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(bar_kve(i % kTcStages));
+          tc::mma_commit(bar_pv);
+          return true;
+        };
+        bool ok = tc::mbar_wait(bar_q, 0, abort, kWaitLimit);
+        for (int j = 0; ok && j < nb; ++j) {
+          const int st = j % kTcStages;
+          if (!tc::mbar_wait(bar_kvf(st), (j / kTcStages) & 1, abort, kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t kbuf = s_base + kOffKV + st * kStageBytes;
+#pragma unroll
+          for (int k = 0; k < kTcD / 16; ++k) {
+            const uint64_t a = tc::sdesc_sw128(s_base + kOffQ + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
+            const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
+            tc::mma_bf16(t_s[j & 1], a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar_sf(j & 1));
+          if (j >= 1 && !pv(j - 1)) ok = false;
+        }
+        if (ok) ok = pv(nb - 1);
+        if (!ok) report(p.status, SPEC_ERR_TIMEOUT);
+        // every MMA issued has completed before TMEM is released
+        tc::mma_commit(bar_fin);
+        int zero = 0;
+        tc::mbar_wait(bar_fin, 0, &zero, kWaitLimit);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------------- softmax warps
+      const uint32_t t_lane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
+      const float sl2 = p.scale_log2;
+      float m_run = -INFINITY, l = 0.f;
+      bool ok = true;
+      bool mask_ready = false;
+      for (int j = 0; j < nb; ++j) {
+        if (!warp_wait(bar_sf(j & 1), (j >> 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t kbuf = s_base + kOffKV + st * kStageBytes;
+        float sv[kTcKeys];
+        tc::tmem_ld32(t_lane + (j & 1) * 64, sv);
+        tc::tmem_ld32(t_lane + (j & 1) * 64 + 32, sv + 32);
+        tc::tmem_wait_ld();
+        const int blk = sr.blk_lo + j;
+        if (blk < npb) {
+          const int nvalid = P - blk * kTcKeys;  // prefix: a length bound, never a mask
+          if (nvalid < kTcKeys) {
 #pragma unroll
-        for (int k = 0; k < kTcD / 16; ++k) {
-          const uint64_t a = tc::sdesc_sw128(s_base + kOffQ + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
-          const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16(t_s[j & 1], a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
+            for (int c = 0; c < kTcKeys; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
+          }
+        } else {  // tree block: ancestor bits
+          if (!mask_ready) {  // the mask comes from the kernel launched just before this one
+            pdl_wait();
+            mask_ready = true;
+          }
+          const uint64_t bits = row_valid ? mrow[blk - npb] : 0ull;
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) sv[c] = ((bits >> c) & 1ull) ? sv[c] : -INFINITY;
         }
-        tc::mma_commit(bar_sf(j & 1));
-        if (j >= 1 && !pv(j - 1)) {
-          ok = false;
-          break;
+        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+        for (int c = 4; c < kTcKeys; c += 4) {
+          mx0 = fmaxf(mx0, sv[c]);
+          mx1 = fmaxf(mx1, sv[c + 1]);
+          mx2 = fmaxf(mx2, sv[c + 2]);
+          mx3 = fmaxf(mx3, sv[c + 3]);
         }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;  // sm_scale > 0
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > -INFINITY && (m_run == -INFINITY || mx > m_run + kRescaleThr)) {
+          alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - mx);
+          m_run = mx;
+          rescale = j > 0;
+        }
+        const float negm = m_run == -INFINITY ? 0.f : -m_run;  // all scores are -inf then
+        uint32_t packed[kTcKeys / 2];
+        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTcKeys; c += 4) {
+          const float p0 = ex2_approx(fmaf(sv[c], sl2, negm));
+          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, negm));
+          const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, negm));
+          const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, negm));
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
+          packed[c >> 1] = pack_bf16x2(p0, p1);
+          packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+        }
+        l = l * alpha + ((r0 + r1) + (r2 + r3));
+        if (j >= 1) {  // PV of the previous block done: O is stable and P[j%2] is free
+          if (!warp_wait(bar_pv, (j - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+        }
+        if (__any_sync(0xffffffffu, rescale)) {  // tcgen05.ld/st are warp-collective
+#pragma unroll
+          for (int ch = 0; ch < kTcD / 32; ++ch) {
+            float o[32];
+            tc::tmem_ld32(t_lane + 128 + ch * 32, o);
+            tc::tmem_wait_ld();
+            const float f = rescale ? alpha : 1.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tc::tmem_st32(t_lane + 128 + ch * 32, o);
+          }
+          tc::tmem_wait_st();
+        }
+        uint8_t* prow = smem + kOffP + (j & 1) * kPBuf + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int phys = cc ^ (row & 7);
+          *reinterpret_cast<uint4*>(prow + phys * 16) =
+              make_uint4(packed[4 * cc], packed[4 * cc + 1], packed[4 * cc + 2], packed[4 * cc + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_pf(j & 1));
       }
-      if (ok) ok = pv(nb - 1);
-      if (!ok) report(p.status, SPEC_ERR_TIMEOUT);
-      // every MMA issued has completed before TMEM is released
-      tc::mma_commit(bar_fin);
-      int zero = 0;
-      tc::mbar_wait(bar_fin, 0, &zero, kWaitLimit);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ softmax warps
-    const uint32_t t_lane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
-    float m_run = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      if (!warp_wait(bar_sf(j & 1), (j >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
+      ok = ok && warp_wait(bar_pv, (nb - 1) & 1, abort);
+      if (!ok && threadIdx.x == 64) report(p.status, SPEC_ERR_TIMEOUT);
       tc::fence_after_sync();
-      float sv[kTcKeys];
-      tc::tmem_ld32(t_lane + (j & 1) * 64, sv);
-      tc::tmem_ld32(t_lane + (j & 1) * 64 + 32, sv + 32);
-      tc::tmem_wait_ld();
-      const int blk = sr.blk_lo + j;
-      float mx = -INFINITY;
-      if (blk < npb) {
-        const int nvalid = min(kTcKeys, P - blk * kTcKeys);  // length bound only, no mask
-#pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          sv[c] = c < nvalid ? sv[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sv[c]);
-        }
-      } else {
-        const uint64_t bits = row_valid ? __ldg(mrow + (blk - npb)) : 0ull;
-#pragma unroll
-        for (int c = 0; c < kTcKeys; ++c) {
-          sv[c] = ((bits >> c) & 1ull) ? sv[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sv[c]);
-        }
-      }
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mx > -INFINITY && (m_run == -INFINITY || mx > m_run + kRescaleThr)) {
-        alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mx);
-        m_run = mx;
-        rescale = j > 0;
-      }
-      uint32_t packed[kTcKeys / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kTcKeys; c += 2) {
-        const float p0 = m_run == -INFINITY ? 0.f : exp2f(sv[c] - m_run);
-        const float p1 = m_run == -INFINITY ? 0.f : exp2f(sv[c + 1] - m_run);
-        rs += p0 + p1;
-        packed[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      if (j >= 1) {  // PV of the previous block done: O is stable and P[j%2] is free
-        if (!warp_wait(bar_pv, (j - 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-      }
-      if (__any_sync(0xffffffffu, rescale)) {  // tcgen05.ld/st are warp-collective
-#pragma unroll
-        for (int ch = 0; ch < kTcD / 32; ++ch) {
-          float o[32];
-          tc::tmem_ld32(t_lane + 128 + ch * 32, o);
-          tc::tmem_wait_ld();
-          const float f = rescale ? alpha : 1.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tc::tmem_st32(t_lane + 128 + ch * 32, o);
-        }
-        tc::tmem_wait_st();
-      }
-      uint8_t* prow = smem + kOffP + (j & 1) * kPBuf + row * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const int phys = cc ^ (row & 7);
-        *reinterpret_cast<uint4*>(prow + phys * 16) =
-            make_uint4(packed[4 * cc], packed[4 * cc + 1], packed[4 * cc + 2], packed[4 * cc + 3]);
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::mbar_arrive(bar_pf(j & 1));
-    }
-    if (ok && warp_wait(bar_pv, (nb - 1) & 1, abort)) {
-      tc::fence_after_sync();
+      // O row out of TMEM: final output when unsplit, else this split's partial
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      float4* po = p.part_o + ((size_t)grp * p.splits + split) * (kTcRows * kTcD / 4);
+#pragma unroll 1
       for (int ch = 0; ch < kTcD / 32; ++ch) {
         float o[32];
         __syncwarp();
         tc::tmem_ld32(t_lane + 128 + ch * 32, o);
         tc::tmem_wait_ld();
-        if (!row_valid) {
-        } else if (p.splits == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kTcD + ch * 32);
+        if (!ok) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.ws.o + ((size_t)split * p.total_rows + orow) * kTcD + ch * 32);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) dst[v] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
-      }
-      if (row_valid) {
         if (p.splits == 1) {
-          if (p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
-        } else {
-          p.ws.ml[(size_t)split * p.total_rows + orow] = make_float2(m_run, l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kTcD + ch * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                  pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                  pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                  pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+          }
+        } else {  // chunk-major: a warp's 32 rows write 512 contiguous bytes per chunk
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            po[(ch * 8 + v) * kTcRows + row] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
-    } else if (threadIdx.x == 64) {
-      report(p.status, SPEC_ERR_TIMEOUT);
+      if (p.splits == 1) {
+        if (row_valid && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
+      } else {
+        p.part_ml[((size_t)grp * p.splits + split) * kTcRows + row] =
+            ok ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
 
-  tc::fence_before_sync();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tbase, kTmemCols);
+    }
+  } else if (warp >= 2) {  // empty key split (only when split): contributes nothing to the merge
+    p.part_ml[((size_t)grp * p.splits + split) * kTcRows + row] = make_float2(-INFINITY, 0.f);
+  }
+  if (p.splits == 1) return;
+
+  // ------------------------------------------------------------------ merge of the splits
+  // The launch is cooperative (every CTA resident at once), so the S CTAs of a group can
+  // wait for one another: each publishes its partial, bumps the group's arrival count,
+  // waits (bounded) until all S arrived, then merges rows [s*128/S, (s+1)*128/S) of the
+  // group by log-sum-exp and writes the bf16 output and the lse. The last CTA to leave
+  // resets the group's counters for the next call.
+  __shared__ int s_go;
   __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tbase, kTmemCols);
+  unsigned* cnt = p.counters + 2 * grp;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(cnt, 1u);
+    int go = 1;
+    const long long t0 = clock64();
+    while (ld_acquire_u32(cnt) < (unsigned)p.splits) {
+      if (clock64() - t0 > kWaitLimit) {
+        report(p.status, SPEC_ERR_TIMEOUT);
+        go = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    s_go = go;
+  }
+  __syncthreads();
+  if (!s_go) return;
+  {
+    const int S = p.splits;
+    const int r0 = split * kTcRows / S, r1 = (split + 1) * kTcRows / S;
+    const int R = r1 - r0;
+    float* wts = reinterpret_cast<float*>(smem + kOffP);  // [R][S] merge weights (P buffers are free)
+    float* lse_r = wts + kTcRows * 32;                    // [R]
+    const float2* ml = p.part_ml + (size_t)grp * S * kTcRows;
+    const float4* po = p.part_o + (size_t)grp * S * (kTcRows * kTcD / 4);
+    for (int r = threadIdx.x; r < R; r += kTcThreads) {
+      float M = -INFINITY;
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, __ldcg(&ml[sp * kTcRows + r0 + r].x));
+      float L = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float2 v = __ldcg(&ml[sp * kTcRows + r0 + r]);
+        const float f = v.x == -INFINITY ? 0.f : ex2_approx(v.x - M);
+        wts[r * S + sp] = f;
+        L = fmaf(v.y, f, L);
+      }
+      const float invL = L > 0.f ? 1.f / L : 0.f;
+      for (int sp = 0; sp < S; ++sp) wts[r * S + sp] *= invL;
+      lse_r[r] = (M + log2f(L)) * kLn2;
+    }
+    __syncthreads();
+    for (int item = threadIdx.x; item < R * 32; item += kTcThreads) {
+      const int chunk = item / R, r = item - chunk * R, rr = r0 + r;
+      const int nl = node0 + rr / G;
+      if (nl >= N) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int sp = 0; sp < S; ++sp) {
+        const float w = wts[r * S + sp];
+        const float4 o = __ldcg(po + ((size_t)sp * 32 + chunk) * kTcRows + rr);
+        acc.x = fmaf(o.x, w, acc.x);
+        acc.y = fmaf(o.y, w, acc.y);
+        acc.z = fmaf(o.z, w, acc.z);
+        acc.w = fmaf(o.w, w, acc.w);
+      }
+      const int hh = g * G + (rr - (rr / G) * G);
+      const size_t orr = (size_t)(base + nl) * p.hq + hh;
+      *reinterpret_cast<uint2*>(p.out + orr * kTcD + chunk * 4) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      if (chunk == 0 && p.lse != nullptr) p.lse[orr] = lse_r[r];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(cnt + 1, 1u) == (unsigned)(p.splits - 1)) {
+    cnt[0] = 0u;  // every CTA of the group has left its wait: reset for the next call
+    cnt[1] = 0u;
   }
 }
 
@@ -426,24 +556,52 @@ bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max
          tensor_map_encoder() != nullptr;
 }
 
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+                                                   cudaSuccess && v > 0)
+      n = v;
+    else
+      return 152;  // no device visible (sizing on a build machine): the GB300 count
+  }
+  return n;
+}
+
+// Key splits per (sequence, KV head, M-tile) group: enough that the groups x splits CTAs
+// (one per SM: 197 KB of shared memory each) cover the SMs when the batch alone does
+// not, never more CTAs than SMs (the split merge needs them all resident), at least two
+// key blocks per split, at most 32 splits.
 int attn_splits_tc(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
   if (hkv <= 0 || hq % hkv) return 1;
   const int G = hq / hkv;
-  const int mtiles = ceil_div(max_nodes * G, kTcRows);
-  const long base = (long)batch * hkv * mtiles;
+  const long groups = (long)batch * hkv * ceil_div(max_nodes * G, kTcRows);
   const int blocks = ceil_div(max_prefix, kTcKeys) + ceil_div(max_nodes, kTcKeys);
-  const int cap = blocks / 2 > 1 ? blocks / 2 : 1;
-  int s = 1;
-  if (base < 152) {
-    s = (int)(152 / (base > 0 ? base : 1));
-  } else {  // several waves: take a second split when it evens out the last wave
-    const double e1 = (double)base / (double)(((base + 151) / 152) * 152);
-    const double e2 = (double)(2 * base) / (double)(((2 * base + 151) / 152) * 152);
-    if (e1 < 0.9 && e2 > e1 + 0.05) s = 2;
+  long s = groups > 0 ? sm_count() / groups : 1;
+  if (s > blocks / 2) s = blocks / 2;
+  if (s > 32) s = 32;
+  return s < 1 ? 1 : (int)s;
+}
+
+struct TcWs {
+  size_t counters, ml, o, total;
+  static TcWs make(long groups, int splits) {
+    TcWs w;
+    size_t off = 0;
+    w.counters = off; off = align_up(off + 2 * sizeof(unsigned) * groups, 256);
+    w.ml = off;       off = align_up(off + sizeof(float2) * groups * splits * kTcRows, 256);
+    w.o = off;        off = align_up(off + sizeof(float) * groups * splits * kTcRows * kTcD, 256);
+    w.total = off;
+    return w;
   }
-  if (s > cap) s = cap;
-  if (s > 64) s = 64;
-  return s < 1 ? 1 : s;
+};
+
+size_t attn_tc_ws_bytes(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
+  const int s = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
+  if (s <= 1) return 0;
+  const long groups = (long)batch * hkv * ceil_div(max_nodes * (hq / hkv), kTcRows);
+  return TcWs::make(groups, s).total;
 }
 
 int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
@@ -503,13 +661,35 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.scale_log2 = sm_scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
-  prm.ws = AttnWs::at(ws, splits, rows, kTcD);
+  const int mtiles = ceil_div(max_nodes * G, kTcRows);
+  const TcWs w = TcWs::make((long)batch * hkv * mtiles, splits);
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  prm.part_o = splits > 1 ? reinterpret_cast<float4*>(wb + w.o) : nullptr;
+  prm.part_ml = splits > 1 ? reinterpret_cast<float2*>(wb + w.ml) : nullptr;
+  prm.counters = splits > 1 ? reinterpret_cast<unsigned*>(wb + w.counters) : nullptr;
   prm.status = status;
-  const dim3 grid(splits, ceil_div(max_nodes * G, kTcRows), batch * hkv);
-  attn_tc_kernel<<<grid, kTcThreads, kSmemBytes, stream>>>(tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  if (splits > 1) return launch_attn_combine(SPEC_BF16, prm.ws, splits, total_nodes, hq, kTcD, out, lse, stream);
-  return SPEC_OK;
+  const dim3 grid(splits, mtiles, batch * hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (splits > 1) {
+    // the split merge waits on sibling CTAs: all of them must be resident at once
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    // programmatic serialization: the prologue (barriers, TMEM, Q and first K/V loads)
+    // overlaps the mask kernel; the softmax waits for it before the first tree block
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // namespace specv

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     int num_pages, int page_size, const int32_t* __restrict__ prefix_len,
     int32_t* __restrict__ seq_len_out, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
     int hkv, int row_bytes, int32_t* status) {
+  pdl_wait();  // accept_len / path come from the acceptance kernel just before
   const int b = blockIdx.x;
   __shared__ int s_ok;
   __shared__ int s_L;
@@ -87,10 +88,11 @@ int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, con
                      const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool, void* v_pool,
                      int batch, int hkv, int d, int32_t* status, cudaStream_t stream) {
   const int row_bytes = d * elem_bytes;
-  kv_commit_kernel<<<batch, 256, 0, stream>>>(
-      static_cast<const uint8_t*>(k_tree), static_cast<const uint8_t*>(v_tree), path, path_cap,
-      accept_len, qo, page_table, max_pages, num_pages, page_size, prefix_len, seq_len_out,
-      static_cast<uint8_t*>(k_pool), static_cast<uint8_t*>(v_pool), hkv, row_bytes, status);
+  if (launch_pdl(kv_commit_kernel, dim3(batch), dim3(256), 0, stream, static_cast<const uint8_t*>(k_tree),
+                 static_cast<const uint8_t*>(v_tree), path, path_cap, accept_len, qo, page_table, max_pages,
+                 num_pages, page_size, prefix_len, seq_len_out, static_cast<uint8_t*>(k_pool),
+                 static_cast<uint8_t*>(v_pool), hkv, row_bytes, status) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(128) tree_mask_kernel(const int32_t* __restric
                                                         uint64_t* __restrict__ mask,
                                                         int32_t* __restrict__ depth,
                                                         int32_t* status) {
+  pdl_trigger();  // the attention kernel may start its mask-independent prologue
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= total_nodes) return;
   const int b = seq_of_row(qo, batch, t);
