@@ -8,27 +8,29 @@
 // tiles run with no mask at all (only a length bound on the ragged last block) and
 // the ancestor bits are tested on the in-tree tiles only.
 //
-// CTA = (key split s, M-tile of 128 query rows, sequence b x KV head g); rows are
-// node-major (row r -> node r / G, head g*G + r % G), so the G query heads of a KV
-// head share every K/V tile (GQA). Keys come in blocks of 64: prefix blocks are 4
-// pages of 16 tokens, TMA-loaded page by page through the page table
-// ([page][Hkv][16][128] bf16, so a (page, head) is one 4 KB tile); tree blocks are
-// 64 rows of the dense tree K/V. Warp roles:
-//   warp 0     TMA producer: Q once, then K/V blocks into a 4-stage ring
-//   warp 1     TMEM allocation; one lane issues the MMAs:
-//                S[j%2] = Q K_j^T   (M 128, N 64, K 128; both operands K-major)
-//                O     += P_j V_j   (M 128, N 128, K 64; V is MN-major)
-//   warps 2-5  softmax, one thread per query row (its TMEM lane): S row -> max /
-//              exp2 / row sum in registers, P row -> bf16 in shared memory
-//              (128-byte swizzle), O rescale in TMEM only when the running max
-//              grows by more than 2^8; finally O / l to global memory.
-// S is double-buffered in TMEM (2 x 64 columns) next to O (128 columns), so QK of
-// block j+1 runs while the softmax of block j does. Every wait is bounded.
-// When the keys are split (a single short sequence cannot fill 152 SMs otherwise),
-// the launch is cooperative: the S split CTAs of one (sequence, KV head, M-tile) group
-// publish unnormalised partials (coalesced, L2-resident), meet at a bounded
-// arrival counter, and each merges a slice of the group's rows by log-sum-exp — the
-// merge needs no second kernel.
+// Query rows of (sequence b, KV head g) are node-major (row r -> node r / G, head
+// g*G + r % G), so the G query heads of a KV head share every K/V tile (GQA); they
+// are cut into M-tiles of 128 rows. A CTA = (key split s, pair of M-tiles, b x g):
+// both tiles share each K/V block, which halves K/V traffic into shared memory and
+// lets two softmax warp groups hide each other's latency (ping-pong). Keys come in
+// blocks of 64: prefix blocks are 4 pages of 16 tokens, TMA-loaded page by page
+// through the page table ([page][Hkv][16][128] bf16: a (page, head) is one 4 KB
+// tile; page ids are fetched a batch of 8 blocks ahead); tree blocks are 64 rows of
+// the dense tree K/V. Warp roles (320 threads):
+//   warp 0      TMA producer: Q of both tiles, then K/V blocks into a 4-stage ring
+//   warp 1      TMEM allocation (512 columns); one lane issues the MMAs, per tile t:
+//                 S_t[j%2] = Q_t K_j^T  (M 128, N 64, K 128; both operands K-major)
+//                 O_t     += P_t V_j    (M 128, N 128, K 64; V is MN-major)
+//   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one query row per
+//               thread (its TMEM lane); S row -> max / exp2 / row sum in registers,
+//               P row -> bf16 in shared memory (128-byte swizzle), O rescaled in
+//               TMEM only when the running max grows by more than 2^8.
+// S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
+// does. Every wait is bounded.
+// When the keys are split (a short batch cannot fill 152 SMs otherwise), the launch
+// is cooperative: the split CTAs of a tile publish unnormalised partials (coalesced,
+// L2-resident), meet at a bounded arrival counter, and each merges a slice of the
+// tile's rows by log-sum-exp after staging it in shared memory — no second kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,22 +43,25 @@ constexpr int kTcRows = 128;
 constexpr int kTcKeys = 64;
 constexpr int kTcD = 128;
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 192;
+constexpr int kTiles = 2;
+constexpr int kTcThreads = 64 + kTiles * 128;
 constexpr float kRescaleThr = 8.0f;            // log2 units: P entries stay <= 2^8
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s) before a wait gives up
 
 constexpr uint32_t kQSlab = kTcRows * 128;                  // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kQTile = 2 * kQSlab;
 constexpr uint32_t kKVSlab = kTcKeys * 128;                 // 8 KB: 64 keys x 64 bf16
 constexpr uint32_t kStageBytes = 4 * kKVSlab;               // K (2 slabs) + V (2 slabs)
 constexpr uint32_t kPBuf = kTcRows * 128;                   // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + 2 * kQSlab;
+constexpr uint32_t kOffKV = kOffQ + kTiles * kQTile;
 constexpr uint32_t kOffP = kOffKV + kTcStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;
+constexpr uint32_t kOffBar = kOffP + kTiles * kPBuf;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;       // barriers + alignment slack
-constexpr uint32_t kTmemCols = 256;                         // S0 | S1 | O
+constexpr uint32_t kTmemCols = 512;                         // per tile: S0 | S1 | O
 constexpr uint32_t kIdescQK = tc::idesc_bf16(kTcRows, kTcKeys, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(kTcRows, kTcD, 1);
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
 struct TcParams {
   const int32_t* page_table;
@@ -65,20 +70,22 @@ struct TcParams {
   const uint64_t* mask;
   int mask_words;
   const int32_t* qo;
-  int hq, hkv, G, splits, total_rows;
+  int hq, hkv, G, splits, mtiles;
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
-  float4* part_o;      // split partials [group][S][32 chunks][128 rows] (unnormalised O)
-  float2* part_ml;     // [group][S][128 rows] (running max in log2 units, row sum)
-  unsigned* counters;  // [group][2] arrivals / departures (zero between calls)
+  float4* part_o;      // split partials [tile group][S][32 chunks][128 rows] (unnormalised O)
+  float2* part_ml;     // [tile group][S][128 rows] (running max in log2 units, row sum)
+  unsigned* counters;  // [tile group][2] arrivals / departures (zero between calls)
   int32_t* status;
 };
 
 struct TcBars {
-  uint64_t q_full, kv_full[kTcStages], kv_empty[kTcStages], s_full[2], p_full[2], pv_done, mma_fin;
+  uint64_t q_full, kv_full[kTcStages], kv_empty[kTcStages];
+  uint64_t s_full[kTiles][2], p_full[kTiles], pv_done[kTiles], mma_fin;
   uint32_t tmem_base;
   int abort;
+  int go;
 };
 
 // One lane waits, the whole warp gets the answer: keeps warp-collective tcgen05.ld/st
@@ -106,6 +113,12 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* ptr) {
   return v;
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(smem_dst)), "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
@@ -115,17 +128,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   TcBars& bars = *reinterpret_cast<TcBars*>(smem + kOffBar);
   const uint32_t s_base = tc::smem_u32(smem);
 
-  const int split = blockIdx.x, mt = blockIdx.y, bg = blockIdx.z;
+  const int split = blockIdx.x, pair = blockIdx.y, bg = blockIdx.z;
   const int G = p.G;
   const int b = bg / p.hkv, g = bg - (bg / p.hkv) * p.hkv;
   const int base = __ldg(p.qo + b);
   const int N = __ldg(p.qo + b + 1) - base;
   const int P = __ldg(p.prefix_len + b);
   const int npt = kTcRows / G;  // tree nodes per M-tile
-  const int node0 = mt * npt;
+  const int node0 = 2 * pair * npt;
+  const bool has1 = node0 + npt < N;  // tile 1 holds rows of this sequence
+  const int ntiles = has1 ? 2 : 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the two exits below are taken by every split CTA of a group alike (they depend on b, g, mt)
-  if (node0 >= N) return;  // this M-tile is past the sequence's tree
+  // the two exits below are taken by every split CTA of a tile alike (they depend on b, g, pair)
+  if (node0 >= N) return;  // this pair of M-tiles is past the sequence's tree
   if (N > p.mask_words * 64 || P < 0 || P > p.max_pages * 16) {
     if (threadIdx.x == 0 && split == 0) report(p.status, SPEC_ERR_CAPACITY);
     return;
@@ -134,22 +149,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nb = sr.blk_hi - sr.blk_lo;
   const int npb = sr.n_prefix_blocks;
 
-  // softmax-thread row bookkeeping (warps 2-5; quarter q of TMEM lanes = warp % 4)
+  // softmax-thread bookkeeping: warps 2-5 tile 0, warps 6-9 tile 1; TMEM lane quarter = warp % 4
+  const int tile = warp >= 6 ? 1 : 0;
   const int row = (warp & 3) * 32 + lane;
-  const int node_l = node0 + row / G;
+  const int node_l = node0 + tile * npt + row / G;
   const int head = g * G + (row - (row / G) * G);
   const bool row_valid = node_l < N;
   const size_t orow = (size_t)(base + node_l) * p.hq + head;
-  const int grp = mt + gridDim.y * bg;  // (sequence, KV head, M-tile) group of the key splits
+  const int grp = (2 * pair + tile) + p.mtiles * bg;  // tile group of the key splits
 
   if (nb > 0) {
     const uint32_t bar_q = tc::smem_u32(&bars.q_full);
-    const uint32_t bar_pv = tc::smem_u32(&bars.pv_done);
     const uint32_t bar_fin = tc::smem_u32(&bars.mma_fin);
     auto bar_kvf = [&](int s) { return tc::smem_u32(&bars.kv_full[s]); };
     auto bar_kve = [&](int s) { return tc::smem_u32(&bars.kv_empty[s]); };
-    auto bar_sf = [&](int s) { return tc::smem_u32(&bars.s_full[s]); };
-    auto bar_pf = [&](int s) { return tc::smem_u32(&bars.p_full[s]); };
+    auto bar_sf = [&](int t, int s) { return tc::smem_u32(&bars.s_full[t][s]); };
+    auto bar_pf = [&](int t) { return tc::smem_u32(&bars.p_full[t]); };
+    auto bar_pv = [&](int t) { return tc::smem_u32(&bars.pv_done[t]); };
     volatile int* abort = &bars.abort;
 
     // Page ids of the producer's next 8 blocks, one per lane (lane l: block 8k + l/4,
@@ -185,10 +201,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (blk < npb) {
         if (lane < 16) {
           const int pp = lane >> 2, which = lane & 3;
-          const int page = page_here;
           const int slab = which & 1, isv = which >> 1;
           const uint32_t dst = dst0 + isv * 2 * kKVSlab + slab * kKVSlab + pp * 2048;
-          tc::tma_load_4d(dst, isv ? &tm_vp : &tm_kp, bar_kvf(st), slab * 64, 0, g, page);
+          tc::tma_load_4d(dst, isv ? &tm_vp : &tm_kp, bar_kvf(st), slab * 64, 0, g, page_here);
         }
       } else if (lane < 4) {
         const int tb = blk - npb;
@@ -198,31 +213,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
 
-    const int first = nb < kTcStages ? nb : kTcStages;
     if (warp == 0) {
-      // barriers, then the first loads at once: their latency overlaps the TMEM allocation
+      // barriers, Q and the first block before the CTA-wide sync: their latency
+      // overlaps the TMEM allocation
       if (lane == 0) {
         tc::mbar_init(bar_q, 1);
         for (int s = 0; s < kTcStages; ++s) {
           tc::mbar_init(bar_kvf(s), 1);
           tc::mbar_init(bar_kve(s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-          tc::mbar_init(bar_sf(s), 1);
-          tc::mbar_init(bar_pf(s), 128);
+        for (int t = 0; t < kTiles; ++t) {
+          tc::mbar_init(bar_sf(t, 0), 1);
+          tc::mbar_init(bar_sf(t, 1), 1);
+          tc::mbar_init(bar_pf(t), 128);
+          tc::mbar_init(bar_pv(t), 1);
         }
-        tc::mbar_init(bar_pv, 1);
         tc::mbar_init(bar_fin, 1);
         bars.abort = 0;
         tc::mbar_fence_init();
-        tc::mbar_arrive_expect_tx(bar_q, 2 * kQSlab);
-        tc::tma_load_3d(s_base + kOffQ, &tm_q, bar_q, 0, g * G, base + node0);
-        tc::tma_load_3d(s_base + kOffQ + kQSlab, &tm_q, bar_q, 64, g * G, base + node0);
+        tc::mbar_arrive_expect_tx(bar_q, ntiles * kQTile);
+        for (int t = 0; t < ntiles; ++t) {
+          const int n0 = base + node0 + t * npt;
+          tc::tma_load_3d(s_base + kOffQ + t * kQTile, &tm_q, bar_q, 0, g * G, n0);
+          tc::tma_load_3d(s_base + kOffQ + t * kQTile + kQSlab, &tm_q, bar_q, 64, g * G, n0);
+        }
       }
       __syncwarp();
       pg_cur = fetch_pages(0);
       pg_nxt = fetch_pages(1);
-      for (int j = 0; j < first; ++j) load_block(j);
+      load_block(0);
     } else if (warp == 1) {
       tc::tmem_alloc(tc::smem_u32(&bars.tmem_base), kTmemCols);
       tc::tmem_relinquish();
@@ -234,8 +253,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
-      int issued = first;
-      for (int j = first; j < nb; ++j) {
+      int issued = 1;
+      for (int j = 1; j < nb; ++j) {
         if (!warp_wait(bar_kve(j % kTcStages), ((j / kTcStages) & 1) ^ 1, abort)) {
           if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
           break;
@@ -253,42 +272,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        const uint32_t t_s[2] = {tbase, tbase + 64};
-        const uint32_t t_o = tbase + 128;
-        auto pv = [&](int i) -> bool {
-          if (!tc::mbar_wait(bar_pf(i & 1), (i >> 1) & 1, abort, kWaitLimit)) return false;
-          tc::fence_after_sync();
-          const uint32_t pbuf = s_base + kOffP + (i & 1) * kPBuf;
-          const uint32_t vbuf = s_base + kOffKV + (i % kTcStages) * kStageBytes + 2 * kKVSlab;
+        auto qk = [&](int j) {
+          const uint32_t kbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes;
+          for (int t = 0; t < ntiles; ++t) {
+            const uint32_t qbuf = s_base + kOffQ + t * kQTile;
 #pragma unroll
-          for (int k = 0; k < kTcKeys / 16; ++k) {
-            const uint64_t a = tc::sdesc_sw128(pbuf + k * 32, 16, 1024);
-            const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
-            tc::mma_bf16(t_o, a, bdesc, kIdescPV, (i > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kTcD / 16; ++k) {
+              const uint64_t a = tc::sdesc_sw128(qbuf + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
+              const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
+              tc::mma_bf16(tbase + t * 256 + (j & 1) * 64, a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(bar_sf(t, j & 1));
           }
-          tc::mma_commit(bar_kve(i % kTcStages));
-          tc::mma_commit(bar_pv);
-          return true;
         };
-        bool ok = tc::mbar_wait(bar_q, 0, abort, kWaitLimit);
-        for (int j = 0; ok && j < nb; ++j) {
-          const int st = j % kTcStages;
-          if (!tc::mbar_wait(bar_kvf(st), (j / kTcStages) & 1, abort, kWaitLimit)) {
-            ok = false;
-            break;
-          }
+        bool ok = tc::mbar_wait(bar_q, 0, abort, kWaitLimit) &&
+                  tc::mbar_wait(bar_kvf(0), 0, abort, kWaitLimit);
+        if (ok) {
           tc::fence_after_sync();
-          const uint32_t kbuf = s_base + kOffKV + st * kStageBytes;
-#pragma unroll
-          for (int k = 0; k < kTcD / 16; ++k) {
-            const uint64_t a = tc::sdesc_sw128(s_base + kOffQ + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
-            const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
-            tc::mma_bf16(t_s[j & 1], a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar_sf(j & 1));
-          if (j >= 1 && !pv(j - 1)) ok = false;
+          qk(0);
         }
-        if (ok) ok = pv(nb - 1);
+        for (int j = 0; ok && j < nb; ++j) {
+          if (j + 1 < nb) {  // S of the next block while the softmax works on this one
+            const int st = (j + 1) % kTcStages;
+            if (!tc::mbar_wait(bar_kvf(st), ((j + 1) / kTcStages) & 1, abort, kWaitLimit)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            qk(j + 1);
+          }
+          const uint32_t vbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes + 2 * kKVSlab;
+          for (int t = 0; t < ntiles && ok; ++t) {
+            if (!tc::mbar_wait(bar_pf(t), j & 1, abort, kWaitLimit)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t pbuf = s_base + kOffP + t * kPBuf;
+#pragma unroll
+            for (int k = 0; k < kTcKeys / 16; ++k) {
+              const uint64_t a = tc::sdesc_sw128(pbuf + k * 32, 16, 1024);
+              const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
+              tc::mma_bf16(tbase + t * 256 + 128, a, bdesc, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(bar_pv(t));
+          }
+          if (ok) tc::mma_commit(bar_kve(j % kTcStages));
+        }
         if (!ok) report(p.status, SPEC_ERR_TIMEOUT);
         // every MMA issued has completed before TMEM is released
         tc::mma_commit(bar_fin);
@@ -296,16 +326,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::mbar_wait(bar_fin, 0, &zero, kWaitLimit);
       }
       __syncwarp();
-    } else {
+    } else if (tile < ntiles) {
       // ---------------------------------------------------------------- softmax warps
-      const uint32_t t_lane = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint32_t t_lane = tbase + tile * 256 + ((uint32_t)((warp & 3) * 32) << 16);
       const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
       const float sl2 = p.scale_log2;
+      uint8_t* prow = smem + kOffP + tile * kPBuf + row * 128;
       float m_run = -INFINITY, l = 0.f;
       bool ok = true;
       bool mask_ready = false;
       for (int j = 0; j < nb; ++j) {
-        if (!warp_wait(bar_sf(j & 1), (j >> 1) & 1, abort)) {
+        if (!warp_wait(bar_sf(tile, j & 1), (j >> 1) & 1, abort)) {
           ok = false;
           break;
         }
@@ -322,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < kTcKeys; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
           }
         } else {  // tree block: ancestor bits
-          if (!mask_ready) {  // the mask comes from the kernel launched just before this one
+          if (!mask_ready) {  // the mask may come from the kernel launched just before this one
             pdl_wait();
             mask_ready = true;
           }
@@ -363,8 +394,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
         l = l * alpha + ((r0 + r1) + (r2 + r3));
-        if (j >= 1) {  // PV of the previous block done: O is stable and P[j%2] is free
-          if (!warp_wait(bar_pv, (j - 1) & 1, abort)) {
+        if (j >= 1) {  // PV of the previous block done: O is stable and the P buffer is free
+          if (!warp_wait(bar_pv(tile), (j - 1) & 1, abort)) {
             ok = false;
             break;
           }
@@ -383,7 +414,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::tmem_wait_st();
         }
-        uint8_t* prow = smem + kOffP + (j & 1) * kPBuf + row * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           const int phys = cc ^ (row & 7);
@@ -392,10 +422,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        tc::mbar_arrive(bar_pf(j & 1));
+        tc::mbar_arrive(bar_pf(tile));
       }
-      ok = ok && warp_wait(bar_pv, (nb - 1) & 1, abort);
-      if (!ok && threadIdx.x == 64) report(p.status, SPEC_ERR_TIMEOUT);
+      ok = ok && warp_wait(bar_pv(tile), (nb - 1) & 1, abort);
+      if (!ok && (threadIdx.x & 127) == 0) report(p.status, SPEC_ERR_TIMEOUT);
       tc::fence_after_sync();
       // O row out of TMEM: final output when unsplit, else this split's partial
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -441,85 +471,108 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_after_sync();
       tc::tmem_dealloc(tbase, kTmemCols);
     }
-  } else if (warp >= 2) {  // empty key split (only when split): contributes nothing to the merge
+  } else if (warp >= 2 && tile < ntiles) {  // empty key split: contributes nothing to the merge
     p.part_ml[((size_t)grp * p.splits + split) * kTcRows + row] = make_float2(-INFINITY, 0.f);
   }
   if (p.splits == 1) return;
 
   // ------------------------------------------------------------------ merge of the splits
-  // The launch is cooperative (every CTA resident at once), so the S CTAs of a group can
-  // wait for one another: each publishes its partial, bumps the group's arrival count,
-  // waits (bounded) until all S arrived, then merges rows [s*128/S, (s+1)*128/S) of the
-  // group by log-sum-exp and writes the bf16 output and the lse. The last CTA to leave
-  // resets the group's counters for the next call.
-  __shared__ int s_go;
+  // The launch is cooperative (every CTA resident at once), so the S split CTAs of a tile
+  // can wait for one another: each publishes its partial, bumps the tile's arrival count,
+  // waits (bounded) until all S arrived, stages rows [s*128/S, (s+1)*128/S) of every
+  // partial into shared memory (cp.async, one round trip), merges them by log-sum-exp
+  // and writes the bf16 output and the lse. The last CTA to leave resets the counters.
+  const int S = p.splits;
   __syncthreads();
-  unsigned* cnt = p.counters + 2 * grp;
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(cnt, 1u);
+    for (int t = 0; t < ntiles; ++t) atomicAdd(p.counters + 2 * ((2 * pair + t) + p.mtiles * bg), 1u);
     int go = 1;
     const long long t0 = clock64();
-    while (ld_acquire_u32(cnt) < (unsigned)p.splits) {
-      if (clock64() - t0 > kWaitLimit) {
-        report(p.status, SPEC_ERR_TIMEOUT);
-        go = 0;
-        break;
+    for (int t = 0; t < ntiles && go; ++t) {
+      const unsigned* c = p.counters + 2 * ((2 * pair + t) + p.mtiles * bg);
+      while (ld_acquire_u32(c) < (unsigned)S) {
+        if (clock64() - t0 > kWaitLimit) {
+          report(p.status, SPEC_ERR_TIMEOUT);
+          go = 0;
+          break;
+        }
+        __nanosleep(32);
       }
-      __nanosleep(32);
     }
-    s_go = go;
+    bars.go = go;
   }
   __syncthreads();
-  if (!s_go) return;
+  if (!bars.go) return;
   {
-    const int S = p.splits;
     const int r0 = split * kTcRows / S, r1 = (split + 1) * kTcRows / S;
     const int R = r1 - r0;
-    float* wts = reinterpret_cast<float*>(smem + kOffP);  // [R][S] merge weights (P buffers are free)
-    float* lse_r = wts + kTcRows * 32;                    // [R]
-    const float2* ml = p.part_ml + (size_t)grp * S * kTcRows;
-    const float4* po = p.part_o + (size_t)grp * S * (kTcRows * kTcD / 4);
-    for (int r = threadIdx.x; r < R; r += kTcThreads) {
+    const int per_tile = S * 32 * R;
+    float4* stage = reinterpret_cast<float4*>(smem + kOffKV);  // [t][s][chunk][R] (K/V ring + P: 160 KB)
+    float* wts = reinterpret_cast<float*>(smem + kOffQ);         // [t][R][S]      (Q region is free)
+    float* lse_r = reinterpret_cast<float*>(smem + kOffQ + 4096);
+    float2* mls = reinterpret_cast<float2*>(smem + kOffQ + 8192);  // [t][s][R]
+    for (int i = threadIdx.x; i < ntiles * per_tile; i += kTcThreads) {
+      const int t = i / per_tile, rem = i - t * per_tile;
+      const int sp = rem / (32 * R), rem2 = rem - sp * 32 * R;
+      const int c = rem2 / R, r = rem2 - c * R;
+      const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
+      cp_async16(stage + i, p.part_o + (gt * S + sp) * (kTcRows * kTcD / 4) + c * kTcRows + r0 + r);
+    }
+    for (int i = threadIdx.x; i < ntiles * S * R; i += kTcThreads) {
+      const int t = i / (S * R), rem = i - t * S * R;
+      const int sp = rem / R, r = rem - sp * R;
+      const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
+      mls[i] = __ldcg(p.part_ml + (gt * S + sp) * kTcRows + r0 + r);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    for (int i = threadIdx.x; i < ntiles * R; i += kTcThreads) {
+      const int t = i / R, r = i - t * R;
       float M = -INFINITY;
-      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, __ldcg(&ml[sp * kTcRows + r0 + r].x));
+      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mls[(t * S + sp) * R + r].x);
       float L = 0.f;
       for (int sp = 0; sp < S; ++sp) {
-        const float2 v = __ldcg(&ml[sp * kTcRows + r0 + r]);
+        const float2 v = mls[(t * S + sp) * R + r];
         const float f = v.x == -INFINITY ? 0.f : ex2_approx(v.x - M);
-        wts[r * S + sp] = f;
+        wts[(t * R + r) * S + sp] = f;
         L = fmaf(v.y, f, L);
       }
       const float invL = L > 0.f ? 1.f / L : 0.f;
-      for (int sp = 0; sp < S; ++sp) wts[r * S + sp] *= invL;
-      lse_r[r] = (M + log2f(L)) * kLn2;
+      for (int sp = 0; sp < S; ++sp) wts[(t * R + r) * S + sp] *= invL;
+      lse_r[t * R + r] = (M + log2f(L)) * kLn2;
     }
     __syncthreads();
-    for (int item = threadIdx.x; item < R * 32; item += kTcThreads) {
-      const int chunk = item / R, r = item - chunk * R, rr = r0 + r;
-      const int nl = node0 + rr / G;
+    for (int i = threadIdx.x; i < ntiles * 32 * R; i += kTcThreads) {
+      const int t = i / (32 * R), rem = i - t * 32 * R;
+      const int c = rem / R, r = rem - c * R, rr = r0 + r;
+      const int nl = node0 + t * npt + rr / G;
       if (nl >= N) continue;
+      const float* w = wts + (t * R + r) * S;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
       for (int sp = 0; sp < S; ++sp) {
-        const float w = wts[r * S + sp];
-        const float4 o = __ldcg(po + ((size_t)sp * 32 + chunk) * kTcRows + rr);
-        acc.x = fmaf(o.x, w, acc.x);
-        acc.y = fmaf(o.y, w, acc.y);
-        acc.z = fmaf(o.z, w, acc.z);
-        acc.w = fmaf(o.w, w, acc.w);
+        const float4 o = stage[((t * S + sp) * 32 + c) * R + r];
+        acc.x = fmaf(o.x, w[sp], acc.x);
+        acc.y = fmaf(o.y, w[sp], acc.y);
+        acc.z = fmaf(o.z, w[sp], acc.z);
+        acc.w = fmaf(o.w, w[sp], acc.w);
       }
       const int hh = g * G + (rr - (rr / G) * G);
       const size_t orr = (size_t)(base + nl) * p.hq + hh;
-      *reinterpret_cast<uint2*>(p.out + orr * kTcD + chunk * 4) =
+      *reinterpret_cast<uint2*>(p.out + orr * kTcD + c * 4) =
           make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      if (chunk == 0 && p.lse != nullptr) p.lse[orr] = lse_r[r];
+      if (c == 0 && p.lse != nullptr) p.lse[orr] = lse_r[t * R + r];
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && atomicAdd(cnt + 1, 1u) == (unsigned)(p.splits - 1)) {
-    cnt[0] = 0u;  // every CTA of the group has left its wait: reset for the next call
-    cnt[1] = 0u;
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < ntiles; ++t) {
+      unsigned* c = p.counters + 2 * ((2 * pair + t) + p.mtiles * bg);
+      if (atomicAdd(c + 1, 1u) == (unsigned)(S - 1)) {  // every split CTA has left its wait
+        c[0] = 0u;
+        c[1] = 0u;
+      }
+    }
   }
 }
 
@@ -543,7 +596,7 @@ static bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint6
                         const cuuint32_t* box) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -569,16 +622,18 @@ static int sm_count() {
   return n;
 }
 
-// Key splits per (sequence, KV head, M-tile) group: enough that the groups x splits CTAs
-// (one per SM: 197 KB of shared memory each) cover the SMs when the batch alone does
-// not, never more CTAs than SMs (the split merge needs them all resident), at least two
-// key blocks per split, at most 32 splits.
+static int tc_mtiles(int max_nodes, int G) { return ceil_div(max_nodes * G, kTcRows); }
+
+// Key splits per CTA work item (sequence, KV head, pair of M-tiles): enough that the
+// items x splits CTAs (one per SM: 225 KB of shared memory each) cover the SMs when the
+// batch alone does not, never more CTAs than SMs (the split merge needs them all
+// resident), at least two key blocks per split, at most 32 splits.
 int attn_splits_tc(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
   if (hkv <= 0 || hq % hkv) return 1;
   const int G = hq / hkv;
-  const long groups = (long)batch * hkv * ceil_div(max_nodes * G, kTcRows);
+  const long items = (long)batch * hkv * ceil_div(tc_mtiles(max_nodes, G), kTiles);
   const int blocks = ceil_div(max_prefix, kTcKeys) + ceil_div(max_nodes, kTcKeys);
-  long s = groups > 0 ? sm_count() / groups : 1;
+  long s = items > 0 ? sm_count() / items : 1;
   if (s > blocks / 2) s = blocks / 2;
   if (s > 32) s = 32;
   return s < 1 ? 1 : (int)s;
@@ -600,7 +655,7 @@ struct TcWs {
 size_t attn_tc_ws_bytes(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
   const int s = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
   if (s <= 1) return 0;
-  const long groups = (long)batch * hkv * ceil_div(max_nodes * (hq / hkv), kTcRows);
+  const long groups = (long)batch * hkv * tc_mtiles(max_nodes, hq / hkv);
   return TcWs::make(groups, s).total;
 }
 
@@ -644,7 +699,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
     attr_set = true;
   }
   const int splits = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
-  const int rows = total_nodes * hq;
+  const int mtiles = tc_mtiles(max_nodes, G);
   TcParams prm;
   prm.page_table = page_table;
   prm.max_pages = max_pages;
@@ -657,20 +712,18 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.hkv = hkv;
   prm.G = G;
   prm.splits = splits;
-  prm.total_rows = rows;
+  prm.mtiles = mtiles;
   prm.scale_log2 = sm_scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
-  const int mtiles = ceil_div(max_nodes * G, kTcRows);
   const TcWs w = TcWs::make((long)batch * hkv * mtiles, splits);
   uint8_t* wb = static_cast<uint8_t*>(ws);
   prm.part_o = splits > 1 ? reinterpret_cast<float4*>(wb + w.o) : nullptr;
   prm.part_ml = splits > 1 ? reinterpret_cast<float2*>(wb + w.ml) : nullptr;
   prm.counters = splits > 1 ? reinterpret_cast<unsigned*>(wb + w.counters) : nullptr;
   prm.status = status;
-  const dim3 grid(splits, mtiles, batch * hkv);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = dim3(splits, ceil_div(mtiles, kTiles), batch * hkv);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
