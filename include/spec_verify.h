@@ -226,6 +226,30 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
                    const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool, void* v_pool,
                    int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream);
 
+/*
+ * spec_accept_noalloc — spec_accept for callers that cannot allocate device memory.
+ *   (No counterpart on the pages: this is a deployment convenience of this library.)
+ *   Some callers have no way to obtain scratch memory: a runtime that only lends out
+ *   the tensors it owns, a plugin host without an allocator, a serving loop that
+ *   forbids allocation once it runs. This entry point takes the same arguments as
+ *   spec_accept minus the workspace and computes the same results; its scratch is a
+ *   fixed 4 MiB array inside the library (a file-scope __device__ array that every GPU
+ *   loading the library holds until the process exits). It allocates and frees nothing.
+ *   - Limit: sizes whose workspace (spec_workspace_size(SPEC_OP_ACCEPT, ...)) exceeds
+ *     4 MiB return SPEC_ERR_WORKSPACE at once (e.g. 128256-token rows: up to ~10K nodes).
+ *   - Set-up: the first call on a device, with that device current, looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - Every call zeroes the array's counters on `stream` first, then runs the kernels.
+ *   - All calls share the one array: calls that may overlap on the GPU (different
+ *     streams, or different host threads) race and must be serialised by the caller.
+ */
+int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_tokens,
+                        const float* target_logits, const float* draft_logits, const float* uniforms,
+                        float temperature, int vocab, const int32_t* qo_indptr, int batch,
+                        int total_nodes, int max_nodes, int path_cap, int32_t* accept_len,
+                        int32_t* path, int32_t* out_tokens, uint8_t* flags, int32_t* dev_status,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,8 @@
 #include <float.h>
 #include <limits.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -642,3 +644,64 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
 }
 
 }  // namespace specv
+
+// ------------------------------------------------------------------------------------
+// Acceptance without caller-provided scratch.
+//
+// Some callers cannot allocate device memory at all: a runtime that hands out only the
+// tensors it owns, a plugin host with no allocator of its own, a serving loop that
+// forbids allocation once it is running. For them spec_accept_noalloc runs the same
+// kernels as spec_accept with its scratch (counters, chunk partials, per-node results)
+// in the file-scope array below, of fixed size kNoAllocScratchBytes. Every GPU that
+// loads the library holds that array until the process exits.
+namespace specv {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
+
+// Device address of g_accept_scratch for the current device. The symbol's host-side
+// name is only a stand-in, so the address is asked of the runtime, once per device,
+// with that device current. Returns nullptr when the lookup fails.
+static void* noalloc_scratch() {
+  constexpr int kMaxDevices = 64;
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace specv
+
+extern "C" int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_tokens,
+                                   const float* target_logits, const float* draft_logits, const float* uniforms,
+                                   float temperature, int vocab, const int32_t* qo_indptr, int batch,
+                                   int total_nodes, int max_nodes, int path_cap, int32_t* accept_len,
+                                   int32_t* path, int32_t* out_tokens, uint8_t* flags, int32_t* dev_status,
+                                   void* stream) {
+  using namespace specv;
+  if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
+  if (batch < 0 || total_nodes < 0 || vocab <= 0 || path_cap < 1 || max_nodes < 1 || max_nodes > kMaxTreeNodes)
+    return SPEC_ERR_ARG;
+  if (batch == 0) return SPEC_OK;
+  if (total_nodes < batch) return SPEC_ERR_ARG;
+  if (!parent || !draft_tokens || !target_logits || !qo_indptr || !accept_len || !path || !out_tokens)
+    return SPEC_ERR_ARG;
+  if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
+  const AcceptWs w = AcceptWs::make(batch, total_nodes, accept_chunks(total_nodes, vocab));
+  if (w.total > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // sizes beyond the fixed scratch
+  void* ws = noalloc_scratch();
+  if (ws == nullptr) return SPEC_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the counters must start at zero
+  if (cudaMemsetAsync(ws, 0, w.partials, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
+                       dev_status, st);
+}
