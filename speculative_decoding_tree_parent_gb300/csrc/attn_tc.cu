@@ -28,9 +28,11 @@
 // S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
 // does. Every wait is bounded.
 // When the keys are split (a short batch cannot fill 152 SMs otherwise), the launch
-// is cooperative: the split CTAs of a tile publish unnormalised partials (coalesced,
-// L2-resident), meet at a bounded arrival counter, and each merges a slice of the
-// tile's rows by log-sum-exp after staging it in shared memory — no second kernel.
+// is cooperative: the split CTAs of a tile publish partials (O / l rounded to bf16 plus
+// the split's log2-sum-exp; coalesced, L2-resident), meet at a bounded arrival counter,
+// and each merges a slice of the tile's rows by log-sum-exp after staging it in shared
+// memory — no second kernel. Rounding the normalised partials to bf16 adds at most
+// 2^-9 max|v| to the output error (the merge is a convex combination of them).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -74,8 +76,8 @@ struct TcParams {
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
-  float4* part_o;      // split partials [tile group][S][32 chunks][128 rows] (unnormalised O)
-  float2* part_ml;     // [tile group][S][128 rows] (running max in log2 units, row sum)
+  uint4* part_o;       // split partials [tile group][S][16 chunks][128 rows]: O / l in bf16, 8 per chunk
+  float* part_lse;     // [tile group][S][128 rows]: log2-sum-exp of the split's scores (-inf: empty)
   unsigned* counters;  // [tile group][2] arrivals / departures (zero between calls)
   int32_t* status;
 };
@@ -214,8 +216,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     if (warp == 0) {
-      // barriers, Q and the first block before the CTA-wide sync: their latency
-      // overlaps the TMEM allocation
+      // page ids (in flight while the barriers are set up), Q and the first block before
+      // the CTA-wide sync: their latency overlaps the TMEM allocation
+      pg_cur = fetch_pages(0);
+      pg_nxt = fetch_pages(1);
       if (lane == 0) {
         tc::mbar_init(bar_q, 1);
         for (int s = 0; s < kTcStages; ++s) {
@@ -239,8 +243,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       __syncwarp();
-      pg_cur = fetch_pages(0);
-      pg_nxt = fetch_pages(1);
       load_block(0);
     } else if (warp == 1) {
       tc::tmem_alloc(tc::smem_u32(&bars.tmem_base), kTmemCols);
@@ -427,9 +429,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = ok && warp_wait(bar_pv(tile), (nb - 1) & 1, abort);
       if (!ok && (threadIdx.x & 127) == 0) report(p.status, SPEC_ERR_TIMEOUT);
       tc::fence_after_sync();
-      // O row out of TMEM: final output when unsplit, else this split's partial
+      // O row out of TMEM: final output when unsplit, else this split's partial (O / l in
+      // bf16, 8 values per 16-byte chunk, chunk-major) and its log2-sum-exp m + log2(l)
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float4* po = p.part_o + ((size_t)grp * p.splits + split) * (kTcRows * kTcD / 4);
+      uint4* po = p.part_o + ((size_t)grp * p.splits + split) * (kTcRows * kTcD / 8);
 #pragma unroll 1
       for (int ch = 0; ch < kTcD / 32; ++ch) {
         float o[32];
@@ -440,27 +443,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
+        uint4 c8[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          c8[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                             pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                             pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                             pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
         if (p.splits == 1) {
           if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kTcD + ch * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                  pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                  pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                  pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+            for (int v = 0; v < 4; ++v) dst[v] = c8[v];
           }
         } else {  // chunk-major: a warp's 32 rows write 512 contiguous bytes per chunk
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            po[(ch * 8 + v) * kTcRows + row] = make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          for (int v = 0; v < 4; ++v) po[(ch * 4 + v) * kTcRows + row] = c8[v];
         }
       }
+      const float lse2 = (ok && l > 0.f) ? m_run + log2f(l) : -INFINITY;
       if (p.splits == 1) {
-        if (row_valid && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l)) * kLn2;
+        if (row_valid && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
       } else {
-        p.part_ml[((size_t)grp * p.splits + split) * kTcRows + row] =
-            ok ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+        p.part_lse[((size_t)grp * p.splits + split) * kTcRows + row] = lse2;
       }
       __syncwarp();
     }
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::tmem_dealloc(tbase, kTmemCols);
     }
   } else if (warp >= 2 && tile < ntiles) {  // empty key split: contributes nothing to the merge
-    p.part_ml[((size_t)grp * p.splits + split) * kTcRows + row] = make_float2(-INFINITY, 0.f);
+    p.part_lse[((size_t)grp * p.splits + split) * kTcRows + row] = -INFINITY;
   }
   if (p.splits == 1) return;
 
@@ -507,60 +512,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   {
     const int r0 = split * kTcRows / S, r1 = (split + 1) * kTcRows / S;
     const int R = r1 - r0;
-    const int per_tile = S * 32 * R;
-    float4* stage = reinterpret_cast<float4*>(smem + kOffKV);  // [t][s][chunk][R] (K/V ring + P: 160 KB)
-    float* wts = reinterpret_cast<float*>(smem + kOffQ);         // [t][R][S]      (Q region is free)
-    float* lse_r = reinterpret_cast<float*>(smem + kOffQ + 4096);
-    float2* mls = reinterpret_cast<float2*>(smem + kOffQ + 8192);  // [t][s][R]
+    const int per_tile = S * 16 * R;
+    uint4* stage = reinterpret_cast<uint4*>(smem + kOffKV);        // [t][s][chunk8][R]   (K/V ring)
+    float* wts = reinterpret_cast<float*>(smem + kOffQ);            // [t][R][S]           (Q region)
+    float* lse_r = reinterpret_cast<float*>(smem + kOffQ + 8192);   // [t][R]
+    float* lss = reinterpret_cast<float*>(smem + kOffQ + 12288);    // [t][s][R]
     for (int i = threadIdx.x; i < ntiles * per_tile; i += kTcThreads) {
       const int t = i / per_tile, rem = i - t * per_tile;
-      const int sp = rem / (32 * R), rem2 = rem - sp * 32 * R;
+      const int sp = rem / (16 * R), rem2 = rem - sp * 16 * R;
       const int c = rem2 / R, r = rem2 - c * R;
       const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
-      cp_async16(stage + i, p.part_o + (gt * S + sp) * (kTcRows * kTcD / 4) + c * kTcRows + r0 + r);
+      cp_async16(stage + i, p.part_o + (gt * S + sp) * (kTcRows * kTcD / 8) + c * kTcRows + r0 + r);
     }
     for (int i = threadIdx.x; i < ntiles * S * R; i += kTcThreads) {
       const int t = i / (S * R), rem = i - t * S * R;
       const int sp = rem / R, r = rem - sp * R;
       const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
-      mls[i] = __ldcg(p.part_ml + (gt * S + sp) * kTcRows + r0 + r);
+      lss[i] = __ldcg(p.part_lse + (gt * S + sp) * kTcRows + r0 + r);
     }
     cp_async_wait_all();
     __syncthreads();
-    for (int i = threadIdx.x; i < ntiles * R; i += kTcThreads) {
+    // merge weights: one warp per row, one lane per split (S <= 32)
+    for (int i = warp; i < ntiles * R; i += kTcThreads / 32) {
       const int t = i / R, r = i - t * R;
-      float M = -INFINITY;
-      for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mls[(t * S + sp) * R + r].x);
-      float L = 0.f;
-      for (int sp = 0; sp < S; ++sp) {
-        const float2 v = mls[(t * S + sp) * R + r];
-        const float f = v.x == -INFINITY ? 0.f : ex2_approx(v.x - M);
-        wts[(t * R + r) * S + sp] = f;
-        L = fmaf(v.y, f, L);
-      }
-      const float invL = L > 0.f ? 1.f / L : 0.f;
-      for (int sp = 0; sp < S; ++sp) wts[(t * R + r) * S + sp] *= invL;
-      lse_r[t * R + r] = (M + log2f(L)) * kLn2;
+      const float v = lane < S ? lss[(t * S + lane) * R + r] : -INFINITY;
+      float M = v;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = (v == -INFINITY) ? 0.f : ex2_approx(v - M);
+      float L = f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane < S) wts[(t * R + r) * S + lane] = L > 0.f ? f / L : 0.f;
+      if (lane == 0) lse_r[t * R + r] = (M + log2f(L)) * kLn2;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < ntiles * 32 * R; i += kTcThreads) {
-      const int t = i / (32 * R), rem = i - t * 32 * R;
+    for (int i = threadIdx.x; i < ntiles * 16 * R; i += kTcThreads) {
+      const int t = i / (16 * R), rem = i - t * 16 * R;
       const int c = rem / R, r = rem - c * R, rr = r0 + r;
       const int nl = node0 + t * npt + rr / G;
       if (nl >= N) continue;
       const float* w = wts + (t * R + r) * S;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int sp = 0; sp < S; ++sp) {
-        const float4 o = stage[((t * S + sp) * 32 + c) * R + r];
-        acc.x = fmaf(o.x, w[sp], acc.x);
-        acc.y = fmaf(o.y, w[sp], acc.y);
-        acc.z = fmaf(o.z, w[sp], acc.z);
-        acc.w = fmaf(o.w, w[sp], acc.w);
+        const uint4 q = stage[((t * S + sp) * 16 + c) * R + r];
+        const float ws = w[sp];
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = fmaf(__uint_as_float(u[k] << 16), ws, acc[2 * k]);
+          acc[2 * k + 1] = fmaf(__uint_as_float(u[k] & 0xFFFF0000u), ws, acc[2 * k + 1]);
+        }
       }
       const int hh = g * G + (rr - (rr / G) * G);
       const size_t orr = (size_t)(base + nl) * p.hq + hh;
-      *reinterpret_cast<uint2*>(p.out + orr * kTcD + c * 4) =
-          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      *reinterpret_cast<uint4*>(p.out + orr * kTcD + c * 8) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
       if (c == 0 && p.lse != nullptr) p.lse[orr] = lse_r[t * R + r];
     }
   }
@@ -645,8 +653,8 @@ struct TcWs {
     TcWs w;
     size_t off = 0;
     w.counters = off; off = align_up(off + 2 * sizeof(unsigned) * groups, 256);
-    w.ml = off;       off = align_up(off + sizeof(float2) * groups * splits * kTcRows, 256);
-    w.o = off;        off = align_up(off + sizeof(float) * groups * splits * kTcRows * kTcD, 256);
+    w.ml = off;       off = align_up(off + sizeof(float) * groups * splits * kTcRows, 256);
+    w.o = off;        off = align_up(off + sizeof(__nv_bfloat16) * groups * splits * kTcRows * kTcD, 256);
     w.total = off;
     return w;
   }
@@ -718,8 +726,8 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.lse = lse;
   const TcWs w = TcWs::make((long)batch * hkv * mtiles, splits);
   uint8_t* wb = static_cast<uint8_t*>(ws);
-  prm.part_o = splits > 1 ? reinterpret_cast<float4*>(wb + w.o) : nullptr;
-  prm.part_ml = splits > 1 ? reinterpret_cast<float2*>(wb + w.ml) : nullptr;
+  prm.part_o = splits > 1 ? reinterpret_cast<uint4*>(wb + w.o) : nullptr;
+  prm.part_lse = splits > 1 ? reinterpret_cast<float*>(wb + w.ml) : nullptr;
   prm.counters = splits > 1 ? reinterpret_cast<unsigned*>(wb + w.counters) : nullptr;
   prm.status = status;
   cudaLaunchConfig_t cfg = {};
