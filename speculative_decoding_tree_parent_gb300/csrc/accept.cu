@@ -118,10 +118,10 @@ __device__ __forceinline__ void chunk_range(int vocab, int c, int& lo, int& hi) 
 }
 
 // Greedy walk of one sequence by one warp: from the root, move to the first child
-// (lowest id) whose draft token equals the node's target argmax.
-__device__ void greedy_walk_warp(int b, int base, int n, const int32_t* __restrict__ parent,
-                                 const int32_t* __restrict__ tokens, const int* argmax, int path_cap,
-                                 int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+// (lowest id) whose draft token equals the node's target argmax. The three arrays hold
+// the sequence's nodes 0..n-1 (staged in shared memory by the caller).
+__device__ void greedy_walk_warp(int b, int n, const int* parent, const int* tokens, const int* argmax,
+                                 int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
                                  uint8_t* flags, int32_t* status) {
   const int lane = threadIdx.x & 31;
   int v = 0, L = 0, bonus = 0;
@@ -129,11 +129,11 @@ __device__ void greedy_walk_warp(int b, int base, int n, const int32_t* __restri
   int32_t* trow = out_tokens + (size_t)b * path_cap;
   if (lane == 0) prow[0] = 0;
   while (true) {
-    const int a = __ldcg(argmax + base + v);
+    const int a = argmax[v];
     int found = -1;
     for (int c0 = v + 1; c0 < n; c0 += 32) {
       const int c = c0 + lane;
-      const bool m = c < n && __ldg(parent + base + c) == v && __ldg(tokens + base + c) == a;
+      const bool m = c < n && parent[c] == v && tokens[c] == a;
       const unsigned bal = __ballot_sync(0xffffffffu, m);
       if (bal) {
         found = c0 + __ffs(bal) - 1;
@@ -152,7 +152,7 @@ __device__ void greedy_walk_warp(int b, int base, int n, const int32_t* __restri
     ++L;
     if (lane == 0) {
       prow[L] = found;
-      trow[L - 1] = __ldg(tokens + base + found);
+      trow[L - 1] = tokens[found];
     }
     v = found;
   }
@@ -249,9 +249,19 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(
     __threadfence();
   }
   __syncthreads();
-  if (!s_last || warp != 0) return;
-  greedy_walk_warp(b, base, n, parent, tokens, argmax, path_cap, accept_len, path, out_tokens, flags,
-                   status);
+  if (!s_last) return;
+  // last row of sequence b: stage the tree (parents, tokens, argmaxes) in shared memory
+  // with one round trip, then walk it there
+  __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes], s_am[kMaxTreeNodes];
+  const int nw = n < kMaxTreeNodes ? n : kMaxTreeNodes;
+  for (int i = threadIdx.x; i < nw; i += kAcceptThreads) {
+    s_par[i] = __ldg(parent + base + i);
+    s_tok[i] = __ldg(tokens + base + i);
+    s_am[i] = __ldcg(argmax + base + i);
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  greedy_walk_warp(b, nw, s_par, s_tok, s_am, path_cap, accept_len, path, out_tokens, flags, status);
 }
 
 // ---------------------------------------------------------------- stochastic: statistics

@@ -20,13 +20,29 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     int num_pages, int page_size, const int32_t* __restrict__ prefix_len,
     int32_t* __restrict__ seq_len_out, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
     int hkv, int row_bytes, int32_t* status) {
-  pdl_wait();  // accept_len / path come from the acceptance kernel just before
   const int b = blockIdx.x;
   __shared__ int s_ok;
   __shared__ int s_L;
+  // Everything the acceptance kernel does not write is read (or pulled into L2) before
+  // waiting for it: the sequence's bounds, its page-table entries past the prefix and
+  // its tree K/V rows (a few KB), so only accept_len / path remain on the critical path.
   const int base = __ldg(qo + b);
   const int n = __ldg(qo + b + 1) - base;
   const int P = __ldg(prefix_len + b);
+  {
+    const int span = n < path_cap ? n : path_cap;
+    const int lp0 = P / page_size, lp1 = (P + span - 1) / page_size;
+    for (int lp = lp0 + (int)threadIdx.x; lp <= lp1 && lp < max_pages; lp += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(page_table + (size_t)b * max_pages + lp));
+    const size_t bytes = (size_t)n * hkv * row_bytes;
+    const uint8_t* k0 = k_tree + (size_t)base * hkv * row_bytes;
+    const uint8_t* v0 = v_tree + (size_t)base * hkv * row_bytes;
+    for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)blockDim.x * 128) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(k0 + off));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(v0 + off));
+    }
+  }
+  pdl_wait();  // accept_len / path come from the acceptance kernel just before
   if (threadIdx.x == 0) {
     int L = __ldg(accept_len + b);
     int ok = 1;
