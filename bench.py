@@ -53,6 +53,35 @@ def _dist():
     return ws, rank, local
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+#
+# The verification step shards by sequence with no exchange step, so N ranks run N
+# independent replicas: each rank draws its own batch and steps it alone. The only
+# collectives are host-side bookkeeping around the timed region — a barrier on each side,
+# the max of the ranks' times and the sum of the tokens they verified.
+
+def replica_seed(index, rank):
+    """Seed of `rank`'s batch of workload `index`: rank 0 keeps the workload's own seed."""
+    return None if rank == 0 else index + 1000 * rank
+
+
+def reduce_over_ranks(x, op, ws, device=None):
+    """max / sum of a host float over the ranks (identity on one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op={"max": dist.ReduceOp.MAX, "sum": dist.ReduceOp.SUM}[op])
+    return float(t.item())
+
+
+def job_throughput(tokens_all_ranks, max_rank_ms):
+    """Whole-job tokens/s: every rank's verified tokens over the slowest rank's time."""
+    return tokens_all_ranks / (max_rank_ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- work counts
 
 def work_counts(inp, accept_len=None):
@@ -183,7 +212,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = W.generate_index(CONFIG_INDEX, seed=CONFIG_INDEX + 1000 * rank if rank else None)
+    inp = W.generate_index(CONFIG_INDEX, seed=replica_seed(CONFIG_INDEX, rank))
     # R device replicas of the batch (same values, separate buffers): one graph replay runs
     # R steps back to back, each on a replica the previous steps did not touch, so every
     # step reads its inputs from HBM (R x ~51 MB > the 129 MB L2); L2 is also flushed
@@ -251,11 +280,7 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) / R for ((a, b),) in ev_step]
     call_ms = {name: [ev_calls[r][i][0].elapsed_time(ev_calls[r][i][1]) / R for r in range(n_rep)]
                for i, name in enumerate(g_calls)}
-    total_ms = sum(step_ms) * R
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_over_ranks(sum(step_ms) * R, "max", ws, dev)
     assert all(rep.device_status() == 0 for rep in reps), [rep.device_status() for rep in reps]
 
     # ---- end-to-end through the C ABI with host buffers ------------------------------
@@ -281,18 +306,14 @@ def run_ours(args):
         b.synchronize()
         if r >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_total = sum(e2e_ms)
-    if ws > 1:
-        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = reduce_over_ranks(sum(e2e_ms), "max", ws, dev)
 
     # ---- figures ------------------------------------------------------------------------
     wc = work_counts(inp, db.accept_len.cpu().numpy())
     hbm, tfl, tfl_sus, peak_kind = _peaks()
     ms_step = total_ms / args.steps
-    tokens_all = wc["tokens"] * ws * args.steps
-    value = tokens_all / (total_ms / 1e3)
+    tokens_all = reduce_over_ranks(wc["tokens"], "sum", ws, dev) * args.steps
+    value = job_throughput(tokens_all, total_ms)
     t_attn = statistics.mean(call_ms["attention"]) / 1e3
     t_acc = statistics.mean(call_ms["accept"]) / 1e3
     t_com = statistics.mean(call_ms["commit"]) / 1e3
@@ -335,7 +356,7 @@ def run_ours(args):
                           "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
         "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
         "roofline": roof,
-        "e2e": {"value": tokens_all / (e2e_total / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+        "e2e": {"value": job_throughput(tokens_all, e2e_total), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_total / args.steps},
         # launches in the timed region: full-step replays + per-call replays (each call's kernels once)
         "gpu_launches": 2 * launches * args.steps,   # step replays + per-call replays, R steps each
