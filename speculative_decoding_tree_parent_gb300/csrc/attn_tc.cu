@@ -16,14 +16,16 @@
 // blocks of 64: prefix blocks are 4 pages of 16 tokens, TMA-loaded page by page
 // through the page table ([page][Hkv][16][128] bf16: a (page, head) is one 4 KB
 // tile; page ids are fetched a batch of 8 blocks ahead); tree blocks are 64 rows of
-// the dense tree K/V. Warp roles (320 threads):
+// the dense tree K/V. Warp roles (352 threads):
 //   warp 0      TMA producer: Q of both tiles, then K/V blocks into a 4-stage ring
-//   warp 1      TMEM allocation (512 columns); one lane issues the MMAs, per tile t:
+//   warp 1      TMEM allocation (512 columns); lane 0 issues the MMAs of tile 0,
+//   warp 10     lane 0 those of tile 1 (one issuing thread sustains only about one
+//               tcgen05.mma per 100 cycles, so each tile gets its own):
 //                 S_t[j%2] = Q_t K_j^T  (M 128, N 64, K 128; both operands K-major)
-//                 O_t     += P_t V_j    (M 128, N 128, K 64; V is MN-major)
+//                 O_t     += P_t V_j    (M 128, N 128, K 64; P from TMEM, V MN-major)
 //   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one query row per
 //               thread (its TMEM lane); S row -> max / exp2 / row sum in registers,
-//               P row -> bf16 in shared memory (128-byte swizzle), O rescaled in
+//               P row -> bf16 pairs in TMEM over the S it came from, O rescaled in
 //               TMEM only when the running max grows by more than 2^8.
 // S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
 // does. Every wait is bounded.
@@ -46,7 +48,7 @@ constexpr int kTcKeys = 64;
 constexpr int kTcD = 128;
 constexpr int kTcStages = 4;
 constexpr int kTiles = 2;
-constexpr int kTcThreads = 64 + kTiles * 128;
+constexpr int kTcThreads = 64 + kTiles * 128 + 32;  // + one more MMA-issuing warp
 constexpr float kRescaleThr = 8.0f;            // log2 units: P entries stay <= 2^8
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s) before a wait gives up
 
@@ -54,13 +56,11 @@ constexpr uint32_t kQSlab = kTcRows * 128;                  // 16 KB: 128 rows x
 constexpr uint32_t kQTile = 2 * kQSlab;
 constexpr uint32_t kKVSlab = kTcKeys * 128;                 // 8 KB: 64 keys x 64 bf16
 constexpr uint32_t kStageBytes = 4 * kKVSlab;               // K (2 slabs) + V (2 slabs)
-constexpr uint32_t kPBuf = kTcRows * 128;                   // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kTiles * kQTile;
-constexpr uint32_t kOffP = kOffKV + kTcStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffP + kTiles * kPBuf;
+constexpr uint32_t kOffBar = kOffKV + kTcStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;       // barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;                         // per tile: S0 | S1 | O
+constexpr uint32_t kTmemCols = 512;                         // per tile: S0 | S1 | O (P aliases S)
 constexpr uint32_t kIdescQK = tc::idesc_bf16(kTcRows, kTcKeys, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(kTcRows, kTcD, 1);
 static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
@@ -84,7 +84,7 @@ struct TcParams {
 
 struct TcBars {
   uint64_t q_full, kv_full[kTcStages], kv_empty[kTcStages];
-  uint64_t s_full[kTiles][2], p_full[kTiles], pv_done[kTiles], mma_fin;
+  uint64_t s_full[kTiles][2], p_full[kTiles], pv_done[kTiles], mma_fin[kTiles];
   uint32_t tmem_base;
   int abort;
   int go;
@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (nb > 0) {
     const uint32_t bar_q = tc::smem_u32(&bars.q_full);
-    const uint32_t bar_fin = tc::smem_u32(&bars.mma_fin);
     auto bar_kvf = [&](int s) { return tc::smem_u32(&bars.kv_full[s]); };
     auto bar_kve = [&](int s) { return tc::smem_u32(&bars.kv_empty[s]); };
     auto bar_sf = [&](int t, int s) { return tc::smem_u32(&bars.s_full[t][s]); };
@@ -224,15 +223,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::mbar_init(bar_q, 1);
         for (int s = 0; s < kTcStages; ++s) {
           tc::mbar_init(bar_kvf(s), 1);
-          tc::mbar_init(bar_kve(s), 1);
+          tc::mbar_init(bar_kve(s), ntiles);  // released by each tile's PV
         }
         for (int t = 0; t < kTiles; ++t) {
           tc::mbar_init(bar_sf(t, 0), 1);
           tc::mbar_init(bar_sf(t, 1), 1);
           tc::mbar_init(bar_pf(t), 128);
           tc::mbar_init(bar_pv(t), 1);
+          tc::mbar_init(tc::smem_u32(&bars.mma_fin[t]), 1);
         }
-        tc::mbar_init(bar_fin, 1);
         bars.abort = 0;
         tc::mbar_fence_init();
         tc::mbar_arrive_expect_tx(bar_q, ntiles * kQTile);
@@ -271,21 +270,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::mbar_wait(bar_kvf(j % kTcStages), (j / kTcStages) & 1, &zero, kWaitLimit);
         tc::mbar_wait(bar_q, 0, &zero, kWaitLimit);
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+    } else if (warp == 1 || warp == kTcThreads / 32 - 1) {
+      // ---------------------------------------------------------------- MMA issuers
+      // One issuing thread per M-tile (warp 1: tile 0, the last warp: tile 1): a thread
+      // issues one tcgen05.mma about every 100 cycles whatever the shape, so two issuers
+      // keep the tensor pipe twice as busy as one.
+      const int t = warp == 1 ? 0 : 1;
+      if (lane == 0 && t < ntiles) {
+        const uint32_t qbuf = s_base + kOffQ + t * kQTile;
         auto qk = [&](int j) {
           const uint32_t kbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes;
-          for (int t = 0; t < ntiles; ++t) {
-            const uint32_t qbuf = s_base + kOffQ + t * kQTile;
 #pragma unroll
-            for (int k = 0; k < kTcD / 16; ++k) {
-              const uint64_t a = tc::sdesc_sw128(qbuf + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
-              const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
-              tc::mma_bf16(tbase + t * 256 + (j & 1) * 64, a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(bar_sf(t, j & 1));
+          for (int k = 0; k < kTcD / 16; ++k) {
+            const uint64_t a = tc::sdesc_sw128(qbuf + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
+            const uint64_t bdesc = tc::sdesc_sw128(kbuf + (k >> 2) * kKVSlab + (k & 3) * 32, 16, 1024);
+            tc::mma_bf16(tbase + t * 256 + (j & 1) * 64, a, bdesc, kIdescQK, k > 0 ? 1u : 0u);
           }
+          tc::mma_commit(bar_sf(t, j & 1));
         };
         bool ok = tc::mbar_wait(bar_q, 0, abort, kWaitLimit) &&
                   tc::mbar_wait(bar_kvf(0), 0, abort, kWaitLimit);
@@ -304,25 +305,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             qk(j + 1);
           }
           const uint32_t vbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes + 2 * kKVSlab;
-          for (int t = 0; t < ntiles && ok; ++t) {
-            if (!tc::mbar_wait(bar_pf(t), j & 1, abort, kWaitLimit)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            const uint32_t pbuf = s_base + kOffP + t * kPBuf;
-#pragma unroll
-            for (int k = 0; k < kTcKeys / 16; ++k) {
-              const uint64_t a = tc::sdesc_sw128(pbuf + k * 32, 16, 1024);
-              const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
-              tc::mma_bf16(tbase + t * 256 + 128, a, bdesc, kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-            }
-            tc::mma_commit(bar_pv(t));
+          if (!tc::mbar_wait(bar_pf(t), j & 1, abort, kWaitLimit)) {
+            ok = false;
+            break;
           }
-          if (ok) tc::mma_commit(bar_kve(j % kTcStages));
+          tc::fence_after_sync();
+          // P(j) sits in the first 32 columns of S buffer j % 2 (bf16 pairs); the QK that
+          // next overwrites that buffer is issued after this PV by this thread (in order)
+#pragma unroll
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint64_t bdesc = tc::sdesc_sw128(vbuf + k * 2048, kKVSlab, 1024);
+            tc::mma_bf16_ts(tbase + t * 256 + 128, tbase + t * 256 + (j & 1) * 64 + 8 * k, bdesc, kIdescPV,
+                            (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(bar_pv(t));
+          tc::mma_commit(bar_kve(j % kTcStages));
         }
         if (!ok) report(p.status, SPEC_ERR_TIMEOUT);
-        // every MMA issued has completed before TMEM is released
+        // every MMA this thread issued has completed before TMEM is released
+        const uint32_t bar_fin = tc::smem_u32(&bars.mma_fin[t]);
         tc::mma_commit(bar_fin);
         int zero = 0;
         tc::mbar_wait(bar_fin, 0, &zero, kWaitLimit);
@@ -333,7 +334,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t t_lane = tbase + tile * 256 + ((uint32_t)((warp & 3) * 32) << 16);
       const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
       const float sl2 = p.scale_log2;
-      uint8_t* prow = smem + kOffP + tile * kPBuf + row * 128;
       float m_run = -INFINITY, l = 0.f;
       bool ok = true;
       bool mask_ready = false;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
         l = l * alpha + ((r0 + r1) + (r2 + r3));
-        if (j >= 1) {  // PV of the previous block done: O is stable and the P buffer is free
+        if (j >= 1) {  // PV of the previous block done: O is stable
           if (!warp_wait(bar_pv(tile), (j - 1) & 1, abort)) {
             ok = false;
             break;
@@ -416,13 +416,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::tmem_wait_st();
         }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int phys = cc ^ (row & 7);
-          *reinterpret_cast<uint4*>(prow + phys * 16) =
-              make_uint4(packed[4 * cc], packed[4 * cc + 1], packed[4 * cc + 2], packed[4 * cc + 3]);
-        }
-        tc::fence_proxy_async_smem();
+        // P(j) into the S buffer it came from (S(j) is in registers now)
+        tc::tmem_st32_u(t_lane + (j & 1) * 64, packed);
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(bar_pf(tile));
       }
@@ -476,7 +472,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_after_sync();
       tc::tmem_dealloc(tbase, kTmemCols);
     }
-  } else if (warp >= 2 && tile < ntiles) {  // empty key split: contributes nothing to the merge
+  } else if (warp >= 2 && warp < 2 + 4 * kTiles && tile < ntiles) {  // empty key split: contributes nothing to the merge
     p.part_lse[((size_t)grp * p.splits + split) * kTcRows + row] = -INFINITY;
   }
   if (p.splits == 1) return;
