@@ -29,12 +29,12 @@
 //               TMEM only when the running max grows by more than 2^8.
 // S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
 // does. Every wait is bounded.
-// When the keys are split (a short batch cannot fill 152 SMs otherwise), the launch
-// is cooperative: the split CTAs of a tile publish partials (O / l rounded to bf16 plus
-// the split's log2-sum-exp; coalesced, L2-resident), meet at a bounded arrival counter,
-// and each merges a slice of the tile's rows by log-sum-exp after staging it in shared
-// memory — no second kernel. Rounding the normalised partials to bf16 adds at most
-// 2^-9 max|v| to the output error (the merge is a convex combination of them).
+// When the keys are split (a short batch cannot fill 152 SMs otherwise), each split CTA
+// writes a partial per tile (O / l rounded to bf16 plus the split's log2-sum-exp;
+// coalesced, L2-resident) and a small merge kernel, launched with programmatic
+// serialization so it is resident before this grid ends, combines them by log-sum-exp.
+// Rounding the normalised partials to bf16 adds at most 2^-9 max|v| to the output error
+// (the merge is a convex combination of them).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -76,9 +76,9 @@ struct TcParams {
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
-  uint4* part_o;       // split partials [tile group][S][16 chunks][128 rows]: O / l in bf16, 8 per chunk
+  uint4* part_o;       // split partials [tile group][S][128 rows][16 chunks]: O / l in bf16, 8 per chunk,
+                       // chunk c of row r at position c ^ (r % 16)
   float* part_lse;     // [tile group][S][128 rows]: log2-sum-exp of the split's scores (-inf: empty)
-  unsigned* counters;  // [tile group][2] arrivals / departures (zero between calls)
   int32_t* status;
 };
 
@@ -87,7 +87,6 @@ struct TcBars {
   uint64_t s_full[kTiles][2], p_full[kTiles], pv_done[kTiles], mma_fin[kTiles];
   uint32_t tmem_base;
   int abort;
-  int go;
 };
 
 // One lane waits, the whole warp gets the answer: keeps warp-collective tcgen05.ld/st
@@ -109,18 +108,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* ptr) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(smem_dst)), "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
@@ -131,6 +118,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t s_base = tc::smem_u32(smem);
 
   const int split = blockIdx.x, pair = blockIdx.y, bg = blockIdx.z;
+  // the split merge (launched next) may be scheduled now: it waits for this grid to end
+  pdl_trigger();
+  if (threadIdx.x == 0) {  // descriptor fetches overlap the first loads of qo / prefix_len
+    tc::prefetch_tmap(&tm_q);
+    tc::prefetch_tmap(&tm_kp);
+    tc::prefetch_tmap(&tm_vp);
+    tc::prefetch_tmap(&tm_kt);
+    tc::prefetch_tmap(&tm_vt);
+  }
   const int G = p.G;
   const int b = bg / p.hkv, g = bg - (bg / p.hkv) * p.hkv;
   const int base = __ldg(p.qo + b);
@@ -475,109 +471,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= 2 && warp < 2 + 4 * kTiles && tile < ntiles) {  // empty key split: contributes nothing to the merge
     p.part_lse[((size_t)grp * p.splits + split) * kTcRows + row] = -INFINITY;
   }
-  if (p.splits == 1) return;
+}
 
-  // ------------------------------------------------------------------ merge of the splits
-  // The launch is cooperative (every CTA resident at once), so the S split CTAs of a tile
-  // can wait for one another: each publishes its partial, bumps the tile's arrival count,
-  // waits (bounded) until all S arrived, stages rows [s*128/S, (s+1)*128/S) of every
-  // partial into shared memory (cp.async, one round trip), merges them by log-sum-exp
-  // and writes the bf16 output and the lse. The last CTA to leave resets the counters.
-  const int S = p.splits;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    for (int t = 0; t < ntiles; ++t) atomicAdd(p.counters + 2 * ((2 * pair + t) + p.mtiles * bg), 1u);
-    int go = 1;
-    const long long t0 = clock64();
-    for (int t = 0; t < ntiles && go; ++t) {
-      const unsigned* c = p.counters + 2 * ((2 * pair + t) + p.mtiles * bg);
-      while (ld_acquire_u32(c) < (unsigned)S) {
-        if (clock64() - t0 > kWaitLimit) {
-          report(p.status, SPEC_ERR_TIMEOUT);
-          go = 0;
-          break;
-        }
-        __nanosleep(32);
-      }
-    }
-    bars.go = go;
-  }
-  __syncthreads();
-  if (!bars.go) return;
-  {
-    const int r0 = split * kTcRows / S, r1 = (split + 1) * kTcRows / S;
-    const int R = r1 - r0;
-    const int per_tile = S * 16 * R;
-    uint4* stage = reinterpret_cast<uint4*>(smem + kOffKV);        // [t][s][chunk8][R]   (K/V ring)
-    float* wts = reinterpret_cast<float*>(smem + kOffQ);            // [t][R][S]           (Q region)
-    float* lse_r = reinterpret_cast<float*>(smem + kOffQ + 8192);   // [t][R]
-    float* lss = reinterpret_cast<float*>(smem + kOffQ + 12288);    // [t][s][R]
-    for (int i = threadIdx.x; i < ntiles * per_tile; i += kTcThreads) {
-      const int t = i / per_tile, rem = i - t * per_tile;
-      const int sp = rem / (16 * R), rem2 = rem - sp * 16 * R;
-      const int c = rem2 / R, r = rem2 - c * R;
-      const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
-      cp_async16(stage + i, p.part_o + (gt * S + sp) * (kTcRows * kTcD / 8) + c * kTcRows + r0 + r);
-    }
-    for (int i = threadIdx.x; i < ntiles * S * R; i += kTcThreads) {
-      const int t = i / (S * R), rem = i - t * S * R;
-      const int sp = rem / R, r = rem - sp * R;
-      const size_t gt = (size_t)(2 * pair + t) + (size_t)p.mtiles * bg;
-      lss[i] = __ldcg(p.part_lse + (gt * S + sp) * kTcRows + r0 + r);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // merge weights: one warp per row, one lane per split (S <= 32)
-    for (int i = warp; i < ntiles * R; i += kTcThreads / 32) {
-      const int t = i / R, r = i - t * R;
-      const float v = lane < S ? lss[(t * S + lane) * R + r] : -INFINITY;
-      float M = v;
+// ------------------------------------------------------------------ merge of the key splits
+// One thread per (tile group, 16-byte chunk, row): a warp reads 32 consecutive rows of one
+// chunk, 512 contiguous bytes per split. Launched with programmatic serialization right
+// after the attention kernel (which lets it start at once): it waits for that grid to
+// finish, then O = sum_s 2^(lse_s - M) O_s / L with M = max_s lse_s, L = sum_s 2^(lse_s - M),
+// and the row's log-sum-exp M + log2 L (natural log on output).
+struct TcMergeParams {
+  const uint4* part_o;
+  const float* part_lse;
+  const int32_t* qo;
+  int splits, mtiles, hkv, hq, G;
+  long groups;
+  __nv_bfloat16* out;
+  float* lse;
+};
+
+constexpr int kMergeThreads = 128;
+constexpr int kMaxSplits = 32;  // attn_splits_tc never returns more
+
+__global__ void __launch_bounds__(kMergeThreads) attn_tc_merge_kernel(const TcMergeParams p) {
+  const long idx = (long)blockIdx.x * kMergeThreads + threadIdx.x;
+  if (idx >= p.groups * 16 * kTcRows) return;
+  const int gt = (int)(idx / (16 * kTcRows));
+  const int rem = (int)(idx - (long)gt * 16 * kTcRows);
+  const int c = rem / kTcRows, r = rem - (rem / kTcRows) * kTcRows;
+  const int tt = gt % p.mtiles, bg = gt / p.mtiles;
+  const int b = bg / p.hkv, g = bg - (bg / p.hkv) * p.hkv;
+  const int G = p.G;
+  const int node_l = tt * (kTcRows / G) + r / G;
+  const int base = __ldg(p.qo + b);  // qo is an input: safe to read before the wait
+  if (node_l >= __ldg(p.qo + b + 1) - base) return;
+  pdl_wait();  // the attention grid has finished: its partials are visible
+  // every load is issued before any arithmetic needs it: the split statistics in one
+  // round trip, then the partial rows eight splits at a time
+  const int S = p.splits;  // <= kMaxSplits
+  const float* ls = p.part_lse + (size_t)gt * S * kTcRows + r;
+  float lv[kMaxSplits];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float f = (v == -INFINITY) ? 0.f : ex2_approx(v - M);
-      float L = f;
+  for (int s = 0; s < kMaxSplits; ++s) lv[s] = s < S ? __ldcg(ls + (size_t)s * kTcRows) : -INFINITY;
+  float M = -INFINITY;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane < S) wts[(t * R + r) * S + lane] = L > 0.f ? f / L : 0.f;
-      if (lane == 0) lse_r[t * R + r] = (M + log2f(L)) * kLn2;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < ntiles * 16 * R; i += kTcThreads) {
-      const int t = i / (16 * R), rem = i - t * 16 * R;
-      const int c = rem / R, r = rem - c * R, rr = r0 + r;
-      const int nl = node0 + t * npt + rr / G;
-      if (nl >= N) continue;
-      const float* w = wts + (t * R + r) * S;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int sp = 0; sp < S; ++sp) {
-        const uint4 q = stage[((t * S + sp) * 16 + c) * R + r];
-        const float ws = w[sp];
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+  for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, lv[s]);
+  float L = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint4* po = p.part_o + (size_t)gt * S * (kTcRows * kTcD / 8) + c * kTcRows + r;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[2 * k] = fmaf(__uint_as_float(u[k] << 16), ws, acc[2 * k]);
-          acc[2 * k + 1] = fmaf(__uint_as_float(u[k] & 0xFFFF0000u), ws, acc[2 * k + 1]);
-        }
-      }
-      const int hh = g * G + (rr - (rr / G) * G);
-      const size_t orr = (size_t)(base + nl) * p.hq + hh;
-      *reinterpret_cast<uint4*>(p.out + orr * kTcD + c * 8) =
-          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                     pack_bf16x2(acc[6], acc[7]));
-      if (c == 0 && p.lse != nullptr) p.lse[orr] = lse_r[t * R + r];
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int t = 0; t < ntiles; ++t) {
-      unsigned* c = p.counters + 2 * ((2 * pair + t) + p.mtiles * bg);
-      if (atomicAdd(c + 1, 1u) == (unsigned)(S - 1)) {  // every split CTA has left its wait
-        c[0] = 0u;
-        c[1] = 0u;
+  for (int s0 = 0; s0 < kMaxSplits; s0 += 8) {
+    if (s0 >= S) break;
+    uint4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)  // an empty split (lse -inf) wrote no partial: not read
+      q[u] = lv[s0 + u] > -INFINITY ? __ldcg(po + (size_t)(s0 + u) * (kTcRows * kTcD / 8)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = lv[s0 + u] > -INFINITY ? ex2_approx(lv[s0 + u] - M) : 0.f;
+      L += w;
+      const uint32_t uu[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[2 * k] = fmaf(__uint_as_float(uu[k] << 16), w, acc[2 * k]);
+        acc[2 * k + 1] = fmaf(__uint_as_float(uu[k] & 0xFFFF0000u), w, acc[2 * k + 1]);
       }
     }
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int head = g * G + (r - (r / G) * G);
+  const size_t orow = (size_t)(base + node_l) * p.hq + head;
+  *reinterpret_cast<uint4*>(p.out + orow * kTcD + c * 8) =
+      make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                 pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+  if (c == 0 && p.lse != nullptr) p.lse[orow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------------------ host
@@ -639,16 +605,15 @@ int attn_splits_tc(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
   const int blocks = ceil_div(max_prefix, kTcKeys) + ceil_div(max_nodes, kTcKeys);
   long s = items > 0 ? sm_count() / items : 1;
   if (s > blocks / 2) s = blocks / 2;
-  if (s > 32) s = 32;
+  if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : (int)s;
 }
 
 struct TcWs {
-  size_t counters, ml, o, total;
+  size_t ml, o, total;
   static TcWs make(long groups, int splits) {
     TcWs w;
     size_t off = 0;
-    w.counters = off; off = align_up(off + 2 * sizeof(unsigned) * groups, 256);
     w.ml = off;       off = align_up(off + sizeof(float) * groups * splits * kTcRows, 256);
     w.o = off;        off = align_up(off + sizeof(__nv_bfloat16) * groups * splits * kTcRows * kTcD, 256);
     w.total = off;
@@ -720,32 +685,44 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.scale_log2 = sm_scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
-  const TcWs w = TcWs::make((long)batch * hkv * mtiles, splits);
+  const long groups = (long)batch * hkv * mtiles;
+  const TcWs w = TcWs::make(groups, splits);
   uint8_t* wb = static_cast<uint8_t*>(ws);
   prm.part_o = splits > 1 ? reinterpret_cast<uint4*>(wb + w.o) : nullptr;
   prm.part_lse = splits > 1 ? reinterpret_cast<float*>(wb + w.ml) : nullptr;
-  prm.counters = splits > 1 ? reinterpret_cast<unsigned*>(wb + w.counters) : nullptr;
   prm.status = status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(splits, ceil_div(mtiles, kTiles), batch * hkv);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
+  // programmatic serialization: the prologue (barriers, TMEM, Q and first K/V loads)
+  // overlaps the mask kernel; the softmax waits for it before the first tree block
   cudaLaunchAttribute attr[1];
-  if (splits > 1) {
-    // the split merge waits on sibling CTAs: all of them must be resident at once
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-  } else {
-    // programmatic serialization: the prologue (barriers, TMEM, Q and first K/V loads)
-    // overlaps the mask kernel; the softmax waits for it before the first tree block
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, attn_tc_kernel, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  if (splits > 1) {
+    TcMergeParams mp;
+    mp.part_o = prm.part_o;
+    mp.part_lse = prm.part_lse;
+    mp.qo = qo;
+    mp.splits = splits;
+    mp.mtiles = mtiles;
+    mp.hkv = hkv;
+    mp.hq = hq;
+    mp.G = G;
+    mp.groups = groups;
+    mp.out = prm.out;
+    mp.lse = lse;
+    const long threads = groups * 16 * kTcRows;
+    if (launch_pdl(attn_tc_merge_kernel, dim3((unsigned)ceil_div(threads, (long)kMergeThreads)),
+                   dim3(kMergeThreads), 0, stream, mp) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -96,12 +96,11 @@ class DeviceBatch:
         return self.launches_per_step(mode)
 
     def launches_per_step(self, mode=None):
-        """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the CUDA-core
-        path splits the keys; the tensor-core path merges inside its cluster), accept 1 (greedy)
-        or 2 (stochastic), commit 1."""
+        """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the keys are
+        split), accept 1 (greedy) or 2 (stochastic), commit 1."""
         mode = mode or self.mode
-        splits, tc = self.attn_plan()
-        attn = 2 if (splits > 1 and not tc) else 1
+        splits, _ = self.attn_plan()
+        attn = 2 if splits > 1 else 1
         return 1 + attn + (2 if mode == "stochastic" else 1) + 1
 
     def attn_plan(self):
