@@ -492,6 +492,9 @@ struct TcMergeParams {
 constexpr int kMergeThreads = 128;
 constexpr int kMaxSplits = 32;  // attn_splits_tc never returns more
 
+// MAXS >= splits: the unrolled load batch, sized to the launch so the registers stay few
+// enough for a merge CTA to sit beside an attention CTA on one SM.
+template <int MAXS>
 __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge_kernel(const TcMergeParams p) {
   const long idx = (long)blockIdx.x * kMergeThreads + threadIdx.x;
   if (idx >= p.groups * 16 * kTcRows) return;
@@ -505,36 +508,33 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge_kernel(const TcMe
   const int base = __ldg(p.qo + b);  // qo is an input: safe to read before the wait
   if (node_l >= __ldg(p.qo + b + 1) - base) return;
   pdl_wait();  // the attention grid has finished: its partials are visible
-  // every load is issued before any arithmetic needs it: the split statistics in one
-  // round trip, then the partial rows eight splits at a time
-  const int S = p.splits;  // <= kMaxSplits
+  // every load (split statistics and partial rows) is issued before any is used: one
+  // round trip to L2
+  const int S = p.splits;  // <= MAXS
   const float* ls = p.part_lse + (size_t)gt * S * kTcRows + r;
-  float lv[kMaxSplits];
+  const uint4* po = p.part_o + (size_t)gt * S * (kTcRows * kTcD / 8) + c * kTcRows + r;
+  float lv[MAXS];
+  uint4 q[MAXS];
 #pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) lv[s] = s < S ? __ldcg(ls + (size_t)s * kTcRows) : -INFINITY;
+  for (int s = 0; s < MAXS; ++s) {
+    lv[s] = s < S ? __ldcg(ls + (size_t)s * kTcRows) : -INFINITY;
+    q[s] = s < S ? __ldcg(po + (size_t)s * (kTcRows * kTcD / 8)) : make_uint4(0, 0, 0, 0);
+  }
   float M = -INFINITY;
 #pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, lv[s]);
+  for (int s = 0; s < MAXS; ++s) M = fmaxf(M, lv[s]);
   float L = 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint4* po = p.part_o + (size_t)gt * S * (kTcRows * kTcD / 8) + c * kTcRows + r;
 #pragma unroll
-  for (int s0 = 0; s0 < kMaxSplits; s0 += 8) {
-    if (s0 >= S) break;
-    uint4 q[8];
+  for (int s = 0; s < MAXS; ++s) {
+    if (lv[s] == -INFINITY) continue;  // an empty split (or s >= S): its row holds no partial
+    const float w = ex2_approx(lv[s] - M);
+    L += w;
+    const uint32_t uu[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
 #pragma unroll
-    for (int u = 0; u < 8; ++u)  // an empty split (lse -inf) wrote no partial: not read
-      q[u] = lv[s0 + u] > -INFINITY ? __ldcg(po + (size_t)(s0 + u) * (kTcRows * kTcD / 8)) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float w = lv[s0 + u] > -INFINITY ? ex2_approx(lv[s0 + u] - M) : 0.f;
-      L += w;
-      const uint32_t uu[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[2 * k] = fmaf(__uint_as_float(uu[k] << 16), w, acc[2 * k]);
-        acc[2 * k + 1] = fmaf(__uint_as_float(uu[k] & 0xFFFF0000u), w, acc[2 * k + 1]);
-      }
+    for (int k = 0; k < 4; ++k) {
+      acc[2 * k] = fmaf(__uint_as_float(uu[k] << 16), w, acc[2 * k]);
+      acc[2 * k + 1] = fmaf(__uint_as_float(uu[k] & 0xFFFF0000u), w, acc[2 * k + 1]);
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -719,9 +719,13 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
     mp.out = prm.out;
     mp.lse = lse;
     const long threads = groups * 16 * kTcRows;
-    if (launch_pdl(attn_tc_merge_kernel, dim3((unsigned)ceil_div(threads, (long)kMergeThreads)),
-                   dim3(kMergeThreads), 0, stream, mp) != cudaSuccess)
-      return SPEC_ERR_CUDA;
+    const dim3 grid((unsigned)ceil_div(threads, (long)kMergeThreads)), block(kMergeThreads);
+    cudaError_t e;
+    if (splits <= 8) e = launch_pdl(attn_tc_merge_kernel<8>, grid, block, 0, stream, mp);
+    else if (splits <= 16) e = launch_pdl(attn_tc_merge_kernel<16>, grid, block, 0, stream, mp);
+    else if (splits <= 24) e = launch_pdl(attn_tc_merge_kernel<24>, grid, block, 0, stream, mp);
+    else e = launch_pdl(attn_tc_merge_kernel<kMaxSplits>, grid, block, 0, stream, mp);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
