@@ -11,11 +11,12 @@
 // the children of a node one after another.
 //
 // Greedy, one launch:
-//   accept_argmax_kernel   grid = chunks x nodes. Each CTA streams one chunk of one
-//                          logits row with 16-byte loads and keeps (max, first index).
-//                          The last CTA of a row (atomic counter, no waiting) merges
-//                          the chunk partials into argmax[t]; the last row of a
-//                          sequence then runs the walk in one warp.
+//   accept_greedy_kernel   one wave of CTAs streams every logits row in 4096-logit
+//                          tasks (16-byte loads, the next task's loads in flight while
+//                          the current one is reduced) and keeps (max, first index)
+//                          per task. The last CTA to finish (atomic counter, no
+//                          waiting) merges the partials into every row's argmax and
+//                          walks every sequence, one warp each.
 // Stochastic, two launches:
 //   accept_stats_kernel    grid = chunks x nodes. Per row of target and draft logits:
 //                          max and sum of exp((x - max) / T) (fp32 elements, Kahan
@@ -53,7 +54,7 @@ constexpr int kMaxTreeNodes = 1024;
 constexpr double kTieEps = 1e-6;    // ratio test near-tie band (absolute)
 constexpr double kBonusEps = 1e-8;  // bonus draw near-tie band (relative to the residual's total)
 
-struct ArgPartial {
+struct alignas(8) ArgPartial {
   float v;
   int i;
 };
@@ -167,101 +168,197 @@ __device__ void greedy_walk_warp(int b, int n, const int* parent, const int* tok
   }
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(
-    const float* __restrict__ logits, int vocab, int chunks, const int32_t* __restrict__ qo,
-    int batch, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
-    int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
-    unsigned* node_cnt, unsigned* seq_cnt, ArgPartial* partials, int* argmax, int32_t* status) {
-  const int t = blockIdx.x / chunks;
-  const int c = blockIdx.x - t * chunks;
-  int lo, hi;
+// Greedy argmax + walk, one launch. A task is one chunk of kGreedyChunk logits of one
+// row; the grid is one wave of CTAs (as many as fit on the SMs at once) and CTA i takes
+// tasks i, i + grid, ... with the loads of its next task issued before the current one
+// is reduced, so every SM keeps two tasks of loads in flight until the stream ends. A
+// task leaves one (max, first index) partial. The last CTA to finish (one counter,
+// no waiting) merges the partials of every row and walks every sequence, one warp per
+// sequence, on the tree staged in shared memory.
+constexpr int kGreedyVec = 4;                                  // float4 per thread per task
+constexpr int kGreedyChunk = kAcceptThreads * kGreedyVec * 4;  // 4096 logits
+constexpr int kGreedyStage = 2048;                             // nodes the final CTA stages
 
-  chunk_range(vocab, c, lo, hi);
-  const float* row = logits + (size_t)t * vocab;
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  if (kVec) {
-    const float4* r4 = reinterpret_cast<const float4*>(row);
-    const int q0 = lo >> 2, q1 = hi >> 2;  // hi is a multiple of 4 when vocab is
-    float4 x[kVecPerThread];
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int j = q0 + threadIdx.x + u * kAcceptThreads;
-      x[u] = j < q1 ? __ldcs(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int e = (q0 + threadIdx.x + u * kAcceptThreads) << 2;
-      if (e < hi) {
-        arg_better(bv, bi, x[u].x, e);
-        arg_better(bv, bi, x[u].y, e + 1);
-        arg_better(bv, bi, x[u].z, e + 2);
-        arg_better(bv, bi, x[u].w, e + 3);
-      }
-    }
-  } else {
-    for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) arg_better(bv, bi, __ldcs(row + e), e);
+int greedy_chunks(int vocab) { return ceil_div(vocab, kGreedyChunk); }
+
+// The same walk on a tree staged in shared memory, in two steps: every node c > 0 whose
+// draft token equals its parent's argmax offers itself to the parent (atomicMin keeps the
+// lowest id), then the warp follows the offers from the root. `child` is scratch of n
+// entries.
+__device__ void greedy_walk_warp_staged(int b, int n, const int* parent, const int* tokens, const int* argmax,
+                                        int* child, int path_cap, int32_t* accept_len, int32_t* path,
+                                        int32_t* out_tokens, uint8_t* flags, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  for (int c = lane; c < n; c += 32) child[c] = INT_MAX;
+  __syncwarp();
+  for (int c = 1 + lane; c < n; c += 32) {
+    const int v = parent[c];
+    if (v >= 0 && v < c && tokens[c] == argmax[v]) atomicMin(child + v, c);
   }
-  warp_arg_reduce(bv, bi);
-  __shared__ float sv[kAcceptThreads / 32];
-  __shared__ int si[kAcceptThreads / 32];
+  __syncwarp();
+  int32_t* prow = path + (size_t)b * path_cap;
+  int32_t* trow = out_tokens + (size_t)b * path_cap;
+  if (lane == 0) {
+    int v = 0, L = 0;
+    prow[0] = 0;
+    while (child[v] != INT_MAX) {
+      if (L + 1 >= path_cap) {  // accepted path does not fit: truncate here
+        report(status, SPEC_ERR_CAPACITY);
+        break;
+      }
+      const int c = child[v];
+      ++L;
+      prow[L] = c;
+      trow[L - 1] = tokens[c];
+      v = c;
+    }
+    trow[L] = argmax[v];
+    accept_len[b] = L;
+    if (flags != nullptr) flags[b] = 0;
+    child[0] = L;  // hand L to the lanes through shared memory
+  }
+  __syncwarp();
+  const int L = child[0];
+  for (int k = L + 1 + lane; k < path_cap; k += 32) {
+    prow[k] = -1;
+    trow[k] = -1;
+  }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kAcceptThreads) accept_greedy_kernel(
+    const float* __restrict__ logits, int vocab, int gchunks, int tasks, const int32_t* __restrict__ qo,
+    int batch, int total_nodes, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
+    int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, unsigned* done,
+    ArgPartial* partials, int* argmax, int32_t* status) {
+  __shared__ float sv[2][kAcceptThreads / 32];
+  __shared__ int si[2][kAcceptThreads / 32];
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sv[warp] = bv;
-    si[warp] = bi;
+  pdl_wait();  // stream order: nothing is read before the previous kernel has finished
+  if (blockIdx.x == gridDim.x - 1) {  // the tree arrays the last CTA stages: into L2 early
+    for (int i = threadIdx.x * 32; i < total_nodes; i += kAcceptThreads * 32) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(parent + i));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(tokens + i));
+    }
   }
-  __syncthreads();
+
+  auto bounds = [&](int task, int& t, int& lo, int& hi) {
+    t = task / gchunks;
+    lo = (task - t * gchunks) * kGreedyChunk;
+    hi = lo + kGreedyChunk < vocab ? lo + kGreedyChunk : vocab;
+  };
+  auto load = [&](int task, float4* x) {
+    int t, lo, hi;
+    bounds(task, t, lo, hi);
+    const float4* r4 = reinterpret_cast<const float4*>(logits + (size_t)t * vocab);
+    const int q1 = hi >> 2;  // vocab % 4 == 0 on this path
+#pragma unroll
+    for (int u = 0; u < kGreedyVec; ++u) {
+      const int j = (lo >> 2) + threadIdx.x + u * kAcceptThreads;
+      x[u] = j < q1 ? __ldcs(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+  };
+  float4 cur[kGreedyVec], nxt[kGreedyVec];
+  if (kVec && (int)blockIdx.x < tasks) load(blockIdx.x, cur);
+  int k = 0;
+  for (int task = blockIdx.x; task < tasks; task += gridDim.x, ++k) {
+    int t, lo, hi;
+    bounds(task, t, lo, hi);
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (kVec) {
+      if (task + (int)gridDim.x < tasks) load(task + gridDim.x, nxt);
+#pragma unroll
+      for (int u = 0; u < kGreedyVec; ++u) {
+        const int e = lo + ((threadIdx.x + u * kAcceptThreads) << 2);
+        if (e < hi) {
+          arg_better(bv, bi, cur[u].x, e);
+          arg_better(bv, bi, cur[u].y, e + 1);
+          arg_better(bv, bi, cur[u].z, e + 2);
+          arg_better(bv, bi, cur[u].w, e + 3);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGreedyVec; ++u) cur[u] = nxt[u];
+    } else {
+      const float* row = logits + (size_t)t * vocab;
+      for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) arg_better(bv, bi, __ldcs(row + e), e);
+    }
+    warp_arg_reduce(bv, bi);
+    if (lane == 0) {  // two slots: task k+1 writes the other one, so one barrier per task
+      sv[k & 1][warp] = bv;
+      si[k & 1][warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kAcceptThreads / 32; ++w) arg_better(bv, bi, sv[k & 1][w], si[k & 1][w]);
+      partials[task] = ArgPartial{bv, bi};
+    }
+  }
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kAcceptThreads / 32; ++w) arg_better(bv, bi, sv[w], si[w]);
-    partials[(size_t)t * chunks + c] = ArgPartial{bv, bi};
-    pdl_trigger();  // this CTA has streamed its chunk: the next kernel may be scheduled
+    pdl_trigger();  // this CTA has streamed its tasks: the next kernel may be scheduled
     __threadfence();
-    const unsigned done = atomicAdd(node_cnt + t, 1u);
-    s_last = done == (unsigned)(chunks - 1);
+    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
-  // last CTA of row t: merge the chunk partials
-  if (warp == 0) {
-    float v = -INFINITY;
-    int i = INT_MAX;
-    for (int k = lane; k < chunks; k += 32) {
-      const ArgPartial* p = partials + (size_t)t * chunks + k;
-      arg_better(v, i, __ldcg(&p->v), __ldcg(&p->i));
-    }
-    warp_arg_reduce(v, i);
-    if (lane == 0) {
-      argmax[t] = i == INT_MAX ? 0 : i;
-      node_cnt[t] = 0;
-      __threadfence();
+
+  // ---- the last CTA: argmax of every row, then the walk of every sequence
+  __shared__ int s_par[kGreedyStage], s_tok[kGreedyStage], s_am[kGreedyStage], s_child[kGreedyStage];
+  const bool staged = total_nodes <= kGreedyStage;
+  if (threadIdx.x == 0) done[0] = 0u;  // every CTA has counted itself: ready for the next call
+  if (staged) {
+    for (int i = threadIdx.x; i < total_nodes; i += kAcceptThreads) {
+      s_par[i] = __ldg(parent + i);
+      s_tok[i] = __ldg(tokens + i);
     }
   }
-  __syncthreads();
-  const int b = seq_of_row(qo, batch, t);
-  const int base = __ldg(qo + b);
-  const int n = __ldg(qo + b + 1) - base;
-  if (threadIdx.x == 0) {
-    const unsigned done = atomicAdd(seq_cnt + b, 1u);
-    s_last = done == (unsigned)(n - 1);
-    if (s_last) seq_cnt[b] = 0;
-    __threadfence();
+  // warp w: rows w, w + 8, ...; eight rows' partials loaded before any is reduced
+  constexpr int kRowsPerPass = 8;
+  for (int t0 = warp; t0 < total_nodes; t0 += kRowsPerPass * (kAcceptThreads / 32)) {
+    float v[kRowsPerPass];
+    int ix[kRowsPerPass];
+#pragma unroll
+    for (int r = 0; r < kRowsPerPass; ++r) {
+      v[r] = -INFINITY;
+      ix[r] = INT_MAX;
+    }
+    for (int c0 = 0; c0 < gchunks; c0 += 32) {
+      const int c = c0 + lane;
+      float2 pv[kRowsPerPass];  // (value, index bits): all loads issued before any compare
+#pragma unroll
+      for (int r = 0; r < kRowsPerPass; ++r) {
+        const int t = t0 + r * (kAcceptThreads / 32);
+        pv[r] = (t < total_nodes && c < gchunks)
+                    ? __ldcg(reinterpret_cast<const float2*>(partials + (size_t)t * gchunks + c))
+                    : make_float2(-INFINITY, __int_as_float(INT_MAX));
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsPerPass; ++r) arg_better(v[r], ix[r], pv[r].x, __float_as_int(pv[r].y));
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerPass; ++r) {
+      const int t = t0 + r * (kAcceptThreads / 32);
+      warp_arg_reduce(v[r], ix[r]);
+      if (lane == 0 && t < total_nodes) {
+        const int a = ix[r] == INT_MAX ? 0 : ix[r];
+        if (staged) s_am[t] = a;
+        else argmax[t] = a;
+      }
+    }
   }
   __syncthreads();
-  if (!s_last) return;
-  // last row of sequence b: stage the tree (parents, tokens, argmaxes) in shared memory
-  // with one round trip, then walk it there
-  __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes], s_am[kMaxTreeNodes];
-  const int nw = n < kMaxTreeNodes ? n : kMaxTreeNodes;
-  for (int i = threadIdx.x; i < nw; i += kAcceptThreads) {
-    s_par[i] = __ldg(parent + base + i);
-    s_tok[i] = __ldg(tokens + base + i);
-    s_am[i] = __ldcg(argmax + base + i);
+  for (int b = warp; b < batch; b += kAcceptThreads / 32) {
+    const int base = __ldg(qo + b);
+    const int n = min(__ldg(qo + b + 1) - base, kMaxTreeNodes);
+    if (staged)
+      greedy_walk_warp_staged(b, n, s_par + base, s_tok + base, s_am + base, s_child + base, path_cap, accept_len,
+                              path, out_tokens, flags, status);
+    else
+      greedy_walk_warp(b, n, parent + base, tokens + base, argmax + base, path_cap, accept_len, path, out_tokens,
+                       flags, status);
   }
-  __syncthreads();
-  if (warp != 0) return;
-  greedy_walk_warp(b, nw, s_par, s_tok, s_am, path_cap, accept_len, path, out_tokens, flags, status);
 }
 
 // ---------------------------------------------------------------- stochastic: statistics
@@ -621,21 +718,33 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
   uint8_t* wb = static_cast<uint8_t*>(ws);
   unsigned* node_cnt = reinterpret_cast<unsigned*>(wb + w.node_cnt);
-  unsigned* seq_cnt = reinterpret_cast<unsigned*>(wb + w.seq_cnt);
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
                    (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
   const dim3 grid((unsigned)(total_nodes * chunks));
   if (mode == SPEC_GREEDY) {
+    // the greedy partials (8 bytes per 4096-logit task) fit where the stochastic ones
+    // (24 bytes per 8192-logit chunk) go
     ArgPartial* part = reinterpret_cast<ArgPartial*>(wb + w.partials);
     int* am = reinterpret_cast<int*>(wb + w.results);
-    if (vec)
-      accept_argmax_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(
-          tl, vocab, chunks, qo, batch, parent, tokens, path_cap, accept_len, path, out_tokens, flags,
-          node_cnt, seq_cnt, part, am, status);
-    else
-      accept_argmax_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(
-          tl, vocab, chunks, qo, batch, parent, tokens, path_cap, accept_len, path, out_tokens, flags,
-          node_cnt, seq_cnt, part, am, status);
+    const int gch = greedy_chunks(vocab);
+    const int tasks = total_nodes * gch;
+    static int per_sm[2] = {0, 0};
+    auto kern = vec ? accept_greedy_kernel<true> : accept_greedy_kernel<false>;
+    int& occ = per_sm[vec ? 1 : 0];
+    if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAcceptThreads, 0) != cudaSuccess ||
+                     occ < 1))
+      occ = 1;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return SPEC_ERR_CUDA;
+    // one wave, every CTA with the same number of tasks
+    const int per_cta = ceil_div(tasks, occ * sms);
+    const int grid_n = ceil_div(tasks, per_cta);
+    if (launch_pdl(kern, dim3((unsigned)grid_n), dim3(kAcceptThreads), 0, stream, tl, vocab, gch, tasks, qo, batch,
+                   total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, node_cnt, part, am,
+                   status) != cudaSuccess)
+      return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   StatPartial* part = reinterpret_cast<StatPartial*>(wb + w.partials);

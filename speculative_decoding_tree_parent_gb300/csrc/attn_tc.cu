@@ -108,6 +108,33 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Key split of a sequence, balanced to the 16-token page: the work units are the prefix
+// pages, then each tree block as 4 units; split s takes units [s U / S, (s+1) U / S).
+// Its prefix pages become blocks of up to 4 pages (the last one may hold fewer); a tree
+// block belongs to the split holding its first unit.
+struct TcSplit {
+  int pg_lo, pg_hi;  // prefix pages [lo, hi)
+  int npb;           // prefix blocks
+  int tb_lo;         // first tree block
+  int nb;            // blocks in all: prefix blocks, then tree blocks tb_lo, tb_lo + 1, ...
+};
+
+__device__ __forceinline__ TcSplit tc_split(int P, int N, int splits, int s) {
+  const int np = (P + 15) >> 4;
+  const int nt = (N + kTcKeys - 1) / kTcKeys;
+  const long units = np + 4L * nt;
+  const int lo = (int)((long)s * units / splits), hi = (int)((long)(s + 1) * units / splits);
+  TcSplit r;
+  r.pg_lo = min(lo, np);
+  r.pg_hi = min(hi, np);
+  r.npb = (r.pg_hi - r.pg_lo + 3) >> 2;
+  const int t_lo = lo <= np ? 0 : (lo - np + 3) >> 2;            // first i with np + 4i >= lo
+  const int t_hi = hi <= np ? 0 : min(nt, (hi - np + 3) >> 2);   // first i with np + 4i >= hi
+  r.tb_lo = t_lo;
+  r.nb = r.npb + max(0, t_hi - t_lo);
+  return r;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
@@ -143,9 +170,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0 && split == 0) report(p.status, SPEC_ERR_CAPACITY);
     return;
   }
-  const SplitRange sr = split_range(P, N, kTcKeys, p.splits, split);
-  const int nb = sr.blk_hi - sr.blk_lo;
-  const int npb = sr.n_prefix_blocks;
+  const TcSplit sr = tc_split(P, N, p.splits, split);
+  const int nb = sr.nb;
+  const int npb = sr.npb;
 
   // softmax-thread bookkeeping: warps 2-5 tile 0, warps 6-9 tile 1; TMEM lane quarter = warp % 4
   const int tile = warp >= 6 ? 1 : 0;
@@ -167,13 +194,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // Page ids of the producer's next 8 blocks, one per lane (lane l: block 8k + l/4,
     // page l%4), fetched a batch ahead so the page-table latency is paid once per 8 blocks.
-    // Pages past the prefix (and invalid ids, reported) become the out-of-range id
+    // Pages past the split (and invalid ids, reported) become the out-of-range id
     // num_pages, which TMA reads as zeros.
     auto fetch_pages = [&](int k) -> int {
-      const int blk = sr.blk_lo + 8 * k + (lane >> 2);
-      const int lp = blk * 4 + (lane & 3);
+      const int blk = 8 * k + (lane >> 2);
+      const int lp = sr.pg_lo + blk * 4 + (lane & 3);
       int page = p.num_pages;
-      if (blk < sr.blk_hi && blk < npb && lp * 16 < P) {
+      if (blk < npb && lp < sr.pg_hi) {
         const int pg = __ldg(p.page_table + (size_t)b * p.max_pages + lp);
         if (pg >= 0 && pg < p.num_pages) page = pg;
         else report(p.status, SPEC_ERR_PAGE);
@@ -187,7 +214,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto load_block = [&](int j) {
       const int st = j % kTcStages;
       const uint32_t dst0 = s_base + kOffKV + st * kStageBytes;
-      const int blk = sr.blk_lo + j;
       if ((j & 7) == 0 && j > 0) {
         pg_cur = pg_nxt;
         pg_nxt = fetch_pages((j >> 3) + 1);
@@ -195,7 +221,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int page_here = __shfl_sync(0xffffffffu, pg_cur, ((j & 7) << 2) + ((lane >> 2) & 3));
       if (lane == 0) tc::mbar_arrive_expect_tx(bar_kvf(st), kStageBytes);
       __syncwarp();
-      if (blk < npb) {
+      if (j < npb) {
         if (lane < 16) {
           const int pp = lane >> 2, which = lane & 3;
           const int slab = which & 1, isv = which >> 1;
@@ -203,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::tma_load_4d(dst, isv ? &tm_vp : &tm_kp, bar_kvf(st), slab * 64, 0, g, page_here);
         }
       } else if (lane < 4) {
-        const int tb = blk - npb;
+        const int tb = sr.tb_lo + (j - npb);
         const int slab = lane & 1, isv = lane >> 1;
         const uint32_t dst = dst0 + isv * 2 * kKVSlab + slab * kKVSlab;
         tc::tma_load_3d(dst, isv ? &tm_vt : &tm_kt, bar_kvf(st), slab * 64, g, base + tb * 64);
@@ -343,9 +369,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::tmem_ld32(t_lane + (j & 1) * 64, sv);
         tc::tmem_ld32(t_lane + (j & 1) * 64 + 32, sv + 32);
         tc::tmem_wait_ld();
-        const int blk = sr.blk_lo + j;
-        if (blk < npb) {
-          const int nvalid = P - blk * kTcKeys;  // prefix: a length bound, never a mask
+        if (j < npb) {  // prefix: a length bound (the split's last page, P), never a mask
+          const int nvalid = min(P, sr.pg_hi * 16) - (sr.pg_lo + 4 * j) * 16;
           if (nvalid < kTcKeys) {
 #pragma unroll
             for (int c = 0; c < kTcKeys; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
@@ -355,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             pdl_wait();
             mask_ready = true;
           }
-          const uint64_t bits = row_valid ? mrow[blk - npb] : 0ull;
+          const uint64_t bits = row_valid ? mrow[sr.tb_lo + (j - npb)] : 0ull;
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c] = ((bits >> c) & 1ull) ? sv[c] : -INFINITY;
         }
