@@ -147,6 +147,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int split = blockIdx.x, pair = blockIdx.y, bg = blockIdx.z;
   // the split merge (launched next) may be scheduled now: it waits for this grid to end
   pdl_trigger();
+  if (threadIdx.x < 32) {  // the sequence's page-table row into L2 while qo / prefix_len load
+    const int b0 = blockIdx.z / p.hkv;
+    for (int i = (threadIdx.x & 31) * 32; i < p.max_pages; i += 32 * 32)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.page_table + (size_t)b0 * p.max_pages + i));
+  }
   if (threadIdx.x == 0) {  // descriptor fetches overlap the first loads of qo / prefix_len
     tc::prefetch_tmap(&tm_q);
     tc::prefetch_tmap(&tm_kp);
@@ -358,7 +363,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float sl2 = p.scale_log2;
       float m_run = -INFINITY, l = 0.f;
       bool ok = true;
-      bool mask_ready = false;
+      // the first tree block's mask word, fetched while the prefix blocks stream (the mask
+      // may come from the kernel launched just before this one: wait for it first)
+      uint64_t bits_next = 0ull;
+      if (nb > npb) {
+        pdl_wait();
+        if (row_valid) bits_next = __ldcg(mrow + sr.tb_lo);
+      }
       for (int j = 0; j < nb; ++j) {
         if (!warp_wait(bar_sf(tile, j & 1), (j >> 1) & 1, abort)) {
           ok = false;
@@ -376,11 +387,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < kTcKeys; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
           }
         } else {  // tree block: ancestor bits
-          if (!mask_ready) {  // the mask may come from the kernel launched just before this one
-            pdl_wait();
-            mask_ready = true;
-          }
-          const uint64_t bits = row_valid ? mrow[sr.tb_lo + (j - npb)] : 0ull;
+          const uint64_t bits = bits_next;
+          if (row_valid && j + 1 < nb) bits_next = __ldcg(mrow + sr.tb_lo + (j + 1 - npb));
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c] = ((bits >> c) & 1ull) ? sv[c] : -INFINITY;
         }
@@ -449,20 +457,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // O row out of TMEM: final output when unsplit, else this split's partial (O / l in
       // bf16, 8 values per 16-byte chunk, chunk-major) and its log2-sum-exp m + log2(l)
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      // nothing is written before the previous kernel in the stream has finished (it may
+      // still be reading the buffers this one is about to write)
+      pdl_wait();
       uint4* po = p.part_o + ((size_t)grp * p.splits + split) * (kTcRows * kTcD / 8);
 #pragma unroll 1
-      for (int ch = 0; ch < kTcD / 32; ++ch) {
-        float o[32];
+      for (int ch = 0; ch < kTcD / 32; ch += 2) {  // two 32-column loads per wait
+        float o[64];
         __syncwarp();
         tc::tmem_ld32(t_lane + 128 + ch * 32, o);
+        tc::tmem_ld32(t_lane + 128 + ch * 32 + 32, o + 32);
         tc::tmem_wait_ld();
         if (!ok) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          for (int i = 0; i < 64; ++i) o[i] = 0.f;
         }
-        uint4 c8[4];
+        uint4 c8[8];
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
+        for (int v = 0; v < 8; ++v)
           c8[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
                              pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
                              pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
@@ -471,11 +483,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kTcD + ch * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = c8[v];
+            for (int v = 0; v < 8; ++v) dst[v] = c8[v];
           }
         } else {  // chunk-major: a warp's 32 rows write 512 contiguous bytes per chunk
 #pragma unroll
-          for (int v = 0; v < 4; ++v) po[(ch * 4 + v) * kTcRows + row] = c8[v];
+          for (int v = 0; v < 8; ++v) po[(ch * 4 + v) * kTcRows + row] = c8[v];
         }
       }
       const float lse2 = (ok && l > 0.f) ? m_run + log2f(l) : -INFINITY;
@@ -494,6 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::tmem_dealloc(tbase, kTmemCols);
     }
   } else if (warp >= 2 && warp < 2 + 4 * kTiles && tile < ntiles) {  // empty key split: contributes nothing to the merge
+    pdl_wait();
     p.part_lse[((size_t)grp * p.splits + split) * kTcRows + row] = -INFINITY;
   }
 }
@@ -514,13 +527,14 @@ struct TcMergeParams {
   float* lse;
 };
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 64;  // small CTAs: one fits beside an attention CTA on an SM
 constexpr int kMaxSplits = 32;  // attn_splits_tc never returns more
 
 // MAXS >= splits: the unrolled load batch, sized to the launch so the registers stay few
 // enough for a merge CTA to sit beside an attention CTA on one SM.
 template <int MAXS>
 __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge_kernel(const TcMergeParams p) {
+  pdl_trigger();  // the next kernel may be scheduled: whatever it reads, it waits for this grid
   const long idx = (long)blockIdx.x * kMergeThreads + threadIdx.x;
   if (idx >= p.groups * 16 * kTcRows) return;
   const int gt = (int)(idx / (16 * kTcRows));
