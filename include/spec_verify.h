@@ -10,6 +10,9 @@
  *   spec_accept            longest accepted path + bonus token (greedy / stochastic)
  *   spec_kv_commit         the accepted path's K/V written into the paged cache
  *
+ * spec_accept_commit runs the last two as one call (the same results, one kernel
+ * boundary fewer).
+ *
  * Sources of the operations (page title, then section):
  *   "EAGLE-2 deep dive" (techknowgenie): architecture section (all tree tokens
  *     verified in one target forward with a 2-D tree mask injected into
@@ -225,6 +228,26 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
                    const int32_t* page_table, int max_pages, int num_pages, int page_size,
                    const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool, void* v_pool,
                    int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream);
+
+/*
+ * spec_accept_commit — spec_accept, then spec_kv_commit of the paths it accepted, in one
+ *   call: the results (accept_len, path, out_tokens, flags, the written pool rows,
+ *   seq_len_out, device errors) are those of the two calls made back to back on
+ *   `stream`. Greedy runs the commit inside the acceptance kernel (its last CTA, right
+ *   after the walk); stochastic launches the commit kernel after its two kernels.
+ *   Arguments: those of spec_accept (mode ... flags, ws, ws_bytes) and of spec_kv_commit
+ *   (dtype ... d); path_cap, path and accept_len serve both. The same host errors, the
+ *   same layouts; ws as for spec_accept.
+ */
+int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tokens,
+                       const float* target_logits, const float* draft_logits, const float* uniforms,
+                       float temperature, int vocab, const int32_t* qo_indptr, int batch,
+                       int total_nodes, int max_nodes, int path_cap, int32_t* accept_len,
+                       int32_t* path, int32_t* out_tokens, uint8_t* flags, int dtype,
+                       const void* k_tree, const void* v_tree, const int32_t* page_table,
+                       int max_pages, int num_pages, int page_size, const int32_t* prefix_len,
+                       int32_t* seq_len_out, void* k_pool, void* v_pool, int hkv, int d, void* ws,
+                       size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
  * spec_accept_noalloc — spec_accept for callers that cannot allocate device memory.

@@ -25,7 +25,7 @@ STATUS = {
     -9: "SPEC_ERR_INDEX",
 }
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
-           "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_noalloc")
+           "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -38,6 +38,8 @@ _SIGS = {
                                    _I, _F, _P, _P, _P, _Z, _P, _P]),
     "spec_accept": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
     "spec_kv_commit": (_I, [_I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "spec_accept_commit": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P,
+                                _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _Z, _P, _P]),
     "spec_accept_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -164,6 +166,22 @@ def spec_kv_commit(k_tree, v_tree, path, accept_len, qo_indptr, page_table, pref
         _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
         _ptr(v_pool), qo_indptr.numel() - 1, T, hkv, d, _ptr(dev_status), _stream(stream))
     return _check(st, "spec_kv_commit")
+
+
+def spec_accept_commit(mode, parent, draft_tokens, target_logits, qo_indptr, max_nodes, accept_len, path,
+                       out_tokens, ws, k_tree, v_tree, page_table, prefix_len, k_pool, v_pool, seq_len_out=None,
+                       draft_logits=None, uniforms=None, temperature=1.0, flags=None, dev_status=None, stream=None):
+    """spec_accept then spec_kv_commit of the accepted paths, as one call."""
+    T, V = target_logits.shape
+    _, hkv, d = k_tree.shape
+    num_pages, _, ps, _ = k_pool.shape
+    st = load().spec_accept_commit(
+        int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+        float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
+        _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _dtype(k_tree), _ptr(k_tree), _ptr(v_tree),
+        _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
+        _ptr(v_pool), hkv, d, _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_accept_commit")
 
 
 def spec_accept_noalloc(mode, parent, draft_tokens, target_logits, qo_indptr, max_nodes, accept_len, path,

@@ -178,6 +178,8 @@ __device__ void greedy_walk_warp(int b, int n, const int* parent, const int* tok
 constexpr int kGreedyVec = 4;                                  // float4 per thread per task
 constexpr int kGreedyChunk = kAcceptThreads * kGreedyVec * 4;  // 4096 logits
 constexpr int kGreedyStage = 2048;                             // nodes the final CTA stages
+constexpr int kCommitCta = 4;          // fused commit: up to this many sequences, one at a time by the CTA
+constexpr int kCommitPathStage = 128;  // path rows up to this long kept in shared memory for it
 
 int greedy_chunks(int vocab) { return ceil_div(vocab, kGreedyChunk); }
 
@@ -185,9 +187,11 @@ int greedy_chunks(int vocab) { return ceil_div(vocab, kGreedyChunk); }
 // draft token equals its parent's argmax offers itself to the parent (atomicMin keeps the
 // lowest id), then the warp follows the offers from the root. `child` is scratch of n
 // entries.
-__device__ void greedy_walk_warp_staged(int b, int n, const int* parent, const int* tokens, const int* argmax,
-                                        int* child, int path_cap, int32_t* accept_len, int32_t* path,
-                                        int32_t* out_tokens, uint8_t* flags, int32_t* status) {
+// `spath` (nullable) receives a shared-memory copy of the path row's first L + 1
+// entries (room for path_cap). Returns L on every lane.
+__device__ int greedy_walk_warp_staged(int b, int n, const int* parent, const int* tokens, const int* argmax,
+                                       int* child, int path_cap, int32_t* accept_len, int32_t* path,
+                                       int32_t* out_tokens, uint8_t* flags, int32_t* status, int* spath) {
   const int lane = threadIdx.x & 31;
   for (int c = lane; c < n; c += 32) child[c] = INT_MAX;
   __syncwarp();
@@ -201,6 +205,7 @@ __device__ void greedy_walk_warp_staged(int b, int n, const int* parent, const i
   if (lane == 0) {
     int v = 0, L = 0;
     prow[0] = 0;
+    if (spath != nullptr) spath[0] = 0;
     while (child[v] != INT_MAX) {
       if (L + 1 >= path_cap) {  // accepted path does not fit: truncate here
         report(status, SPEC_ERR_CAPACITY);
@@ -209,6 +214,7 @@ __device__ void greedy_walk_warp_staged(int b, int n, const int* parent, const i
       const int c = child[v];
       ++L;
       prow[L] = c;
+      if (spath != nullptr) spath[L] = c;
       trow[L - 1] = tokens[c];
       v = c;
     }
@@ -223,23 +229,121 @@ __device__ void greedy_walk_warp_staged(int b, int n, const int* parent, const i
     prow[k] = -1;
     trow[k] = -1;
   }
+  return L;
 }
 
+// Commit of sequence b (the rules of kv_commit_kernel) by a team: the whole CTA
+// (kCta) or one warp. L and the path come from this CTA's walk: `spath` in shared
+// memory (nullable: then the global row `gpath`, written before a barrier). Every slot
+// is validated and the first rows' K/V are loaded before the team's vote, so a valid
+// commit costs one memory round trip; a sequence with an error is reported and left
+// unwritten.
+template <bool kCta>
+__device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, int L, const int* spath,
+                                const int32_t* gpath, int path_cap, int32_t* status) {
+  const int rank = kCta ? (int)threadIdx.x : (int)(threadIdx.x & 31);
+  const int size = kCta ? (int)blockDim.x : 32;
+  const int P = __ldg(ca.prefix_len + b);
+  const int32_t* prow_pt = ca.page_table + (size_t)b * ca.max_pages;
+  auto node_at = [&](int i) { return spath != nullptr ? spath[i] : gpath[i]; };
+  int code = 0;
+  if (L < 0 || L >= path_cap || L >= n || P < 0) {
+    code = SPEC_ERR_INDEX;
+  } else {
+    for (int i = rank; i <= L; i += size) {
+      const int node = node_at(i);
+      const int lp = (P + i) / ca.page_size;
+      const int page = lp < ca.max_pages ? __ldg(prow_pt + lp) : -1;
+      int c = 0;
+      if (node < 0 || node >= n || (i == 0 && node != 0)) c = SPEC_ERR_INDEX;
+      else if (lp >= ca.max_pages) c = SPEC_ERR_CAPACITY;
+      else if (page < 0 || page >= ca.num_pages) c = SPEC_ERR_PAGE;
+      if (code == 0) code = c;
+    }
+  }
+  const int row_bytes = ca.d * ca.elem_bytes;
+  const int vecs = row_bytes >> 4;
+  const int total = code == 0 ? (L + 1) * ca.hkv * vecs : 0;
+  // the first rows' loads go out with the checks (a row only if its node is in range)
+  constexpr int kPer = 2;
+  uint4 kb[kPer], vb[kPer];
+  size_t dsts[kPer];
+  auto locate = [&](int e, size_t& src, size_t& dst) {
+    const int r = e / vecs, vi = e - (e / vecs) * vecs;
+    const int i = r / ca.hkv, g = r - (r / ca.hkv) * ca.hkv;
+    const int slot = P + i;
+    const int node = node_at(i);
+    const int lp = slot / ca.page_size;
+    const int page = lp < ca.max_pages ? __ldg(prow_pt + lp) : -1;  // another slot's check may have failed
+    src = ((size_t)(base + node) * ca.hkv + g) * row_bytes + ((size_t)vi << 4);
+    dst = (((size_t)page * ca.hkv + g) * ca.page_size + (slot % ca.page_size)) * row_bytes + ((size_t)vi << 4);
+    return node >= 0 && node < n && page >= 0 && page < ca.num_pages;
+  };
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = rank + u * size;
+    size_t src = 0;
+    dsts[u] = 0;
+    if (e < total && locate(e, src, dsts[u])) {
+      kb[u] = __ldg(reinterpret_cast<const uint4*>(ca.k_tree + src));
+      vb[u] = __ldg(reinterpret_cast<const uint4*>(ca.v_tree + src));
+    }
+  }
+  const bool bad = kCta ? __syncthreads_or(code != 0) : __any_sync(0xffffffffu, code != 0);
+  if (bad) {
+    if (code != 0) report(status, code);
+    return;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    if (rank + u * size < total) {
+      *reinterpret_cast<uint4*>(ca.k_pool + dsts[u]) = kb[u];
+      *reinterpret_cast<uint4*>(ca.v_pool + dsts[u]) = vb[u];
+    }
+  }
+  for (int e = rank + kPer * size; e < total; e += size) {
+    size_t src, dst;
+    locate(e, src, dst);
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(ca.k_tree + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(ca.v_tree + src));
+    *reinterpret_cast<uint4*>(ca.k_pool + dst) = kv;
+    *reinterpret_cast<uint4*>(ca.v_pool + dst) = vv;
+  }
+  if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
+}
+
+// (five CTAs per SM: the streaming loop needs the occupancy, the final CTA's epilogue may spill)
 template <bool kVec>
-__global__ void __launch_bounds__(kAcceptThreads) accept_greedy_kernel(
+__global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     const float* __restrict__ logits, int vocab, int gchunks, int tasks, const int32_t* __restrict__ qo,
     int batch, int total_nodes, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
     int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, unsigned* done,
-    ArgPartial* partials, int* argmax, int32_t* status) {
+    ArgPartial* partials, int* argmax, int32_t* status, const CommitArgs ca) {
   __shared__ float sv[2][kAcceptThreads / 32];
   __shared__ int si[2][kAcceptThreads / 32];
   __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();  // stream order: nothing is read before the previous kernel has finished
-  if (blockIdx.x == gridDim.x - 1) {  // the tree arrays the last CTA stages: into L2 early
+  if (blockIdx.x == gridDim.x - 1) {  // what the last CTA reads at the end: into L2 early
     for (int i = threadIdx.x * 32; i < total_nodes; i += kAcceptThreads * 32) {
       asm volatile("prefetch.global.L2 [%0];" ::"l"(parent + i));
       asm volatile("prefetch.global.L2 [%0];" ::"l"(tokens + i));
+    }
+    if (ca.k_tree != nullptr) {  // each sequence's page-table entries from its prefix end on
+      for (int bb = threadIdx.x; bb < batch; bb += kAcceptThreads) {
+        const int P = __ldg(ca.prefix_len + bb);
+        const int lp = P >= 0 ? P / ca.page_size : 0;
+        if (lp < ca.max_pages)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(ca.page_table + (size_t)bb * ca.max_pages + lp));
+      }
+    }
+    if (ca.k_tree != nullptr) {  // the tree K/V rows the commit copies (a few MB at most)
+      const size_t bytes = (size_t)total_nodes * ca.hkv * ca.d * ca.elem_bytes;
+      if (bytes <= (size_t(4) << 20))
+        for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)kAcceptThreads * 128) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(ca.k_tree + off));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(ca.v_tree + off));
+        }
     }
   }
 
@@ -297,7 +401,9 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_greedy_kernel(
     }
   }
   if (threadIdx.x == 0) {
-    pdl_trigger();  // this CTA has streamed its tasks: the next kernel may be scheduled
+    // this CTA has streamed its tasks: the next kernel may be scheduled -- unless this
+    // launch also commits K/V, which a next kernel may read before it waits
+    if (ca.k_tree == nullptr) pdl_trigger();
     __threadfence();
     s_last = atomicAdd(done, 1u) == gridDim.x - 1;
   }
@@ -306,6 +412,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_greedy_kernel(
 
   // ---- the last CTA: argmax of every row, then the walk of every sequence
   __shared__ int s_par[kGreedyStage], s_tok[kGreedyStage], s_am[kGreedyStage], s_child[kGreedyStage];
+  __shared__ int s_len[kCommitCta];                     // L of sequences 0 .. 3 (fused commit)
+  __shared__ int s_cpath[kCommitCta][kCommitPathStage];  // their paths, when path_cap fits
   const bool staged = total_nodes <= kGreedyStage;
   if (threadIdx.x == 0) done[0] = 0u;  // every CTA has counted itself: ready for the next call
   if (staged) {
@@ -352,12 +460,33 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_greedy_kernel(
   for (int b = warp; b < batch; b += kAcceptThreads / 32) {
     const int base = __ldg(qo + b);
     const int n = min(__ldg(qo + b + 1) - base, kMaxTreeNodes);
-    if (staged)
-      greedy_walk_warp_staged(b, n, s_par + base, s_tok + base, s_am + base, s_child + base, path_cap, accept_len,
-                              path, out_tokens, flags, status);
+    if (staged) {
+      int* sp = (ca.k_tree != nullptr && b < kCommitCta && path_cap <= kCommitPathStage) ? s_cpath[b] : nullptr;
+      const int L = greedy_walk_warp_staged(b, n, s_par + base, s_tok + base, s_am + base, s_child + base, path_cap,
+                                            accept_len, path, out_tokens, flags, status, sp);
+      if (b < kCommitCta && lane == 0) s_len[b] = L;
+    }
     else
       greedy_walk_warp(b, n, parent + base, tokens + base, argmax + base, path_cap, accept_len, path, out_tokens,
                        flags, status);
+  }
+  if (ca.k_tree == nullptr) return;
+  // ---- fused commit of every sequence's accepted path
+  __syncthreads();  // accept_len and the path rows written above are visible to the CTA
+  if (batch <= kCommitCta) {  // few sequences: the whole CTA on each in turn
+    const bool in_smem = staged && path_cap <= kCommitPathStage;
+    for (int b = 0; b < batch; ++b) {
+      const int base = __ldg(qo + b);
+      commit_sequence<true>(ca, b, base, __ldg(qo + b + 1) - base, staged ? s_len[b] : accept_len[b],
+                            in_smem ? s_cpath[b] : nullptr, path + (size_t)b * path_cap, path_cap, status);
+      __syncthreads();
+    }
+  } else {
+    for (int b = warp; b < batch; b += kAcceptThreads / 32) {
+      const int base = __ldg(qo + b);
+      commit_sequence<false>(ca, b, base, __ldg(qo + b + 1) - base, accept_len[b], nullptr,
+                             path + (size_t)b * path_cap, path_cap, status);
+    }
   }
 }
 
@@ -709,11 +838,20 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   }
 }
 
+int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
+                     const int32_t* accept_len, const int32_t* qo, const int32_t* page_table, int max_pages,
+                     int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
+                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream);
+
+// `commit` (nullable): also commit the accepted paths' K/V, as spec_kv_commit would right
+// after; greedy does it inside the acceptance kernel, stochastic with the commit kernel.
 int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl,
                   const float* dl, const float* uniforms, float temperature, int vocab,
                   const int32_t* qo, int batch, int total_nodes, int path_cap, int32_t* accept_len,
                   int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws, int32_t* status,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const CommitArgs* commit) {
+  CommitArgs ca = {};
+  if (commit != nullptr) ca = *commit;
   const int chunks = accept_chunks(total_nodes, vocab);
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
   uint8_t* wb = static_cast<uint8_t*>(ws);
@@ -743,7 +881,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     const int grid_n = ceil_div(tasks, per_cta);
     if (launch_pdl(kern, dim3((unsigned)grid_n), dim3(kAcceptThreads), 0, stream, tl, vocab, gch, tasks, qo, batch,
                    total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, node_cnt, part, am,
-                   status) != cudaSuccess)
+                   status, ca) != cudaSuccess)
       return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
@@ -759,7 +897,11 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
                  dl, uniforms, temperature, vocab, qo, path_cap, (const NodeStats*)st, accept_len, path, out_tokens,
                  flags, status) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (ca.k_tree == nullptr) return SPEC_OK;
+  return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
+                          ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
+                          ca.v_pool, batch, ca.hkv, ca.d, status, stream);
 }
 
 }  // namespace specv
@@ -822,5 +964,5 @@ extern "C" int spec_accept_noalloc(int mode, const int32_t* parent, const int32_
   if (cudaMemsetAsync(ws, 0, w.partials, st) != cudaSuccess) return SPEC_ERR_CUDA;
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, st);
+                       dev_status, st, nullptr);
 }

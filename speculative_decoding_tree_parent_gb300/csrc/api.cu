@@ -12,7 +12,7 @@ int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, con
 int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl, const float* dl,
                   const float* uniforms, float temperature, int vocab, const int32_t* qo, int batch,
                   int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
-                  uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream);
+                  uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream, const CommitArgs* commit);
 size_t accept_ws_bytes(int batch, int total_nodes, int vocab);
 int launch_attn_simt(int dtype, const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
                      const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
@@ -134,11 +134,12 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
                           sm_scale, out, lse, ws, dev_status, st);
 }
 
-int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
-                const float* draft_logits, const float* uniforms, float temperature, int vocab,
-                const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
-                int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws,
-                size_t ws_bytes, int32_t* dev_status, void* stream) {
+// Host checks of spec_accept's arguments (SPEC_OK when they pass).
+static int check_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                        const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                        const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                        const int32_t* accept_len, const int32_t* path, const int32_t* out_tokens, const void* ws,
+                        size_t ws_bytes) {
   if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
   if (batch < 0 || total_nodes < 0 || vocab <= 0 || path_cap < 1 || max_nodes < 1 || max_nodes > kMaxNodes)
     return SPEC_ERR_ARG;
@@ -149,15 +150,14 @@ int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, co
   if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
   const size_t need = spec_workspace_size(SPEC_OP_ACCEPT, batch, total_nodes, max_nodes, 0, 0, 0, 0, vocab);
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return SPEC_ERR_WORKSPACE;
-  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
-                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, static_cast<cudaStream_t>(stream));
+  return SPEC_OK;
 }
 
-int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
-                   const int32_t* accept_len, const int32_t* qo_indptr, const int32_t* page_table, int max_pages,
-                   int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
-                   void* v_pool, int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream) {
+// Host checks of spec_kv_commit's arguments (SPEC_OK when they pass).
+static int check_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
+                        const int32_t* accept_len, const int32_t* qo_indptr, const int32_t* page_table,
+                        int max_pages, int num_pages, int page_size, const int32_t* prefix_len, const void* k_pool,
+                        const void* v_pool, int batch, int total_nodes, int hkv, int d) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (batch < 0 || total_nodes < 0 || path_cap < 1 || max_pages < 0 || num_pages < 0 || page_size <= 0 ||
       hkv <= 0 || d <= 0)
@@ -168,6 +168,64 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
   if (!k_tree || !v_tree || !path || !accept_len || !qo_indptr || !page_table || !prefix_len || !k_pool || !v_pool)
     return SPEC_ERR_ARG;
   if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_pool) || !aligned16(v_pool)) return SPEC_ERR_ARG;
+  return SPEC_OK;
+}
+
+int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws,
+                size_t ws_bytes, int32_t* dev_status, void* stream) {
+  const int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                              qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws,
+                              ws_bytes);
+  if (rc != SPEC_OK || batch == 0) return rc;
+  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
+                       dev_status, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                       const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                       const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                       int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, int dtype,
+                       const void* k_tree, const void* v_tree, const int32_t* page_table, int max_pages,
+                       int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
+                       void* v_pool, int hkv, int d, void* ws, size_t ws_bytes, int32_t* dev_status,
+                       void* stream) {
+  int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                        qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws, ws_bytes);
+  if (rc != SPEC_OK) return rc;
+  rc = check_commit(dtype, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages, num_pages,
+                    page_size, prefix_len, k_pool, v_pool, batch, total_nodes, hkv, d);
+  if (rc != SPEC_OK || batch == 0) return rc;
+  CommitArgs ca;
+  ca.k_tree = static_cast<const uint8_t*>(k_tree);
+  ca.v_tree = static_cast<const uint8_t*>(v_tree);
+  ca.page_table = page_table;
+  ca.max_pages = max_pages;
+  ca.num_pages = num_pages;
+  ca.page_size = page_size;
+  ca.prefix_len = prefix_len;
+  ca.seq_len_out = seq_len_out;
+  ca.k_pool = static_cast<uint8_t*>(k_pool);
+  ca.v_pool = static_cast<uint8_t*>(v_pool);
+  ca.hkv = hkv;
+  ca.d = d;
+  ca.elem_bytes = dtype == SPEC_F32 ? 4 : 2;
+  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
+                       dev_status, static_cast<cudaStream_t>(stream), &ca);
+}
+
+int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
+                   const int32_t* accept_len, const int32_t* qo_indptr, const int32_t* page_table, int max_pages,
+                   int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
+                   void* v_pool, int batch, int total_nodes, int hkv, int d, int32_t* dev_status, void* stream) {
+  const int rc = check_commit(dtype, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
+                              num_pages, page_size, prefix_len, k_pool, v_pool, batch, total_nodes, hkv, d);
+  if (rc != SPEC_OK || batch == 0) return rc;
+  const int elem = dtype == SPEC_F32 ? 4 : 2;
   return launch_kv_commit(elem, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
                           num_pages, page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
                           static_cast<cudaStream_t>(stream));

@@ -40,6 +40,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Arguments of the KV commit when it runs fused after the acceptance (spec_accept_commit).
+struct CommitArgs {
+  const uint8_t* k_tree;  // nullptr: no commit
+  const uint8_t* v_tree;
+  const int32_t* page_table;
+  int max_pages, num_pages, page_size;
+  const int32_t* prefix_len;
+  int32_t* seq_len_out;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  int hkv, d, elem_bytes;
+};
+
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 

@@ -87,21 +87,39 @@ class DeviceBatch:
         return B.spec_kv_commit(self.k_tree, self.v_tree, self.path, self.accept_len, self.qo, self.page_table,
                                 self.prefix_len, self.k_pool, self.v_pool, self.seq_len, self.status, stream)
 
-    def step(self, mode=None, stream=None):
-        """One full verification step (4 calls); returns the number of kernel launches issued."""
+    def accept_commit(self, mode=None, stream=None):
+        """spec_accept then spec_kv_commit, as the one fused call."""
+        mode = mode or self.mode
+        m = B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY
+        return B.spec_accept_commit(m, self.parent, self.tokens, self.target_logits, self.qo, self.max_nodes,
+                                    self.accept_len, self.path, self.out_tokens, self.acc_ws, self.k_tree,
+                                    self.v_tree, self.page_table, self.prefix_len, self.k_pool, self.v_pool,
+                                    seq_len_out=self.seq_len, draft_logits=self.draft_logits if m else None,
+                                    uniforms=self.uniforms if m else None, temperature=self.inp.temperature,
+                                    flags=self.flags, dev_status=self.status, stream=stream)
+
+    def step(self, mode=None, stream=None, fused=True):
+        """One full verification step: mask, attention, then acceptance + KV commit (one fused
+        call, or the two separate ones). Returns the number of kernel launches issued."""
         self.build_mask(stream)
         self.attention(stream)
-        self.accept(mode, stream)
-        self.commit(stream)
-        return self.launches_per_step(mode)
+        if fused:
+            self.accept_commit(mode, stream)
+        else:
+            self.accept(mode, stream)
+            self.commit(stream)
+        return self.launches_per_step(mode, fused)
 
-    def launches_per_step(self, mode=None):
+    def launches_per_step(self, mode=None, fused=True):
         """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the keys are
-        split), accept 1 (greedy) or 2 (stochastic), commit 1."""
+        split), then accept 1 (greedy) or 2 (stochastic) and commit 1 -- except that the fused
+        greedy call commits inside its acceptance kernel."""
         mode = mode or self.mode
         splits, _ = self.attn_plan()
         attn = 2 if splits > 1 else 1
-        return 1 + attn + (2 if mode == "stochastic" else 1) + 1
+        acc = 2 if mode == "stochastic" else 1
+        commit = 0 if (fused and mode != "stochastic") else 1
+        return 1 + attn + acc + commit
 
     def attn_plan(self):
         inp = self.inp

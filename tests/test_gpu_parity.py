@@ -400,3 +400,60 @@ def test_commit_rejects_bad_path():
     torch.cuda.synchronize()
     assert _status(db) == -9
     assert torch.equal(before, db.k_pool)
+
+
+# ----------------------------------------------------------------------------- fused accept + commit
+
+@pytest.mark.parametrize("cfg,mode", [(1, "greedy"), (2, "greedy"), (3, "greedy"), (5, "greedy"),
+                                      (4, "stochastic"), (5, "stochastic")])
+def test_accept_commit_fused(inputs, cfg, mode):
+    """spec_accept_commit = spec_accept then spec_kv_commit: accepted paths against the
+    oracle, committed bytes against the oracle's commit of those paths, and everything
+    bit-identical to the two separate calls."""
+    inp = inputs(cfg)
+    fused = DeviceBatch(inp, mode=mode)
+    fused.accept_commit(mode)
+    sep = DeviceBatch(inp, mode=mode)
+    sep.accept(mode)
+    sep.commit()
+    torch.cuda.synchronize()
+    assert _status(fused) == 0 and _status(sep) == 0
+    ref = _oracle_accept(inp, mode)
+    assert _accept_compare(fused, ref) <= max(1, inp.batch // 20)
+    for name in ("accept_len", "path", "out_tokens", "seq_len", "k_pool", "v_pool"):
+        assert torch.equal(getattr(fused, name), getattr(sep, name)), name
+    acc = fused.accept_len.cpu().numpy()
+    path = fused.path.cpu().numpy()
+    k2, v2, seq_len = oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree,
+                                       inp.v_tree, path, acc, inp.qo_indptr, inp.page_size)
+    assert np.array_equal(fused.k_pool.float().cpu().numpy(), k2)
+    assert np.array_equal(fused.v_pool.float().cpu().numpy(), v2)
+    assert np.array_equal(fused.seq_len.cpu().numpy(), seq_len)
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_accept_commit_fused_bad_page(inputs, cfg):
+    """A page id outside the pool at a commit slot: SPEC_ERR_PAGE, that sequence left
+    unwritten, the acceptance results still those of the oracle."""
+    inp = inputs(cfg)
+    db = DeviceBatch(inp)
+    # sequence 0: every page-table entry from its prefix end on points outside the pool
+    P0 = int(inp.prefix_len[0])
+    db.page_table[0, P0 // inp.page_size:] = inp.num_pages + 7
+    before_k, before_v = db.k_pool.clone(), db.v_pool.clone()
+    db.accept_commit("greedy")
+    torch.cuda.synchronize()
+    assert _status(db) == -3   # SPEC_ERR_PAGE
+    ref = _oracle_accept(inp, "greedy")
+    assert _accept_compare(db, ref) == 0
+    # pages of sequence 0 untouched; other sequences committed as the oracle does
+    pt = inp.page_table.copy()
+    pt[0, P0 // inp.page_size:] = inp.num_pages + 7
+    acc = db.accept_len.cpu().numpy()
+    path = db.path.cpu().numpy()
+    ok = np.arange(inp.batch) != 0
+    k2, v2, _ = oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree, inp.v_tree,
+                                 np.where(ok[:, None], path, -1), np.where(ok, acc, -1), inp.qo_indptr,
+                                 inp.page_size)
+    assert np.array_equal(db.k_pool.float().cpu().numpy(), k2)
+    assert np.array_equal(db.v_pool.float().cpu().numpy(), v2)
