@@ -63,6 +63,30 @@ class DeviceBatch:
         self.attn_ws = torch.zeros(max(attn_ws, 256), dtype=torch.uint8, device=dev)
         self.acc_ws = torch.zeros(max(acc_ws, 256), dtype=torch.uint8, device=dev)
 
+    # --- one-copy transfers -------------------------------------------------------------
+    STEP_INPUTS = ("q", "k_tree", "v_tree", "parent", "qo", "tokens", "page_table", "prefix_len")
+    STEP_RESULTS = ("accept_len", "path", "out_tokens", "seq_len")
+
+    def pack(self, names):
+        """Re-home the named tensors as views of one device buffer (256-byte aligned slots)
+        and return a pinned host buffer with the same layout, so that one copy moves them
+        all. Call it before capturing a graph that uses them."""
+        slots, off = [], 0
+        for name in names:
+            t = getattr(self, name)
+            slots.append((name, off))
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        dev_buf = torch.empty(max(off, 256), dtype=torch.uint8, device=self.device)
+        host_buf = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+        for name, o in slots:
+            t = getattr(self, name)
+            n = t.numel() * t.element_size()
+            view = dev_buf[o:o + n].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            host_buf[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+            setattr(self, name, view)
+        return dev_buf, host_buf
+
     # --- the four calls -------------------------------------------------------------
     def build_mask(self, stream=None):
         return B.spec_build_tree_mask(self.parent, self.qo, self.max_nodes, self.mask, self.depth, self.status,
