@@ -457,3 +457,18 @@ def test_accept_commit_fused_bad_page(inputs, cfg):
                                  inp.page_size)
     assert np.array_equal(db.k_pool.float().cpu().numpy(), k2)
     assert np.array_equal(db.v_pool.float().cpu().numpy(), v2)
+
+
+@pytest.mark.parametrize("cfg", [5])
+def test_accept_greedy_after_stochastic_same_workspace(inputs, cfg):
+    """One workspace serving both modes in turn: greedy after stochastic (and again) is
+    still exact -- the greedy call's scratch is not left over from the stochastic one."""
+    inp = inputs(cfg)
+    db = DeviceBatch(inp, mode="stochastic")
+    ref = _oracle_accept(inp, "greedy")
+    for mode in ("stochastic", "greedy", "stochastic", "greedy"):
+        db.accept(mode)
+        torch.cuda.synchronize()
+        assert _status(db) == 0
+        if mode == "greedy":
+            assert _accept_compare(db, ref) == 0
