@@ -49,8 +49,23 @@
  *     it when it wants a fresh report.
  *   - Workspace: `ws` is scratch of at least spec_workspace_size(...) bytes,
  *     256-byte aligned. It must be zero-filled before its first use with
- *     spec_accept; every call leaves the counters it uses at zero again. One
- *     workspace must not serve two calls that may run concurrently.
+ *     spec_accept (it keeps arrival counters there); every call leaves the
+ *     counters it uses at zero again. One workspace must not serve two calls
+ *     that may run concurrently.
+ *   - Early start: the kernels are launched with programmatic stream
+ *     serialization, so a call may begin while the kernel enqueued before it
+ *     is still running. Every kernel waits for that predecessor before it
+ *     writes anything and before it reads what the predecessor may write,
+ *     with one exception: spec_tree_verify_attn reads q, k_pool, v_pool,
+ *     k_tree, v_tree, page_table, prefix_len and qo_indptr (everything but
+ *     the mask) before that wait. If the kernel enqueued just before it
+ *     writes one of those and signals its dependents early (the
+ *     griddepcontrol.launch_dependents instruction), put an event or another
+ *     kernel between the two. Kernels that never signal early (the usual
+ *     case) need nothing. Of this library's kernels, the ones that signal
+ *     early write only mask and depth (spec_build_tree_mask), out and lse
+ *     (the attention's split merge) and the acceptance results (greedy
+ *     spec_accept); the commit kernels, which write the pool, never do.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -151,7 +166,7 @@ int spec_build_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int ba
  *   out        [total_nodes][hq][d] (out)
  *   lse        float [total_nodes][hq] (out, nullable)  natural-log log-sum-exp.
  *   ws         workspace of spec_workspace_size(SPEC_OP_ATTN, ...) bytes (key-split
- *              partial results).
+ *              partial results; any contents).
  *   Device errors: SPEC_ERR_PAGE (page id outside [0, num_pages): the page is read
  *   as zeros), SPEC_ERR_TIMEOUT.
  */

@@ -18,9 +18,10 @@
 //                          waiting) merges the partials into every row's argmax and
 //                          walks every sequence, one warp each.
 // Stochastic, two launches:
-//   accept_stats_kernel    grid = chunks x nodes. Per row of target and draft logits:
-//                          max and sum of exp((x - max) / T) (fp32 elements, Kahan
-//                          compensated, fp64 across threads and chunks).
+//   accept_stats_kernel    grid = chunks x nodes. Per chunk of a row of target and
+//                          draft logits: max and sum of exp((x - max) / T) (fp32
+//                          elements, Kahan compensated, fp64 across threads). The walk
+//                          merges a node's chunk partials when it visits the node.
 //   accept_walk_kernel     one 8-CTA cluster per sequence. The decisions at a node
 //                          need sums over the vocabulary of the residual
 //                          max(p - c q, 0) (see below); each CTA sums its eighth of the
@@ -67,14 +68,16 @@ struct NodeStats {
   double z_p, z_q;
 };
 
-// Workspace layout for spec_accept (offsets in bytes, each 256-aligned).
+// Workspace layout for spec_accept (offsets in bytes, each 256-aligned). The one
+// counter (greedy's finished-CTA count) sits at offset 0 for every size and mode and
+// every call leaves it at zero, so no size change can hand it stale partial data.
 struct AcceptWs {
-  size_t node_cnt, seq_cnt, partials, results, total;
+  size_t counter, partials, results, total;
   static AcceptWs make(int batch, int total_nodes, int chunks) {
+    (void)batch;
     AcceptWs w;
     size_t off = 0;
-    w.node_cnt = off; off = align_up(off + sizeof(unsigned) * (size_t)total_nodes, 256);
-    w.seq_cnt = off;  off = align_up(off + sizeof(unsigned) * (size_t)batch, 256);
+    w.counter = off;  off = align_up(off + sizeof(unsigned), 256);
     w.partials = off; off = align_up(off + sizeof(StatPartial) * (size_t)total_nodes * chunks, 256);
     w.results = off;  off = align_up(off + sizeof(NodeStats) * (size_t)total_nodes, 256);
     w.total = off;
@@ -542,7 +545,7 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
 template <bool kVec>
 __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
     const float* __restrict__ tl, const float* __restrict__ dl, int vocab, int chunks, float invT,
-    unsigned* node_cnt, StatPartial* partials, NodeStats* stats) {
+    StatPartial* partials) {
   const int t = blockIdx.x / chunks;
   const int c = blockIdx.x - t * chunks;
   int lo, hi;
@@ -579,7 +582,6 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
   }
   __shared__ float redf[kAcceptThreads / 32];
   __shared__ double redd[kAcceptThreads / 32];
-  __shared__ bool s_last;
   const float Mp = block_max(ep.m, redf);
   const float Mq = block_max(eq.m, redf);
   const double Sp = block_sum(ep.m == -INFINITY ? 0.0 : (double)ep.s * (double)expf((ep.m - Mp) * invT), redd);
@@ -587,29 +589,42 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
   if (threadIdx.x == 0) {
     partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, Sp, Sq};
     pdl_trigger();
-    __threadfence();
-    s_last = atomicAdd(node_cnt + t, 1u) == (unsigned)(chunks - 1);
   }
-  __syncthreads();
-  if (!s_last || threadIdx.x != 0) return;
-  const volatile StatPartial* vp = partials + (size_t)t * chunks;
+}
+
+// Statistics of one row from its chunk partials, by one warp: lane k takes chunks k,
+// k + 32, ... in order, then a fixed xor tree. Every CTA that calls it for the same row
+// gets bitwise the same result.
+__device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float invT) {
+  const int lane = threadIdx.x & 31;
   float mp = -INFINITY, mq = -INFINITY;
-  for (int k = 0; k < chunks; ++k) {
-    mp = fmaxf(mp, vp[k].m_p);
-    mq = fmaxf(mq, vp[k].m_q);
+  for (int k = lane; k < chunks; k += 32) {
+    mp = fmaxf(mp, __ldcg(&part[k].m_p));
+    mq = fmaxf(mq, __ldcg(&part[k].m_q));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+    mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
   }
   double zp = 0.0, zq = 0.0;
-  for (int k = 0; k < chunks; ++k) {
-    if (vp[k].m_p != -INFINITY) zp += vp[k].s_p * (double)expf((vp[k].m_p - mp) * invT);
-    if (vp[k].m_q != -INFINITY) zq += vp[k].s_q * (double)expf((vp[k].m_q - mq) * invT);
+  for (int k = lane; k < chunks; k += 32) {
+    const float m_p = __ldcg(&part[k].m_p), m_q = __ldcg(&part[k].m_q);
+    if (m_p != -INFINITY) zp += __ldcg(&part[k].s_p) * (double)expf((m_p - mp) * invT);
+    if (m_q != -INFINITY) zq += __ldcg(&part[k].s_q) * (double)expf((m_q - mq) * invT);
   }
-  stats[t] = NodeStats{mp, mq, zp, zq};
-  node_cnt[t] = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    zp += __shfl_xor_sync(0xffffffffu, zp, o);
+    zq += __shfl_xor_sync(0xffffffffu, zq, o);
+  }
+  return NodeStats{mp, mq, zp, zq};
 }
 
 // ---------------------------------------------------------------- stochastic: walk
 
 struct WalkShared {
+  NodeStats st;                       // statistics of the node being visited
   double part[2][kWalkThreads / 32];  // block reduction scratch
   double cta_sum[2];                  // this CTA's pass total (double-buffered by pass parity)
   double scan[kWalkThreads];          // per-thread sums for the bonus search
@@ -667,8 +682,8 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     accept_walk_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
                        const float* __restrict__ tl, const float* __restrict__ dl,
                        const float* __restrict__ uniforms, float temperature, int vocab,
-                       const int32_t* __restrict__ qo, int path_cap, const NodeStats* stats,
-                       int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+                       const int32_t* __restrict__ qo, int path_cap, const StatPartial* partials,
+                       int chunks, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
                        int32_t* status) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ WalkShared sh;
@@ -690,12 +705,16 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   int v = 0, L = 0, flag = 0, bonus = 0;
   int parity = 0;
   while (true) {
-    const NodeStats st = stats[base + v];
-    RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
-               (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
+    if (threadIdx.x < 32) {  // v's statistics from its chunk partials (the load overlaps the bitmap)
+      const NodeStats m = merge_row_stats(partials + (size_t)(base + v) * chunks, chunks, invT);
+      if (threadIdx.x == 0) sh.st = m;
+    }
     // children bitmap of v
     for (int w = threadIdx.x; w < kMaxTreeNodes / 32; w += blockDim.x) sh.kids[w] = 0u;
     __syncthreads();
+    const NodeStats st = sh.st;
+    RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
+               (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
     for (int c = v + 1 + threadIdx.x; c < n; c += blockDim.x)
       if (__ldg(parent + base + c) == v) atomicOr(&sh.kids[c >> 5], 1u << (c & 31));
     __syncthreads();
@@ -855,7 +874,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   const int chunks = accept_chunks(total_nodes, vocab);
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
   uint8_t* wb = static_cast<uint8_t*>(ws);
-  unsigned* node_cnt = reinterpret_cast<unsigned*>(wb + w.node_cnt);
+  unsigned* counter = reinterpret_cast<unsigned*>(wb + w.counter);
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
                    (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
   const dim3 grid((unsigned)(total_nodes * chunks));
@@ -880,22 +899,21 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     const int per_cta = ceil_div(tasks, occ * sms);
     const int grid_n = ceil_div(tasks, per_cta);
     if (launch_pdl(kern, dim3((unsigned)grid_n), dim3(kAcceptThreads), 0, stream, tl, vocab, gch, tasks, qo, batch,
-                   total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, node_cnt, part, am,
+                   total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, counter, part, am,
                    status, ca) != cudaSuccess)
       return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   StatPartial* part = reinterpret_cast<StatPartial*>(wb + w.partials);
-  NodeStats* st = reinterpret_cast<NodeStats*>(wb + w.results);
   const float invT = 1.0f / temperature;
   if (vec)
-    accept_stats_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, node_cnt, part, st);
+    accept_stats_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
   else
-    accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, node_cnt, part, st);
+    accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), 0, stream, parent, tokens, tl,
-                 dl, uniforms, temperature, vocab, qo, path_cap, (const NodeStats*)st, accept_len, path, out_tokens,
-                 flags, status) != cudaSuccess)
+                 dl, uniforms, temperature, vocab, qo, path_cap, (const StatPartial*)part, chunks, accept_len, path,
+                 out_tokens, flags, status) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (ca.k_tree == nullptr) return SPEC_OK;

@@ -264,6 +264,42 @@ def test_attention_workspace_too_small(inputs):
     assert ei.value.status == -5
 
 
+def test_attention_workspace_shared_across_sizes(inputs):
+    """One workspace serving split launches of two different plans, in turn and back to back
+    in one stream (each call may start while the previous call's merge still runs): every
+    call equals a call on its own fresh workspace, bit for bit. The workspace starts as
+    garbage: the attention needs no zeroed scratch."""
+    a = DeviceBatch(inputs(2))
+    b = DeviceBatch(_sensitive("bf16", 32, 8, 128, [300, 2000, 70], [9, 40, 17], seed=21))
+    plans = [db.attn_plan()[0] for db in (a, b)]
+    assert min(plans) > 1 and plans[0] != plans[1], plans
+    refs = []
+    for db in (a, b):
+        db.build_mask()
+        db.attention()
+        torch.cuda.synchronize()
+        assert _status(db) == 0
+        refs.append(db.out.clone())
+    need = max(db.attn_ws.numel() for db in (a, b))
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
+    for db in (a, b):
+        db.attn_ws = ws
+    for it, db in enumerate([b, a, a, b, a, b, b]):
+        db.out.zero_()
+        db.attention()
+        torch.cuda.synchronize()
+        assert _status(db) == 0, it
+        assert torch.equal(db.out, refs[0 if db is a else 1]), it
+    # back to back with no host sync: each call may start while the previous one's merge runs
+    a.out.zero_()
+    b.out.zero_()
+    for db in [a, b, b, a, b, a]:
+        db.attention()
+    torch.cuda.synchronize()
+    assert _status(a) == 0 and _status(b) == 0
+    assert torch.equal(a.out, refs[0]) and torch.equal(b.out, refs[1])
+
+
 # ----------------------------------------------------------------------------- accept
 
 def _oracle_accept(inp, mode):
@@ -472,3 +508,36 @@ def test_accept_greedy_after_stochastic_same_workspace(inputs, cfg):
         assert _status(db) == 0
         if mode == "greedy":
             assert _accept_compare(db, ref) == 0
+
+
+def test_accept_workspace_shared_across_sizes(inputs):
+    """One workspace serving acceptance calls of different sizes and modes in turn. Every
+    byte past the first 256 (the one counter) starts as garbage, and the bigger call comes
+    after the smaller one, so no size-dependent counter could start from stale data: each
+    call must equal the same call on its own fresh workspace, bit for bit."""
+    small = DeviceBatch(inputs(5), mode="stochastic")
+    big = DeviceBatch(inputs(4), mode="stochastic")
+    assert big.T > small.T
+    refs = {}
+    for db in (small, big):
+        for mode in ("stochastic", "greedy"):
+            db.accept(mode)
+            torch.cuda.synchronize()
+            assert _status(db) == 0
+            refs[(id(db), mode)] = [x.clone() for x in (db.accept_len, db.path, db.out_tokens, db.flags)]
+    need = max(small.acc_ws.numel(), big.acc_ws.numel())
+    ws = torch.full((need,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws[:256] = 0
+    small.acc_ws = ws
+    big.acc_ws = ws
+    for db, mode in [(small, "stochastic"), (big, "stochastic"), (small, "greedy"), (big, "greedy"),
+                     (big, "stochastic"), (small, "stochastic")]:
+        for x in (db.accept_len, db.path, db.out_tokens, db.flags):
+            x.fill_(-7 if x.dtype != torch.uint8 else 7)
+        db.accept(mode)
+        torch.cuda.synchronize()
+        assert _status(db) == 0
+        got = (db.accept_len, db.path, db.out_tokens, db.flags)
+        for g, r in zip(got, refs[(id(db), mode)]):
+            assert torch.equal(g, r), (mode, db.T)
+    assert int(ws[:256].sum()) == 0
