@@ -13,10 +13,11 @@
 // Greedy, one launch:
 //   accept_greedy_kernel   one wave of CTAs streams every logits row in 4096-logit
 //                          tasks (16-byte loads, the next task's loads in flight while
-//                          the current one is reduced) and keeps (max, first index)
-//                          per task. The last CTA to finish (atomic counter, no
-//                          waiting) merges the partials into every row's argmax and
-//                          walks every sequence, one warp each.
+//                          the current one is reduced); each task folds its (max, first
+//                          index) into its row's slot with one 64-bit atomicMax. The
+//                          last CTA to finish (atomic counter, no waiting) reads every
+//                          row's argmax from the slots and walks every sequence, one
+//                          warp each.
 // Stochastic, two launches:
 //   accept_stats_kernel    grid = chunks x nodes. Per chunk of a row of target and
 //                          draft logits: max and sum of exp((x - max) / T) (fp32
@@ -68,16 +69,19 @@ struct NodeStats {
   double z_p, z_q;
 };
 
-// Workspace layout for spec_accept (offsets in bytes, each 256-aligned). The one
-// counter (greedy's finished-CTA count) sits at offset 0 for every size and mode and
-// every call leaves it at zero, so no size change can hand it stale partial data.
+// Workspace layout for spec_accept (offsets in bytes, each 256-aligned). The greedy
+// kernel's counter (finished CTAs) and its per-row argmax slots sit in a fixed area at
+// the start, the same for every size and mode, that holds nothing else; every call leaves
+// them at zero, so no size change can hand them stale partial data.
+constexpr int kArgSlots = 8192;  // rows whose argmax is folded in a slot (more: task partials)
 struct AcceptWs {
-  size_t counter, partials, results, total;
+  size_t counter, slots, partials, results, total;
   static AcceptWs make(int batch, int total_nodes, int chunks) {
     (void)batch;
     AcceptWs w;
     size_t off = 0;
     w.counter = off;  off = align_up(off + sizeof(unsigned), 256);
+    w.slots = off;    off = align_up(off + sizeof(unsigned long long) * kArgSlots, 256);
     w.partials = off; off = align_up(off + sizeof(StatPartial) * (size_t)total_nodes * chunks, 256);
     w.results = off;  off = align_up(off + sizeof(NodeStats) * (size_t)total_nodes, 256);
     w.total = off;
@@ -105,6 +109,16 @@ __device__ __forceinline__ void arg_better(float& v, int& i, float v2, int i2) {
     i = i2;
   }
 }
+
+// (value, index) as one 64-bit key whose unsigned order is the argmax order: larger
+// value first, then the lower index (the index is stored complemented). Every real key
+// is > 0, so 0 marks an empty slot.
+__device__ __forceinline__ unsigned long long arg_key(float v, int i) {
+  unsigned u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned)(~i);
+}
+__device__ __forceinline__ int arg_key_index(unsigned long long key) { return (int)~(unsigned)key; }
 
 __device__ __forceinline__ void warp_arg_reduce(float& v, int& i) {
 #pragma unroll
@@ -175,9 +189,10 @@ __device__ void greedy_walk_warp(int b, int n, const int* parent, const int* tok
 // row; the grid is one wave of CTAs (as many as fit on the SMs at once) and CTA i takes
 // tasks i, i + grid, ... with the loads of its next task issued before the current one
 // is reduced, so every SM keeps two tasks of loads in flight until the stream ends. A
-// task leaves one (max, first index) partial. The last CTA to finish (one counter,
-// no waiting) merges the partials of every row and walks every sequence, one warp per
-// sequence, on the tree staged in shared memory.
+// task folds its (max, first index) into its row's slot (64-bit atomicMax on an
+// order-preserving key; beyond kArgSlots rows it leaves a partial instead). The last CTA
+// to finish (one counter, no waiting) reads every row's argmax (or merges the partials)
+// and walks every sequence, one warp per sequence, on the tree staged in shared memory.
 constexpr int kGreedyVec = 4;                                  // float4 per thread per task
 constexpr int kGreedyChunk = kAcceptThreads * kGreedyVec * 4;  // 4096 logits
 constexpr int kGreedyStage = 2048;                             // nodes the final CTA stages
@@ -321,7 +336,7 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     const float* __restrict__ logits, int vocab, int gchunks, int tasks, const int32_t* __restrict__ qo,
     int batch, int total_nodes, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
     int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, unsigned* done,
-    ArgPartial* partials, int* argmax, int32_t* status, const CommitArgs ca) {
+    unsigned long long* slots, ArgPartial* partials, int* argmax, int32_t* status, const CommitArgs ca) {
   __shared__ float sv[2][kAcceptThreads / 32];
   __shared__ int si[2][kAcceptThreads / 32];
   __shared__ bool s_last;
@@ -400,7 +415,8 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     __syncthreads();
     if (threadIdx.x == 0) {
       for (int w = 1; w < kAcceptThreads / 32; ++w) arg_better(bv, bi, sv[k & 1][w], si[k & 1][w]);
-      partials[task] = ArgPartial{bv, bi};
+      if (slots != nullptr) atomicMax(slots + t, arg_key(bv, bi));  // the row's running argmax
+      else partials[task] = ArgPartial{bv, bi};
     }
   }
   if (threadIdx.x == 0) {
@@ -425,9 +441,19 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
       s_tok[i] = __ldg(tokens + i);
     }
   }
+  if (slots != nullptr) {  // each row's argmax is already folded into its slot
+    for (int t = threadIdx.x; t < total_nodes; t += kAcceptThreads) {
+      const unsigned long long key = __ldcg(slots + t);
+      slots[t] = 0ull;  // empty again for the next call
+      const int ix = arg_key_index(key);
+      const int a = (key == 0ull || ix < 0 || ix >= vocab) ? 0 : ix;
+      if (staged) s_am[t] = a;
+      else argmax[t] = a;
+    }
+  }
   // warp w: rows w, w + 8, ...; eight rows' partials loaded before any is reduced
   constexpr int kRowsPerPass = 8;
-  for (int t0 = warp; t0 < total_nodes; t0 += kRowsPerPass * (kAcceptThreads / 32)) {
+  for (int t0 = warp; slots == nullptr && t0 < total_nodes; t0 += kRowsPerPass * (kAcceptThreads / 32)) {
     float v[kRowsPerPass];
     int ix[kRowsPerPass];
 #pragma unroll
@@ -899,7 +925,8 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     const int per_cta = ceil_div(tasks, occ * sms);
     const int grid_n = ceil_div(tasks, per_cta);
     if (launch_pdl(kern, dim3((unsigned)grid_n), dim3(kAcceptThreads), 0, stream, tl, vocab, gch, tasks, qo, batch,
-                   total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, counter, part, am,
+                   total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, counter,
+                   total_nodes <= kArgSlots ? reinterpret_cast<unsigned long long*>(wb + w.slots) : nullptr, part, am,
                    status, ca) != cudaSuccess)
       return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

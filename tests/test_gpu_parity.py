@@ -335,14 +335,16 @@ def test_accept_config(inputs, cfg, mode):
     assert (db.accept_len.cpu().numpy() <= inp.max_depth).all()
 
 
-@pytest.mark.parametrize("seed", range(3))
-def test_accept_greedy_ties_and_duplicates(seed):
-    """Quantised logits (many exact ties) and duplicate sibling tokens."""
+@pytest.mark.parametrize("seed,Bn,V,nmax", [(0, 40, 37, 40), (1, 40, 64, 40), (2, 40, 37, 40),
+                                             (3, 300, 37, 64), (4, 300, 64, 64)])
+def test_accept_greedy_ties_and_duplicates(seed, Bn, V, nmax):
+    """Quantised logits (many exact ties) and duplicate sibling tokens. The 300-sequence
+    cases hold more than 8192 rows, past the per-row argmax slots (task partials, then a
+    merge in the last CTA); V = 64 takes the 16-byte load path, V = 37 the scalar one."""
     rng = np.random.default_rng(seed)
-    Bn, V = 40, 37
     parents, toks, qo = [], [], [0]
     for b in range(Bn):
-        n = int(rng.integers(1, 40))
+        n = int(rng.integers(1, nmax))
         p = [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
         parents.append(p)
         toks.append(rng.integers(0, 4, n))
@@ -356,7 +358,8 @@ def test_accept_greedy_ties_and_duplicates(seed):
     inp = replace(inp, qo_indptr=np.array(qo, np.int32), parent=np.concatenate(parents).astype(np.int32),
                   draft_tokens=np.concatenate(toks).astype(np.int32), target_logits=logits, vocab=V,
                   q=np.zeros((T, 4, 64), np.float32), k_tree=np.zeros((T, 1, 64), np.float32),
-                  v_tree=np.zeros((T, 1, 64), np.float32), max_depth=40)
+                  v_tree=np.zeros((T, 1, 64), np.float32), max_depth=nmax)
+    assert (T > 8192) == (Bn == 300), T
     db = DeviceBatch(inp)
     db.accept("greedy")
     torch.cuda.synchronize()
