@@ -256,19 +256,22 @@ __device__ int greedy_walk_warp_staged(int b, int n, const int* parent, const in
 // is validated and the first rows' K/V are loaded before the team's vote, so a valid
 // commit costs one memory round trip; a sequence with an error is reported and left
 // unwritten.
+// Rows `first` .. L are copied (first = 1 when the root row went early, see
+// commit_root_early, whose P is then passed as P_pre; P_pre < 0: P is read here).
 template <bool kCta>
 __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, int L, const int* spath,
-                                const int32_t* gpath, int path_cap, int32_t* status) {
+                                const int32_t* gpath, int path_cap, int32_t* status, int first = 0,
+                                int P_pre = -1) {
   const int rank = kCta ? (int)threadIdx.x : (int)(threadIdx.x & 31);
   const int size = kCta ? (int)blockDim.x : 32;
-  const int P = __ldg(ca.prefix_len + b);
+  const int P = P_pre >= 0 ? P_pre : __ldg(ca.prefix_len + b);
   const int32_t* prow_pt = ca.page_table + (size_t)b * ca.max_pages;
   auto node_at = [&](int i) { return spath != nullptr ? spath[i] : gpath[i]; };
   int code = 0;
   if (L < 0 || L >= path_cap || L >= n || P < 0) {
     code = SPEC_ERR_INDEX;
   } else {
-    for (int i = rank; i <= L; i += size) {
+    for (int i = first + rank; i <= L; i += size) {
       const int node = node_at(i);
       const int lp = (P + i) / ca.page_size;
       const int page = lp < ca.max_pages ? __ldg(prow_pt + lp) : -1;
@@ -281,14 +284,14 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
   }
   const int row_bytes = ca.d * ca.elem_bytes;
   const int vecs = row_bytes >> 4;
-  const int total = code == 0 ? (L + 1) * ca.hkv * vecs : 0;
+  const int total = code == 0 && L >= first ? (L + 1 - first) * ca.hkv * vecs : 0;
   // the first rows' loads go out with the checks (a row only if its node is in range)
   constexpr int kPer = 2;
   uint4 kb[kPer], vb[kPer];
   size_t dsts[kPer];
   auto locate = [&](int e, size_t& src, size_t& dst) {
     const int r = e / vecs, vi = e - (e / vecs) * vecs;
-    const int i = r / ca.hkv, g = r - (r / ca.hkv) * ca.hkv;
+    const int i = first + r / ca.hkv, g = r - (r / ca.hkv) * ca.hkv;
     const int slot = P + i;
     const int node = node_at(i);
     const int lp = slot / ca.page_size;
@@ -328,6 +331,61 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
     *reinterpret_cast<uint4*>(ca.v_pool + dst) = vv;
   }
   if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
+}
+
+// ---- the root row committed while the walk runs (fused greedy commit, few sequences)
+// The root (node 0, the last accepted token) always goes to slot P, whatever the walk
+// decides; only rows 1 .. L wait for it. One warp of the final CTA stages the root rows
+// with asynchronous copies into shared memory the walk leaves unused (root_stage), then,
+// while the walk runs, checks every slot the walk could reach (P .. P + path_cap - 1):
+// when all lie in valid pages nothing after the walk can fail, so the row is written at
+// once and the result is that of committing after the walk (root_write); otherwise the
+// commit after the walk copies it (and reports the error).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(smem)),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Root K/V rows of the sequence whose node 0 is global row `base` into buf (K, then V).
+__device__ void root_stage(const CommitArgs& ca, int base, uint4* buf) {
+  const int lane = threadIdx.x & 31;
+  const int row_bytes = ca.d * ca.elem_bytes, chunks = ca.hkv * row_bytes / 16;
+  const size_t src = (size_t)base * ca.hkv * row_bytes;  // node 0: its heads back to back
+  for (int e = lane; e < chunks; e += 32) {
+    cp_async16(buf + e, ca.k_tree + src + ((size_t)e << 4));
+    cp_async16(buf + chunks + e, ca.v_tree + src + ((size_t)e << 4));
+  }
+}
+
+// The staged root rows of sequence b to slot P, when every reachable slot's page is valid
+// (each lane stores the chunks its own copies staged). Returns P when written, else -1.
+__device__ int root_write(const CommitArgs& ca, int b, int P, int n, int path_cap, const uint4* buf) {
+  const int lane = threadIdx.x & 31;
+  if (P < 0 || n < 1 || path_cap < 1) return -1;
+  const int lp0 = P / ca.page_size, lp1 = (P + path_cap - 1) / ca.page_size;
+  if (lp1 - lp0 >= 32) return -1;
+  int page = -1;
+  bool ok = true;
+  if (lp0 + lane <= lp1) {
+    const int lp = lp0 + lane;
+    page = lp < ca.max_pages ? __ldg(ca.page_table + (size_t)b * ca.max_pages + lp) : -1;
+    ok = page >= 0 && page < ca.num_pages;
+  }
+  if (!__all_sync(0xffffffffu, ok)) return -1;
+  const int pg = __shfl_sync(0xffffffffu, page, 0);
+  const int row_bytes = ca.d * ca.elem_bytes, vecs = row_bytes >> 4, chunks = ca.hkv * vecs;
+  const size_t dst0 = ((size_t)pg * ca.hkv * ca.page_size + P % ca.page_size) * row_bytes;
+  for (int e = lane; e < chunks; e += 32) {
+    const int g = e / vecs, vi = e - g * vecs;
+    const size_t dst = dst0 + (size_t)g * ca.page_size * row_bytes + ((size_t)vi << 4);
+    *reinterpret_cast<uint4*>(ca.k_pool + dst) = buf[e];
+    *reinterpret_cast<uint4*>(ca.v_pool + dst) = buf[chunks + e];
+  }
+  return P;
 }
 
 // (five CTAs per SM: the streaming loop needs the occupancy, the final CTA's epilogue may spill)
@@ -430,11 +488,33 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
   if (!s_last) return;
 
   // ---- the last CTA: argmax of every row, then the walk of every sequence
-  __shared__ int s_par[kGreedyStage], s_tok[kGreedyStage], s_am[kGreedyStage], s_child[kGreedyStage];
+  __shared__ __align__(16) int s_stage[4][kGreedyStage];
+  int* const s_par = s_stage[0];
+  int* const s_tok = s_stage[1];
+  int* const s_am = s_stage[2];
+  int* const s_child = s_stage[3];
   __shared__ int s_len[kCommitCta];                     // L of sequences 0 .. 3 (fused commit)
+  __shared__ int s_root_P[kCommitCta];                  // P when their root row went early, else -1
   __shared__ int s_cpath[kCommitCta][kCommitPathStage];  // their paths, when path_cap fits
   const bool staged = total_nodes <= kGreedyStage;
   if (threadIdx.x == 0) done[0] = 0u;  // every CTA has counted itself: ready for the next call
+  // root rows of the fused commit: staged by the last warp (warps 0 .. batch - 1 walk) in
+  // the upper halves of the staging arrays, which hold nothing when the trees are small
+  constexpr int kRootWarp = kAcceptThreads / 32 - 1;
+  const int root_chunks = ca.k_tree != nullptr ? ca.hkv * ca.d * ca.elem_bytes / 16 : 0;
+  const bool early = ca.k_tree != nullptr && batch <= kCommitCta && total_nodes <= kGreedyStage / 2 &&
+                     2 * root_chunks * 16 <= (kGreedyStage / 2) * (int)sizeof(int);
+  auto root_buf = [&](int b) { return reinterpret_cast<uint4*>(s_stage[b] + kGreedyStage / 2); };
+  int root_P = -1, root_n = 0;  // lane b of the root warp: sequence b's prefix length, node count
+  if (early && warp == kRootWarp) {
+    int base = 0;
+    if (lane < batch) {
+      base = __ldg(qo + lane);
+      root_n = __ldg(qo + lane + 1) - base;
+      root_P = __ldg(ca.prefix_len + lane);  // not waited for before the walk
+    }
+    for (int b = 0; b < batch; ++b) root_stage(ca, __shfl_sync(0xffffffffu, base, b), root_buf(b));
+  }
   if (staged) {
     for (int i = threadIdx.x; i < total_nodes; i += kAcceptThreads) {
       s_par[i] = __ldg(parent + i);
@@ -499,6 +579,14 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
       greedy_walk_warp(b, n, parent + base, tokens + base, argmax + base, path_cap, accept_len, path, out_tokens,
                        flags, status);
   }
+  if (early && warp == kRootWarp) {  // while warps 0 .. batch - 1 walk
+    cp_async_wait_all();
+    for (int b = 0; b < batch; ++b) {
+      const int r = root_write(ca, b, __shfl_sync(0xffffffffu, root_P, b), __shfl_sync(0xffffffffu, root_n, b),
+                               path_cap, root_buf(b));
+      if (lane == 0) s_root_P[b] = r;
+    }
+  }
   if (ca.k_tree == nullptr) return;
   // ---- fused commit of every sequence's accepted path
   __syncthreads();  // accept_len and the path rows written above are visible to the CTA
@@ -506,8 +594,10 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     const bool in_smem = staged && path_cap <= kCommitPathStage;
     for (int b = 0; b < batch; ++b) {
       const int base = __ldg(qo + b);
+      const int rootP = early ? s_root_P[b] : -1;
       commit_sequence<true>(ca, b, base, __ldg(qo + b + 1) - base, staged ? s_len[b] : accept_len[b],
-                            in_smem ? s_cpath[b] : nullptr, path + (size_t)b * path_cap, path_cap, status);
+                            in_smem ? s_cpath[b] : nullptr, path + (size_t)b * path_cap, path_cap, status,
+                            rootP >= 0 ? 1 : 0, rootP);
       __syncthreads();
     }
   } else {

@@ -498,6 +498,41 @@ def test_accept_commit_fused_bad_page(inputs, cfg):
     assert np.array_equal(db.v_pool.float().cpu().numpy(), v2)
 
 
+@pytest.mark.parametrize("P", [120, 124, 126, 127, 128])
+@pytest.mark.parametrize("deep", [False, True])
+def test_accept_commit_fused_equals_separate_near_bad_page(inputs, P, deep):
+    """The reachable commit slots (P .. P + path_cap - 1) straddle a page boundary and the
+    second page is outside the pool: the fused call (which may copy the root row before the
+    walk) must leave exactly what spec_accept followed by spec_kv_commit leaves -- the same
+    status, pool bytes, seq_len and acceptance results, whether or not the accepted path
+    reaches the bad page. `deep`: every draft token is its parent's target argmax, so the
+    walk accepts a path as deep as the tree (rows past the root are committed too)."""
+    from dataclasses import replace
+    base = inputs(1)
+    pt = base.page_table.copy()
+    pt[0, 128 // base.page_size] = base.num_pages + 3
+    tokens = base.draft_tokens.copy()
+    if deep:
+        am = base.target_logits.argmax(axis=1)
+        tokens[1:] = am[base.parent[1:]]
+    inp = replace(base, prefix_len=np.array([P], np.int32), page_table=pt, draft_tokens=tokens)
+    fused, sep = DeviceBatch(inp), DeviceBatch(inp)
+    fused.accept_commit("greedy")
+    sep.accept("greedy")
+    sep.commit()
+    torch.cuda.synchronize()
+    assert _status(fused) == _status(sep)
+    for x, y in [(fused.accept_len, sep.accept_len), (fused.path, sep.path), (fused.out_tokens, sep.out_tokens),
+                 (fused.seq_len, sep.seq_len), (fused.k_pool, sep.k_pool), (fused.v_pool, sep.v_pool)]:
+        assert torch.equal(x, y)
+    L = int(sep.accept_len.item())
+    assert (L >= 2) == deep, L
+    reaches = P + L >= 128
+    assert _status(sep) == (-3 if reaches else 0), (P, L)
+    ref = _oracle_accept(inp, "greedy")
+    assert _accept_compare(fused, ref) == 0
+
+
 @pytest.mark.parametrize("cfg", [5])
 def test_accept_greedy_after_stochastic_same_workspace(inputs, cfg):
     """One workspace serving both modes in turn: greedy after stochastic (and again) is
