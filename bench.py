@@ -33,9 +33,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify attn tokens/s, TFLOP/s & GB/s (% roofline); accept+commit µs/step"
-WORKLOAD = "llama3-8b-single-verify: bf16, B1, Hq32/Hkv8, D128, prefix 4096 (16-token pages, shuffled), " \
-           "64-node EAGLE-2 tree (top-10, depth<=8), vocab 128256 fp32 logits, greedy + commit"
-CONFIG_INDEX = 2
+WORKLOADS = {
+    1: "tiny-fp32-verify: f32, B1, Hq4/Hkv1, D64, prefix 128 (identity pages), 16-node random tree (depth<=4), "
+       "vocab 1000, greedy + commit",
+    2: "llama3-8b-single-verify: bf16, B1, Hq32/Hkv8, D128, prefix 4096 (16-token pages, shuffled), "
+       "64-node EAGLE-2 tree (top-10, depth<=8), vocab 128256 fp32 logits, greedy + commit",
+    3: "llama3-8b-batch32-verify: bf16, B32, Hq32/Hkv8, D128, prefix U[512,8192] (16-token pages scattered over "
+       "one pool), 64-node EAGLE-2 trees, vocab 128256, greedy + commit",
+    4: "llama70b-32k-stochastic-verify: bf16, B8, Hq64/Hkv8, D128, prefix 32768, 128-node trees (top-10, "
+       "depth<=8), vocab 128256 target + draft fp32 logits, stochastic (T=1) + commit",
+    5: "chain-b128-verify: bf16, B128, Hq32/Hkv8, D128, prefix U[256,4096], draft chains of 1-8 tokens, "
+       "vocab 128256, greedy + commit",
+}
+CONFIG_INDEX = 2                # the workload the headline throughput is quoted on
 L2_BYTES = 256 << 20          # flush buffer, larger than the 129 MB L2
 
 
@@ -85,7 +95,7 @@ def job_throughput(tokens_all_ranks, max_rank_ms):
 
 # ----------------------------------------------------------------------------- work counts
 
-def work_counts(inp, accept_len=None):
+def work_counts(inp, accept_len=None, mode="greedy"):
     """Algorithmic FLOPs and bytes of one step's kernels (per launch)."""
     import numpy as np
 
@@ -107,7 +117,8 @@ def work_counts(inp, accept_len=None):
                      + inp.total_nodes * inp.hkv * inp.d * esz * 2  # tree K and V
                      + inp.total_nodes * inp.hq * inp.d * esz * 2   # Q in, O out
                      + inp.total_nodes * inp.mask_words * 8)
-    accept_bytes = int(inp.total_nodes * inp.vocab * 4)   # one pass over every node's logits
+    # one pass over every node's logits (target, and draft too for stochastic acceptance)
+    accept_bytes = int(inp.total_nodes * inp.vocab * 4 * (2 if mode == "stochastic" else 1))
     commit_bytes = 0
     if accept_len is not None:
         commit_bytes = int(((np.asarray(accept_len) + 1) * inp.hkv * inp.d * esz * 2 * 2).sum())
@@ -213,13 +224,18 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = W.generate_index(CONFIG_INDEX, seed=replica_seed(CONFIG_INDEX, rank))
+    idx = args.workload
+    inp = W.generate_index(idx, seed=replica_seed(idx, rank))
+    mode = W.SPECS[idx].modes[0]
+    wc0 = work_counts(inp, mode=mode)
     # R device replicas of the batch (same values, separate buffers): one graph replay runs
     # R steps back to back, each on a replica the previous steps did not touch, so every
-    # step reads its inputs from HBM (R x ~51 MB > the 129 MB L2); L2 is also flushed
-    # before every replay. R divides K so exactly K steps are timed.
-    R = max(r for r in range(1, 9) if args.steps % r == 0)
-    reps = [DeviceBatch(inp, device=dev, mode="greedy") for _ in range(R)]
+    # step reads its inputs from HBM (R x ~51 MB > the 129 MB L2 for the Llama-3-8B-shaped
+    # single sequence); L2 is also flushed before every replay. R divides K so exactly K
+    # steps are timed. A step whose inputs alone exceed twice the L2 needs one replica.
+    R = 1 if wc0["attn_bytes"] + wc0["accept_bytes"] > 2 * L2_BYTES else \
+        max(r for r in range(1, 9) if args.steps % r == 0)
+    reps = [DeviceBatch(inp, device=dev, mode=mode) for _ in range(R)]
     db = reps[0]
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_BYTES, dtype=torch.uint8, device=dev)
@@ -227,7 +243,7 @@ def run_ours(args):
 
     with torch.cuda.stream(stream):
         for rep in reps:                        # load the library, settle the workspaces
-            rep.step("greedy")
+            rep.step(mode)
     torch.cuda.synchronize()
     assert all(rep.device_status() == 0 for rep in reps)
 
@@ -240,14 +256,14 @@ def run_ours(args):
     def over_reps(name):
         def run():
             for rep in reps:
-                getattr(rep, name)("greedy") if name in ("accept", "accept_commit") else getattr(rep, name)()
+                getattr(rep, name)(mode) if name in ("accept", "accept_commit") else getattr(rep, name)()
         return run
 
-    g_step = capture(lambda: [rep.step("greedy") for rep in reps])
+    g_step = capture(lambda: [rep.step(mode) for rep in reps])
     g_calls = {"mask": capture(over_reps("build_mask")), "attention": capture(over_reps("attention")),
                "accept": capture(over_reps("accept")), "commit": capture(over_reps("commit")),
                "accept_commit": capture(over_reps("accept_commit"))}
-    launches = db.launches_per_step("greedy")
+    launches = db.launches_per_step(mode)
     splits, tc = db.attn_plan()
 
     def flush_l2():
@@ -296,17 +312,19 @@ def run_ours(args):
     # small inputs share one pinned buffer and one device buffer (one copy); the logits
     # (98% of the bytes) go up on a second stream while the mask and the attention run,
     # and the acceptance waits for them; the results come back in one copy.
-    e2e = DeviceBatch(inp, device=dev, mode="greedy")
-    small_dev, small_host = e2e.pack(DeviceBatch.STEP_INPUTS)
-    res_dev, res_host = e2e.pack(DeviceBatch.STEP_RESULTS)
-    logits_host = e2e.target_logits.cpu().pin_memory()
+    e2e = DeviceBatch(inp, device=dev, mode=mode)
+    stoch = mode == "stochastic"
+    small_dev, small_host = e2e.pack(DeviceBatch.STEP_INPUTS + (("uniforms",) if stoch else ()))
+    res_dev, res_host = e2e.pack(DeviceBatch.STEP_RESULTS + (("flags",) if stoch else ()))
+    big = [e2e.target_logits] + ([e2e.draft_logits] if stoch else [])   # the logits: one copy each
+    big_host = [x.cpu().pin_memory() for x in big]
     with torch.cuda.stream(stream):
-        e2e.step("greedy")
+        e2e.step(mode)
     torch.cuda.synchronize()
     g_front = capture(lambda: (e2e.build_mask(), e2e.attention()))
-    g_back = capture(lambda: e2e.accept_commit("greedy"))
+    g_back = capture(lambda: e2e.accept_commit(mode))
     copy_stream = torch.cuda.Stream(device=dev)
-    bi = small_host.numel() + logits_host.numel() * logits_host.element_size()
+    bi = small_host.numel() + sum(x.numel() * x.element_size() for x in big_host)
     bo = res_host.numel()
     e2e_ms = []
     for r in range(args.warmup + args.steps):
@@ -318,7 +336,8 @@ def run_ours(args):
             small_dev.copy_(small_host, non_blocking=True)
             copy_stream.wait_event(a)
             with torch.cuda.stream(copy_stream):
-                e2e.target_logits.copy_(logits_host, non_blocking=True)
+                for x, xh in zip(big, big_host):
+                    x.copy_(xh, non_blocking=True)
                 up.record(copy_stream)
             g_front.replay()
             stream.wait_event(up)
@@ -332,7 +351,7 @@ def run_ours(args):
     e2e_total = reduce_over_ranks(sum(e2e_ms), "max", ws, dev)
 
     # ---- figures ------------------------------------------------------------------------
-    wc = work_counts(inp, db.accept_len.cpu().numpy())
+    wc = work_counts(inp, db.accept_len.cpu().numpy(), mode)
     hbm, tfl, tfl_sus, peak_kind = _peaks()
     ms_step = total_ms / args.steps
     tokens_all = reduce_over_ranks(wc["tokens"], "sum", ws, dev) * args.steps
@@ -364,8 +383,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": inp.batch, "tree_nodes": inp.total_nodes,
+        "vs_baseline": None, "dtype": "bf16" if inp.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": WORKLOADS[idx], "batch": inp.batch, "tree_nodes": inp.total_nodes,
                    "prefix": int(inp.max_prefix), "hq": inp.hq, "hkv": inp.hkv, "head_dim": inp.d,
                    "vocab": inp.vocab,
                    "l2": f"inputs larger than L2: {R} device replicas rotated inside each replay "
@@ -389,7 +408,7 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds, mode)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -399,11 +418,15 @@ def run_ours(args):
 
 # ----------------------------------------------------------------------------- oracle arm
 
-def _oracle_step(inp, oracle):
+def _oracle_step(inp, oracle, mode="greedy"):
     mask, _ = oracle.ancestor_mask_batch(inp.parent, inp.qo_indptr, inp.max_nodes)
     oracle.tree_verify_attention(inp.q, inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree,
                                  inp.v_tree, mask, inp.qo_indptr, inp.hq, inp.hkv)
-    acc = oracle.greedy_accept(inp.parent, inp.draft_tokens, inp.target_logits, inp.qo_indptr, inp.path_cap)
+    if mode == "stochastic":
+        acc = oracle.stochastic_accept(inp.parent, inp.draft_tokens, inp.target_logits, inp.draft_logits,
+                                       inp.uniforms, inp.temperature, inp.qo_indptr, inp.path_cap)
+    else:
+        acc = oracle.greedy_accept(inp.parent, inp.draft_tokens, inp.target_logits, inp.qo_indptr, inp.path_cap)
     oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree, inp.v_tree, acc.path,
                      acc.accept_len, inp.qo_indptr, inp.page_size)
 
@@ -415,20 +438,31 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(inp, seconds):
-    """The oracle, as it stands, on the host cores: whole config steps for about `seconds`."""
+def oracle_sample(inp):
+    """What the oracle is timed on: the whole batch of one sequence, else its first sequence
+    (the oracle's cost grows linearly with the sequences, so tokens/s carries over)."""
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+
+    if inp.batch == 1:
+        return inp, "full verification steps of the same workload"
+    return W.subset(inp, [0]), (f"verification steps of sequence 0 of the batch ({int(inp.qo_indptr[1])} of "
+                                f"{inp.total_nodes} nodes)")
+
+
+def cpu_baseline(inp, seconds, mode="greedy"):
+    """The oracle, as it stands, on the host cores: whole steps for about `seconds`."""
     import oracle
 
+    smp, what = oracle_sample(inp)
     n, t0 = 0, time.perf_counter()
     while True:
-        _oracle_step(inp, oracle)
+        _oracle_step(smp, oracle, mode)
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": n * inp.total_nodes / dt, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-            "sample": f"{n} full verification steps of the same workload (fp64 numpy; BLAS threads = host cores)",
-            "seconds": dt}
+    return {"value": n * smp.total_nodes / dt, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{n} {what} (fp64 numpy; BLAS threads = host cores)", "seconds": dt}
 
 
 def run_reference(args):
@@ -438,22 +472,24 @@ def run_reference(args):
     from speculative_decoding_tree_parent_gb300 import workloads as W
     import oracle
 
-    inp = W.generate_index(CONFIG_INDEX)
+    idx = args.workload
+    mode = W.SPECS[idx].modes[0]
+    inp, what = oracle_sample(W.generate_index(idx))
     for _ in range(args.warmup):
-        _oracle_step(inp, oracle)
+        _oracle_step(inp, oracle, mode)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        _oracle_step(inp, oracle)
+        _oracle_step(inp, oracle, mode)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = inp.total_nodes * args.steps / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "parallelism": "host cores (rank 0 only)"},
+            "config": {"workload": WORKLOADS[idx], "parallelism": "host cores (rank 0 only)"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
-                             "sample": "whole verification steps of the same workload, one per timed step"},
+                             "sample": f"{what}, one per timed step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -466,6 +502,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=CONFIG_INDEX, choices=sorted(WORKLOADS),
+                    help="workload index (default: the Llama-3-8B-shaped single-sequence verify the headline "
+                         "is quoted on; the others are its parity cases, timed here for kernel scaling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -248,8 +248,9 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
  * spec_accept_commit — spec_accept, then spec_kv_commit of the paths it accepted, in one
  *   call: the results (accept_len, path, out_tokens, flags, the written pool rows,
  *   seq_len_out, device errors) are those of the two calls made back to back on
- *   `stream`. Greedy runs the commit inside the acceptance kernel (its last CTA, right
- *   after the walk); stochastic launches the commit kernel after its two kernels.
+ *   `stream`. Greedy with up to 4 sequences runs the commit inside the acceptance kernel
+ *   (its last CTA, right after the walk); more sequences, and stochastic acceptance, launch
+ *   the commit kernel after the acceptance kernels.
  *   Arguments: those of spec_accept (mode ... flags, ws, ws_bytes) and of spec_kv_commit
  *   (dtype ... d); path_cap, path and accept_len serve both. The same host errors, the
  *   same layouts; ws as for spec_accept.

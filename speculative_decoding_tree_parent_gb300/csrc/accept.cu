@@ -987,6 +987,17 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
                   cudaStream_t stream, const CommitArgs* commit) {
   CommitArgs ca = {};
   if (commit != nullptr) ca = *commit;
+  // Greedy commits inside the acceptance kernel only for a few sequences: its final CTA does
+  // them one after another. More sequences are committed by the commit kernel (one CTA per
+  // sequence, launched to start as the acceptance grid drains), like the stochastic path.
+  if (mode == SPEC_GREEDY && ca.k_tree != nullptr && batch > kCommitCta) {
+    const int e = launch_accept(mode, parent, tokens, tl, dl, uniforms, temperature, vocab, qo, batch, total_nodes,
+                                path_cap, accept_len, path, out_tokens, flags, ws, status, stream, nullptr);
+    if (e != SPEC_OK) return e;
+    return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
+                            ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
+                            ca.v_pool, batch, ca.hkv, ca.d, status, stream);
+  }
   const int chunks = accept_chunks(total_nodes, vocab);
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
   uint8_t* wb = static_cast<uint8_t*>(ws);

@@ -137,12 +137,12 @@ class DeviceBatch:
     def launches_per_step(self, mode=None, fused=True):
         """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the keys are
         split), then accept 1 (greedy) or 2 (stochastic) and commit 1 -- except that the fused
-        greedy call commits inside its acceptance kernel."""
+        greedy call of up to 4 sequences commits inside its acceptance kernel."""
         mode = mode or self.mode
         splits, _ = self.attn_plan()
         attn = 2 if splits > 1 else 1
         acc = 2 if mode == "stochastic" else 1
-        commit = 0 if (fused and mode != "stochastic") else 1
+        commit = 0 if (fused and mode != "stochastic" and self.B <= 4) else 1
         return 1 + attn + acc + commit
 
     def attn_plan(self):
