@@ -675,19 +675,39 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
     const float4* q4 = reinterpret_cast<const float4*>(rq);
     const int q0 = lo >> 2, q1 = hi >> 2;
     float4 a[kVecPerThread], d[kVecPerThread];
+    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
     for (int u = 0; u < kVecPerThread; ++u) {
       const int j = q0 + threadIdx.x + u * kAcceptThreads;
-      if (j < q1) {
-        a[u] = __ldcs(p4 + j);
-        d[u] = __ldcs(q4 + j);
-      }
+      a[u] = j < q1 ? __ldcs(p4 + j) : none;
+      d[u] = j < q1 ? __ldcs(q4 + j) : none;
     }
+    // every value is in registers: the max first, then one exponential per value (no
+    // running rescale, no divergent branch); values outside the chunk are -inf and add 0
+    float mp = -INFINITY, mq = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kVecPerThread; ++u) {
-      if (q0 + threadIdx.x + u * kAcceptThreads < q1) {
-        ep.add(a[u].x, invT); ep.add(a[u].y, invT); ep.add(a[u].z, invT); ep.add(a[u].w, invT);
-        eq.add(d[u].x, invT); eq.add(d[u].y, invT); eq.add(d[u].z, invT); eq.add(d[u].w, invT);
+      mp = fmaxf(mp, fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w)));
+      mq = fmaxf(mq, fmaxf(fmaxf(d[u].x, d[u].y), fmaxf(d[u].z, d[u].w)));
+    }
+    if (mp != -INFINITY) {
+      ep.m = mp;
+#pragma unroll
+      for (int u = 0; u < kVecPerThread; ++u) {
+        ep.kahan(expf((a[u].x - mp) * invT));
+        ep.kahan(expf((a[u].y - mp) * invT));
+        ep.kahan(expf((a[u].z - mp) * invT));
+        ep.kahan(expf((a[u].w - mp) * invT));
+      }
+    }
+    if (mq != -INFINITY) {
+      eq.m = mq;
+#pragma unroll
+      for (int u = 0; u < kVecPerThread; ++u) {
+        eq.kahan(expf((d[u].x - mq) * invT));
+        eq.kahan(expf((d[u].y - mq) * invT));
+        eq.kahan(expf((d[u].z - mq) * invT));
+        eq.kahan(expf((d[u].w - mq) * invT));
       }
     }
   } else {
