@@ -759,58 +759,160 @@ __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float 
 
 // ---------------------------------------------------------------- stochastic: walk
 
+// The CTA's slice [c_lo, c_hi) of the vocabulary (a multiple of 4 tokens long, so rows
+// with 16-byte alignment stage with float4 loads) is cut into kWalkWarps contiguous
+// segments, one per warp (a multiple of 32 tokens each); lane l of a warp takes the
+// segment's tokens l, l + 32, ... At a node's first pass p and q of the slice are staged
+// in shared memory as fp32 values (dynamic shared memory: kWalkStage of each at most,
+// i.e. vocabularies up to 8 x kWalkStage tokens; larger ones are evaluated from global
+// memory on every pass, with the same arithmetic). Sums: fp32 Kahan per lane, double-float
+// (an fp32 pair, error-free adds) across the lanes of a warp, fp64 across the warps of a
+// CTA and the CTAs of the cluster -- fp64 only there: its rate on this part is too low for
+// the inner loops.
+constexpr int kWalkWarps = kWalkThreads / 32;
+constexpr int kWalkStage = 24576;
+
 struct WalkShared {
   NodeStats st;                       // statistics of the node being visited
-  double part[2][kWalkThreads / 32];  // block reduction scratch
+  float part_hi[kWalkWarps], part_lo[kWalkWarps];  // this pass's segment sums (double-float)
+  double seg_pre[kWalkWarps];         // exclusive prefix of the segment sums (bonus draw)
   double cta_sum[2];                  // this CTA's pass total (double-buffered by pass parity)
-  double scan[kWalkThreads];          // per-thread sums for the bonus search
   unsigned kids[kMaxTreeNodes / 32];  // children bitmap of the current node
   int found;                          // bonus token found by this CTA (-1 = none)
   int found_flag;
 };
 
-// p(t) and q(t) in fp32 from the node statistics.
+struct F2 {
+  float hi, lo;
+};
+// Double-float sum. Its first step is exact (two-sum), so a + b and b + a give the same
+// bits: every lane of a butterfly ends with the same total.
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const float s = a.hi + b.hi;
+  const float v = s - a.hi;
+  float e = (a.hi - (s - v)) + (b.hi - v);
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return F2{hi, e - (hi - s)};
+}
+__device__ __forceinline__ F2 f2_warp_sum(F2 x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    x = f2_add(x, F2{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)});
+  return x;
+}
+
+// p(t) and q(t) of the visited node in fp32, from global memory (the staging source and
+// the path for vocabularies too large to stage).
 struct RowEval {
   const float* tl;
   const float* dl;
   float m_p, m_q, invT, inv_zp, inv_zq;
-  __device__ __forceinline__ float p(int t) const { return expf((__ldg(tl + t) - m_p) * invT) * inv_zp; }
-  __device__ __forceinline__ float q(int t) const { return expf((__ldg(dl + t) - m_q) * invT) * inv_zq; }
-  __device__ __forceinline__ float resid(int t, float c) const {
-    const float pt = p(t);
-    return c == 0.f ? pt : fmaxf(pt - c * q(t), 0.f);
+  __device__ __forceinline__ float pv(float x) const { return expf((x - m_p) * invT) * inv_zp; }
+  __device__ __forceinline__ float qv(float x) const { return expf((x - m_q) * invT) * inv_zq; }
+  __device__ __forceinline__ float p(int t) const { return pv(__ldg(tl + t)); }
+  __device__ __forceinline__ float q(int t) const { return qv(__ldg(dl + t)); }
+};
+
+struct WalkSlice {
+  int c_lo, n, seg;  // slice start, its length, the segment length
+  float* sp;         // staged p and q (nullptr: not staged for this vocabulary)
+  float* sq;
+  __device__ __forceinline__ float p(const RowEval& ev, int i) const { return sp ? sp[i] : ev.p(c_lo + i); }
+  __device__ __forceinline__ float q(const RowEval& ev, int i) const { return sq ? sq[i] : ev.q(c_lo + i); }
+  __device__ __forceinline__ float resid(const RowEval& ev, int i, float c) const {
+    const float pt = p(ev, i);
+    return c == 0.f ? pt : fmaxf(pt - c * q(ev, i), 0.f);
   }
 };
 
-// This thread's contiguous sub-range of the CTA's slice of the vocabulary.
-__device__ __forceinline__ void walk_range(int vocab, int rank, int& lo, int& hi) {
-  const int per_cta = (vocab + kWalkCluster - 1) / kWalkCluster;
-  const int c_lo = rank * per_cta;
-  const int c_hi = min(vocab, c_lo + per_cta);
-  const int n = max(0, c_hi - c_lo);
-  const int per_thr = (n + kWalkThreads - 1) / kWalkThreads;
-  lo = min(c_hi, c_lo + (int)threadIdx.x * per_thr);
-  hi = min(c_hi, lo + per_thr);
+__device__ __forceinline__ WalkSlice walk_slice(int vocab, int rank, float* smem) {
+  const int per_cta = ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
+  WalkSlice s;
+  s.c_lo = rank * per_cta;
+  s.n = max(0, min(vocab, s.c_lo + per_cta) - s.c_lo);
+  s.seg = (((s.n + kWalkWarps - 1) / kWalkWarps) + 31) & ~31;
+  const bool staged = per_cta <= kWalkStage;
+  s.sp = staged ? smem : nullptr;
+  s.sq = staged ? smem + per_cta : nullptr;
+  return s;
 }
 
-// Sum over the whole vocabulary (all CTAs of the cluster) of the residual with
-// coefficient c; identical bitwise in every CTA.
-__device__ double cluster_resid_sum(cg::cluster_group& cl, WalkShared& sh, const RowEval& ev, int vocab,
-                                    float c, int parity) {
-  int lo, hi;
-  walk_range(vocab, (int)cl.block_rank(), lo, hi);
+// p and q of the slice into shared memory (coalesced; float4 when the rows allow it).
+__device__ void walk_stage(const WalkSlice& sl, const RowEval& ev, bool vec) {
+  if (vec) {
+    const float4* t4 = reinterpret_cast<const float4*>(ev.tl + sl.c_lo);
+    const float4* d4 = reinterpret_cast<const float4*>(ev.dl + sl.c_lo);
+    float4* p4 = reinterpret_cast<float4*>(sl.sp);
+    float4* q4 = reinterpret_cast<float4*>(sl.sq);
+    const int n4 = sl.n >> 2;  // (n is a multiple of 4 when the vocabulary is)
+    constexpr int kU = 4;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += kU * kWalkThreads) {
+      float4 a[kU], d[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kWalkThreads;
+        if (i < n4) {
+          a[u] = __ldg(t4 + i);
+          d[u] = __ldg(d4 + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kWalkThreads;
+        if (i < n4) {
+          p4[i] = make_float4(ev.pv(a[u].x), ev.pv(a[u].y), ev.pv(a[u].z), ev.pv(a[u].w));
+          q4[i] = make_float4(ev.qv(d[u].x), ev.qv(d[u].y), ev.qv(d[u].z), ev.qv(d[u].w));
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < sl.n; i += kWalkThreads) {
+      sl.sp[i] = ev.p(sl.c_lo + i);
+      sl.sq[i] = ev.q(sl.c_lo + i);
+    }
+  }
+  __syncthreads();
+}
+
+// One pass: sum over the whole vocabulary (all CTAs of the cluster) of the residual with
+// coefficient c, identical bitwise in every CTA. Leaves the segment sums in
+// sh.part_hi / part_lo and, when `prefix`, their exclusive prefix in sh.seg_pre; *cta_pre
+// receives the sum over the CTAs ranked before this one.
+__device__ double walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& sl, const RowEval& ev,
+                            float c, int parity, bool prefix, double* cta_pre) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
   float s = 0.f, comp = 0.f;
-  for (int t = lo; t < hi; ++t) {
-    const float y = ev.resid(t, c) - comp;
+  for (int i = s_lo + lane; i < s_hi; i += 32) {
+    const float y = sl.resid(ev, i, c) - comp;
     const float z = s + y;
     comp = (z - s) - y;
     s = z;
   }
-  const double tot = block_sum((double)s, sh.part[parity]);
-  if (threadIdx.x == 0) sh.cta_sum[parity] = tot;
+  const F2 w = f2_warp_sum(F2{s, -comp});
+  if (lane == 0) {
+    sh.part_hi[warp] = w.hi;
+    sh.part_lo[warp] = w.lo;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int k = 0; k < kWalkWarps; ++k) {
+      if (prefix) sh.seg_pre[k] = tot;
+      tot += (double)sh.part_hi[k] + (double)sh.part_lo[k];
+    }
+    sh.cta_sum[parity] = tot;
+  }
   cl.sync();
-  double all = 0.0;
-  for (int r = 0; r < kWalkCluster; ++r) all += *cl.map_shared_rank(&sh.cta_sum[parity], r);
+  const int rank = (int)cl.block_rank();
+  double all = 0.0, pre = 0.0;
+  for (int r = 0; r < kWalkCluster; ++r) {
+    const double x = *cl.map_shared_rank(&sh.cta_sum[parity], r);
+    if (r < rank) pre += x;
+    all += x;
+  }
+  if (cta_pre != nullptr) *cta_pre = pre;
   return all;
 }
 
@@ -820,12 +922,14 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
                        const float* __restrict__ uniforms, float temperature, int vocab,
                        const int32_t* __restrict__ qo, int path_cap, const StatPartial* partials,
                        int chunks, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
-                       int32_t* status) {
+                       int32_t* status, bool vec) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ WalkShared sh;
+  extern __shared__ __align__(16) float walk_smem[];
   pdl_wait();  // the statistics kernel's results
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int base = __ldg(qo + b);
   const int n = __ldg(qo + b + 1) - base;
   const float invT = 1.0f / temperature;
@@ -837,6 +941,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     if (writer) report(status, SPEC_ERR_CAPACITY);
     return;
   }
+  const WalkSlice sl = walk_slice(vocab, rank, walk_smem);
   if (writer) prow[0] = 0;
   int v = 0, L = 0, flag = 0, bonus = 0;
   int parity = 0;
@@ -849,8 +954,13 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     for (int w = threadIdx.x; w < kMaxTreeNodes / 32; w += blockDim.x) sh.kids[w] = 0u;
     __syncthreads();
     const NodeStats st = sh.st;
-    RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
-               (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
+    const RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
+                     (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
+    bool staged = false;  // p and q of v's slice in shared memory (done before v's first pass)
+    auto stage = [&]() {
+      if (!staged && sl.sp != nullptr) walk_stage(sl, ev, vec);
+      staged = true;
+    };
     for (int c = v + 1 + threadIdx.x; c < n; c += blockDim.x)
       if (__ldg(parent + base + c) == v) atomicOr(&sh.kids[c >> 5], 1u << (c & 31));
     __syncthreads();
@@ -882,8 +992,9 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
           accepted = c;
           break;
         }
+        stage();
         const double cn = cc + ss;
-        const double sn = cluster_resid_sum(cl, sh, ev, vocab, (float)cn, parity);
+        const double sn = walk_pass(cl, sh, sl, ev, (float)cn, parity, false, nullptr);
         parity ^= 1;
         if (sn > 0.0) {
           cc = cn;
@@ -906,66 +1017,61 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
         continue;
       }
     }
-    // bonus: inverse-CDF draw from r = max(p - cc q, 0) / ss with u_bonus of v
+    // bonus: inverse-CDF draw from r = max(p - cc q, 0) / ss with u_bonus of v: the smallest
+    // token whose cumulative residual exceeds u * total. The segment sums locate the
+    // segment holding the threshold; its warp scans it 32 tokens at a time.
     {
-      int lo, hi;
-      walk_range(vocab, rank, lo, hi);
+      stage();
       const float cf = (float)cc;
-      float s = 0.f, comp = 0.f;
-      for (int t = lo; t < hi; ++t) {
-        const float y = ev.resid(t, cf) - comp;
-        const float z = s + y;
-        comp = (z - s) - y;
-        s = z;
-      }
-      sh.scan[threadIdx.x] = (double)s;
-      __syncthreads();
-      if (threadIdx.x == 0) {  // exclusive scan over threads (fixed order)
-        double acc = 0.0;
-        for (int k = 0; k < kWalkThreads; ++k) {
-          const double x = sh.scan[k];
-          sh.scan[k] = acc;
-          acc += x;
-        }
-        sh.cta_sum[parity] = acc;
+      double cta_pre = 0.0;
+      const double total = walk_pass(cl, sh, sl, ev, cf, parity, true, &cta_pre);
+      parity ^= 1;
+      if (threadIdx.x == 0) {
         sh.found = -1;
         sh.found_flag = 0;
       }
       __syncthreads();
-      const double my_pre_local = sh.scan[threadIdx.x];
-      const double my_next_local = threadIdx.x + 1 < kWalkThreads ? sh.scan[threadIdx.x + 1] : sh.cta_sum[parity];
-      cl.sync();
-      double cta_pre = 0.0, total = 0.0;
-      for (int r = 0; r < kWalkCluster; ++r) {
-        const double x = *cl.map_shared_rank(&sh.cta_sum[parity], r);
-        if (r < rank) cta_pre += x;
-        total += x;
-      }
       const double thr = (double)__ldg(uniforms + 2 * (size_t)(base + v) + 1) * total;
-      const double pre = cta_pre + my_pre_local;
-      const double nxt = cta_pre + my_next_local;
-      if (pre <= thr && thr < nxt && hi > lo) {
-        double acc = pre;
+      const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
+      const double seg_start = cta_pre + sh.seg_pre[warp];
+      const double seg_sum = (double)sh.part_hi[warp] + (double)sh.part_lo[warp];
+      if (s_hi > s_lo && seg_start <= thr && thr < seg_start + seg_sum) {  // (warp-uniform)
+        const double loc = thr - seg_start;
+        F2 carry{0.f, 0.f};
         int tok = -1, last_pos = -1, fl = 0;
-        for (int t = lo; t < hi; ++t) {
-          const float rv = ev.resid(t, cf);
-          if (rv > 0.f) last_pos = t;
-          const double before = acc;
-          acc += (double)rv;
-          if (acc > thr) {
-            tok = t;
-            if (fabs(acc - thr) <= kBonusEps * total || fabs(before - thr) <= kBonusEps * total) fl = 2;
-            break;
+        for (int i0 = s_lo; i0 < s_hi && tok < 0; i0 += 32) {
+          const int i = i0 + lane;
+          const float rv = i < s_hi ? sl.resid(ev, i, cf) : 0.f;
+          F2 inc{rv, 0.f};  // inclusive scan of the round (double-float), then the carry
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const F2 y{__shfl_up_sync(0xffffffffu, inc.hi, o), __shfl_up_sync(0xffffffffu, inc.lo, o)};
+            if (lane >= o) inc = f2_add(y, inc);
           }
+          const F2 cum = f2_add(carry, inc);
+          const double after = (double)cum.hi + (double)cum.lo;
+          const double before = after - (double)rv;
+          const unsigned hit = __ballot_sync(0xffffffffu, i < s_hi && after > loc);
+          const unsigned pos = __ballot_sync(0xffffffffu, i < s_hi && rv > 0.f);
+          if (pos) last_pos = i0 + 31 - __clz(pos);
+          if (hit) {
+            const int l = __ffs(hit) - 1;
+            tok = sl.c_lo + i0 + l;
+            const double a_l = __shfl_sync(0xffffffffu, after, l);
+            const double b_l = __shfl_sync(0xffffffffu, before, l);
+            if (fabs(a_l - loc) <= kBonusEps * total || fabs(b_l - loc) <= kBonusEps * total) fl = 2;
+          }
+          carry = F2{__shfl_sync(0xffffffffu, cum.hi, 31), __shfl_sync(0xffffffffu, cum.lo, 31)};
         }
-        if (tok < 0) {  // rounding put the crossing just past this range's last mass
-          tok = last_pos >= 0 ? last_pos : lo;
+        if (tok < 0) {  // rounding put the crossing just past this segment's last mass
+          tok = sl.c_lo + (last_pos >= 0 ? last_pos : s_lo);
           fl = 2;
         }
-        sh.found = tok;
-        sh.found_flag = fl;
+        if (lane == 0) {
+          sh.found = tok;
+          sh.found_flag = fl;
+        }
       }
-      parity ^= 1;
       cl.sync();
       if (rank == 0 && threadIdx.x == 0) {
         int tok = -1;
@@ -976,6 +1082,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
             flag |= *cl.map_shared_rank(&sh.found_flag, r);
           }
         }
+        if (tok < 0) flag |= 2;  // (no segment held the threshold: an fp64 rounding gap, flagged)
         bonus = tok < 0 ? 0 : tok;
       }
       cl.sync();  // keep every CTA's shared memory alive until rank 0 has read it
@@ -1059,9 +1166,19 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   else
     accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), 0, stream, parent, tokens, tl,
-                 dl, uniforms, temperature, vocab, qo, path_cap, (const StatPartial*)part, chunks, accept_len, path,
-                 out_tokens, flags, status) != cudaSuccess)
+  // dynamic shared memory of the walk: each CTA's slice of p and q (when it fits)
+  const int per_cta = ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
+  const size_t walk_smem = per_cta <= kWalkStage ? 2 * sizeof(float) * (size_t)per_cta : 0;
+  static bool walk_attr = false;
+  if (!walk_attr) {
+    if (cudaFuncSetAttribute(accept_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(2 * sizeof(float) * kWalkStage)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    walk_attr = true;
+  }
+  if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), walk_smem, stream, parent,
+                 tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, (const StatPartial*)part, chunks,
+                 accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (ca.k_tree == nullptr) return SPEC_OK;
