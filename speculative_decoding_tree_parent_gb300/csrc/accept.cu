@@ -765,18 +765,18 @@ __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float 
 // segment's tokens l, l + 32, ... At a node's first pass p and q of the slice are staged
 // in shared memory as fp32 values (dynamic shared memory: kWalkStage of each at most,
 // i.e. vocabularies up to 8 x kWalkStage tokens; larger ones are evaluated from global
-// memory on every pass, with the same arithmetic). Sums: fp32 Kahan per lane, double-float
-// (an fp32 pair, error-free adds) across the lanes of a warp, fp64 across the warps of a
-// CTA and the CTAs of the cluster -- fp64 only there: its rate on this part is too low for
-// the inner loops.
+// memory on every pass, with the same arithmetic). Sums: fp32 Kahan per lane, then
+// double-float (an fp32 pair, error-free adds, about 48 significant bits) across lanes,
+// warps and the CTAs of the cluster. fp64 is kept to a few operations per decision: on
+// this part a dependent fp64 operation costs hundreds of cycles.
 constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kWalkStage = 24576;
 
 struct WalkShared {
   NodeStats st;                       // statistics of the node being visited
   float part_hi[kWalkWarps], part_lo[kWalkWarps];  // this pass's segment sums (double-float)
-  double seg_pre[kWalkWarps];         // exclusive prefix of the segment sums (bonus draw)
-  double cta_sum[2];                  // this CTA's pass total (double-buffered by pass parity)
+  float pre_hi[kWalkWarps], pre_lo[kWalkWarps];    // their exclusive prefix (bonus draw)
+  float cta_hi[2], cta_lo[2];         // this CTA's pass total (double-buffered by pass parity)
   unsigned kids[kMaxTreeNodes / 32];  // children bitmap of the current node
   int found;                          // bonus token found by this CTA (-1 = none)
   int found_flag;
@@ -876,11 +876,11 @@ __device__ void walk_stage(const WalkSlice& sl, const RowEval& ev, bool vec) {
 }
 
 // One pass: sum over the whole vocabulary (all CTAs of the cluster) of the residual with
-// coefficient c, identical bitwise in every CTA. Leaves the segment sums in
-// sh.part_hi / part_lo and, when `prefix`, their exclusive prefix in sh.seg_pre; *cta_pre
-// receives the sum over the CTAs ranked before this one.
-__device__ double walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& sl, const RowEval& ev,
-                            float c, int parity, bool prefix, double* cta_pre) {
+// coefficient c, identical bitwise in every CTA (double-float). Leaves the segment sums in
+// sh.part_hi / part_lo and, when `prefix`, their exclusive prefix in sh.pre_hi / pre_lo;
+// *cta_pre receives the sum over the CTAs ranked before this one.
+__device__ F2 walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& sl, const RowEval& ev, float c,
+                        int parity, bool prefix, F2* cta_pre) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
   float s = 0.f, comp = 0.f;
@@ -897,24 +897,36 @@ __device__ double walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSli
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double tot = 0.0;
+    F2 tot{0.f, 0.f};
     for (int k = 0; k < kWalkWarps; ++k) {
-      if (prefix) sh.seg_pre[k] = tot;
-      tot += (double)sh.part_hi[k] + (double)sh.part_lo[k];
+      if (prefix) {
+        sh.pre_hi[k] = tot.hi;
+        sh.pre_lo[k] = tot.lo;
+      }
+      tot = f2_add(tot, F2{sh.part_hi[k], sh.part_lo[k]});
     }
-    sh.cta_sum[parity] = tot;
+    sh.cta_hi[parity] = tot.hi;
+    sh.cta_lo[parity] = tot.lo;
   }
   cl.sync();
   const int rank = (int)cl.block_rank();
-  double all = 0.0, pre = 0.0;
+  F2 all{0.f, 0.f}, pre{0.f, 0.f};
   for (int r = 0; r < kWalkCluster; ++r) {
-    const double x = *cl.map_shared_rank(&sh.cta_sum[parity], r);
-    if (r < rank) pre += x;
-    all += x;
+    const F2 x{*cl.map_shared_rank(&sh.cta_hi[parity], r), *cl.map_shared_rank(&sh.cta_lo[parity], r)};
+    if (r == rank) pre = all;
+    all = f2_add(all, x);
   }
   if (cta_pre != nullptr) *cta_pre = pre;
   return all;
 }
+
+__device__ __forceinline__ double f2_to_d(F2 x) { return (double)x.hi + (double)x.lo; }
+__device__ __forceinline__ F2 d_to_f2(double x) {
+  const float hi = (float)x;
+  return F2{hi, (float)(x - (double)hi)};
+}
+// a > b for normalised double-float values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 
 __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThreads)
     accept_walk_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
@@ -933,7 +945,6 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   const int base = __ldg(qo + b);
   const int n = __ldg(qo + b + 1) - base;
   const float invT = 1.0f / temperature;
-  const double invTd = 1.0 / (double)temperature;
   int32_t* prow = path + (size_t)b * path_cap;
   int32_t* trow = out_tokens + (size_t)b * path_cap;
   const bool writer = rank == 0 && threadIdx.x == 0;
@@ -976,17 +987,19 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
           if (writer) report(status, SPEC_ERR_INDEX);
           continue;
         }
-        const double px = exp(((double)__ldg(ev.tl + x) - (double)st.m_p) * invTd) / st.z_p;
-        const double qx = exp(((double)__ldg(ev.dl + x) - (double)st.m_q) * invTd) / st.z_q;
+        // p(x), q(x): the fp32 values the passes use; the test u < max(p - cc q, 0) / (ss q)
+        // as u ss q < max(p - cc q, 0) in fp64, with no exponential or division there
+        const double px = (double)ev.p(x), qx = (double)ev.q(x);
         const double u = (double)__ldg(uniforms + 2 * (size_t)(base + c));
-        const double rx = fmax(px - cc * qx, 0.0) / ss;
+        const double num = fmax(fma(-cc, qx, px), 0.0);
         bool ok;
         if (qx > 0.0) {
-          const double ratio = rx / qx;
-          if (fabs(u - ratio) <= kTieEps) flag |= 1;
-          ok = u < ratio;
+          const double den = ss * qx;
+          const double lhs = u * den;
+          if (fabs(lhs - num) <= kTieEps * den) flag |= 1;
+          ok = lhs < num;
         } else {
-          ok = rx > 0.0;
+          ok = num > 0.0;
         }
         if (ok) {
           accepted = c;
@@ -994,7 +1007,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
         }
         stage();
         const double cn = cc + ss;
-        const double sn = walk_pass(cl, sh, sl, ev, (float)cn, parity, false, nullptr);
+        const double sn = f2_to_d(walk_pass(cl, sh, sl, ev, (float)cn, parity, false, nullptr));
         parity ^= 1;
         if (sn > 0.0) {
           cc = cn;
@@ -1023,20 +1036,23 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     {
       stage();
       const float cf = (float)cc;
-      double cta_pre = 0.0;
-      const double total = walk_pass(cl, sh, sl, ev, cf, parity, true, &cta_pre);
+      F2 cta_pre{0.f, 0.f};
+      const F2 total2 = walk_pass(cl, sh, sl, ev, cf, parity, true, &cta_pre);
+      const double total = f2_to_d(total2);
       parity ^= 1;
       if (threadIdx.x == 0) {
         sh.found = -1;
         sh.found_flag = 0;
       }
       __syncthreads();
-      const double thr = (double)__ldg(uniforms + 2 * (size_t)(base + v) + 1) * total;
+      // threshold and segment bounds in double-float: the segment intervals tile the line
+      const F2 thr = d_to_f2((double)__ldg(uniforms + 2 * (size_t)(base + v) + 1) * total);
       const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
-      const double seg_start = cta_pre + sh.seg_pre[warp];
-      const double seg_sum = (double)sh.part_hi[warp] + (double)sh.part_lo[warp];
-      if (s_hi > s_lo && seg_start <= thr && thr < seg_start + seg_sum) {  // (warp-uniform)
-        const double loc = thr - seg_start;
+      const F2 seg_start = f2_add(cta_pre, F2{sh.pre_hi[warp], sh.pre_lo[warp]});
+      const F2 seg_end = f2_add(seg_start, F2{sh.part_hi[warp], sh.part_lo[warp]});
+      if (s_hi > s_lo && !f2_gt(seg_start, thr) && f2_gt(seg_end, thr)) {  // (warp-uniform)
+        const F2 loc = f2_add(thr, F2{-seg_start.hi, -seg_start.lo});
+        const float band = (float)(kBonusEps * total);
         F2 carry{0.f, 0.f};
         int tok = -1, last_pos = -1, fl = 0;
         for (int i0 = s_lo; i0 < s_hi && tok < 0; i0 += 32) {
@@ -1049,17 +1065,18 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
             if (lane >= o) inc = f2_add(y, inc);
           }
           const F2 cum = f2_add(carry, inc);
-          const double after = (double)cum.hi + (double)cum.lo;
-          const double before = after - (double)rv;
-          const unsigned hit = __ballot_sync(0xffffffffu, i < s_hi && after > loc);
+          const unsigned hit = __ballot_sync(0xffffffffu, i < s_hi && f2_gt(cum, loc));
           const unsigned pos = __ballot_sync(0xffffffffu, i < s_hi && rv > 0.f);
           if (pos) last_pos = i0 + 31 - __clz(pos);
           if (hit) {
             const int l = __ffs(hit) - 1;
             tok = sl.c_lo + i0 + l;
-            const double a_l = __shfl_sync(0xffffffffu, after, l);
-            const double b_l = __shfl_sync(0xffffffffu, before, l);
-            if (fabs(a_l - loc) <= kBonusEps * total || fabs(b_l - loc) <= kBonusEps * total) fl = 2;
+            // distances of the crossing token's two CDF edges from the threshold
+            const F2 da = f2_add(cum, F2{-loc.hi, -loc.lo});
+            const F2 db = f2_add(da, F2{-rv, 0.f});
+            const float d_after = __shfl_sync(0xffffffffu, da.hi + da.lo, l);
+            const float d_before = __shfl_sync(0xffffffffu, db.hi + db.lo, l);
+            if (fabsf(d_after) <= band || fabsf(d_before) <= band) fl = 2;
           }
           carry = F2{__shfl_sync(0xffffffffu, cum.hi, 31), __shfl_sync(0xffffffffu, cum.lo, 31)};
         }
