@@ -633,6 +633,34 @@ struct OnlineExp {
   }
 };
 
+struct F2 {
+  float hi, lo;
+};
+// Double-float sum. Its first step is exact (two-sum), so a + b and b + a give the same
+// bits: every lane of a butterfly ends with the same total.
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const float s = a.hi + b.hi;
+  const float v = s - a.hi;
+  float e = (a.hi - (s - v)) + (b.hi - v);
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return F2{hi, e - (hi - s)};
+}
+__device__ __forceinline__ F2 f2_warp_sum(F2 x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    x = f2_add(x, F2{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)});
+  return x;
+}
+
+__device__ __forceinline__ double f2_to_d(F2 x) { return (double)x.hi + (double)x.lo; }
+__device__ __forceinline__ F2 d_to_f2(double x) {
+  const float hi = (float)x;
+  return F2{hi, (float)(x - (double)hi)};
+}
+// a > b for normalised double-float values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -642,19 +670,6 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   __syncthreads();
   float r = red[0];
   for (int w = 1; w < nw; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-
-// Block-wide fp64 sum; every thread gets the same value (summed in a fixed order).
-__device__ __forceinline__ double block_sum(double v, double* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  double r = red[0];
-  for (int w = 1; w < nw; ++w) r += red[w];
   return r;
 }
 
@@ -717,13 +732,33 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
     }
   }
   __shared__ float redf[kAcceptThreads / 32];
-  __shared__ double redd[kAcceptThreads / 32];
+  __shared__ float red_hi[2][kAcceptThreads / 32], red_lo[2][kAcceptThreads / 32];
   const float Mp = block_max(ep.m, redf);
   const float Mq = block_max(eq.m, redf);
-  const double Sp = block_sum(ep.m == -INFINITY ? 0.0 : (double)ep.s * (double)expf((ep.m - Mp) * invT), redd);
-  const double Sq = block_sum(eq.m == -INFINITY ? 0.0 : (double)eq.s * (double)expf((eq.m - Mq) * invT), redd);
+  // each thread's compensated sum rescaled to the block max as a double-float, then summed
+  // across the block in double-float (fp64 only for the stored result)
+  auto rescaled = [&](const OnlineExp& e, float M) {
+    if (e.m == -INFINITY) return F2{0.f, 0.f};
+    const float f = expf((e.m - M) * invT);
+    const float hi = e.s * f;
+    return F2{hi, fmaf(e.s, f, -hi) - e.comp * f};
+  };
+  const F2 sp = f2_warp_sum(rescaled(ep, Mp)), sq = f2_warp_sum(rescaled(eq, Mq));
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red_hi[0][warp] = sp.hi;
+    red_lo[0][warp] = sp.lo;
+    red_hi[1][warp] = sq.hi;
+    red_lo[1][warp] = sq.lo;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, Sp, Sq};
+    F2 tp{0.f, 0.f}, tq{0.f, 0.f};
+    for (int w = 0; w < kAcceptThreads / 32; ++w) {
+      tp = f2_add(tp, F2{red_hi[0][w], red_lo[0][w]});
+      tq = f2_add(tq, F2{red_hi[1][w], red_lo[1][w]});
+    }
+    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, f2_to_d(tp), f2_to_d(tq)};
     pdl_trigger();
   }
 }
@@ -781,26 +816,6 @@ struct WalkShared {
   int found;                          // bonus token found by this CTA (-1 = none)
   int found_flag;
 };
-
-struct F2 {
-  float hi, lo;
-};
-// Double-float sum. Its first step is exact (two-sum), so a + b and b + a give the same
-// bits: every lane of a butterfly ends with the same total.
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
-  const float s = a.hi + b.hi;
-  const float v = s - a.hi;
-  float e = (a.hi - (s - v)) + (b.hi - v);
-  e += a.lo + b.lo;
-  const float hi = s + e;
-  return F2{hi, e - (hi - s)};
-}
-__device__ __forceinline__ F2 f2_warp_sum(F2 x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    x = f2_add(x, F2{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)});
-  return x;
-}
 
 // p(t) and q(t) of the visited node in fp32, from global memory (the staging source and
 // the path for vocabularies too large to stage).
@@ -919,14 +934,6 @@ __device__ F2 walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& 
   if (cta_pre != nullptr) *cta_pre = pre;
   return all;
 }
-
-__device__ __forceinline__ double f2_to_d(F2 x) { return (double)x.hi + (double)x.lo; }
-__device__ __forceinline__ F2 d_to_f2(double x) {
-  const float hi = (float)x;
-  return F2{hi, (float)(x - (double)hi)};
-}
-// a > b for normalised double-float values (|lo| at most half an ulp of hi).
-__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 
 __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThreads)
     accept_walk_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
