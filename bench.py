@@ -198,13 +198,14 @@ KERNEL_SOURCES = {
 }
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload
+    and the kernel source is unchanged since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(kernel)
-    if not rec or rec.get("source_digest") != _kernel_digest(KERNEL_SOURCES[kernel]):
+    if not rec or rec.get("workload") != workload or rec.get("source_digest") != _kernel_digest(KERNEL_SOURCES[kernel]):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -378,7 +379,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": acc_gbs, "peak": hbm, "unit": "GB/s", "frac": acc_gbs / hbm}
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_kind} (burst)"
-    roof["traffic"] = recorded_traffic(dom)
+    roof["traffic"] = recorded_traffic(dom, idx)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
