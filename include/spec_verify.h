@@ -254,6 +254,16 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
  *   Arguments: those of spec_accept (mode ... flags, ws, ws_bytes) and of spec_kv_commit
  *   (dtype ... d); path_cap, path and accept_len serve both. The same host errors, the
  *   same layouts; ws as for spec_accept.
+ *   Next-step tokens on the device ("Accelerating Sonar", MTP-schedule section: a kernel
+ *   places the next token after the shift, with no CPU-GPU sync):
+ *   token_buf  int32 [batch][token_stride] (in/out, nullable)  each sequence's tokens by
+ *              position, the root (the last accepted token) at prefix_len[b]. With every
+ *              commit of sequence b the call also writes out_tokens[b][0 .. L] (the L
+ *              accepted tokens, then the bonus token, the next step's root) to
+ *              token_buf[b][P + 1 .. P + L + 1], P = prefix_len[b]; nothing else of the row
+ *              changes. A row without room (P + L + 1 >= token_stride) is a device error
+ *              SPEC_ERR_CAPACITY, and that sequence is left unwritten (K/V and tokens).
+ *   token_stride  row length of token_buf (>= 1 when token_buf is given).
  */
 int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tokens,
                        const float* target_logits, const float* draft_logits, const float* uniforms,
@@ -262,8 +272,9 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
                        int32_t* path, int32_t* out_tokens, uint8_t* flags, int dtype,
                        const void* k_tree, const void* v_tree, const int32_t* page_table,
                        int max_pages, int num_pages, int page_size, const int32_t* prefix_len,
-                       int32_t* seq_len_out, void* k_pool, void* v_pool, int hkv, int d, void* ws,
-                       size_t ws_bytes, int32_t* dev_status, void* stream);
+                       int32_t* seq_len_out, void* k_pool, void* v_pool, int hkv, int d,
+                       int32_t* token_buf, int token_stride, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, void* stream);
 
 /*
  * spec_accept_noalloc — spec_accept for callers that cannot allocate device memory.

@@ -27,7 +27,7 @@ Modules and the passages they follow (page title, then section):
   commit      "EAGLE-2 deep dive", architecture section (verification must not
               contaminate the target KV cache); "Accelerating Sonar", draft-target and
               MTP-schedule sections (KV entries filled for accepted tokens; a kernel
-              inserts the next token after the shift, with no CPU sync).
+              inserts the next token after the shift, with no CPU sync: token_insert).
 
 Readings where the pages are silent are stated in each function's docstring.
 Every function here is pinned by `tests/test_oracle_*.py` against brute force,
@@ -37,7 +37,7 @@ closed forms, textbook routines or hand-worked examples in `tests/golden/`.
 from .tree_mask import ancestor_mask, ancestor_mask_batch, pack_mask_words
 from .attention import tree_verify_attention, tree_verify_attention_rows, gather_prefix
 from .accept import greedy_accept, stochastic_accept, AcceptResult
-from .commit import kv_commit
+from .commit import kv_commit, token_insert
 
 __all__ = [
     "ancestor_mask",
@@ -50,4 +50,5 @@ __all__ = [
     "stochastic_accept",
     "AcceptResult",
     "kv_commit",
+    "token_insert",
 ]

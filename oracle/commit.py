@@ -40,3 +40,22 @@ def kv_commit(k_pool, v_pool, page_table, prefix_len, k_tree, v_tree, path, acce
             vp[page, :, slot % page_size, :] = v_tree[a + node]
         seq_len[b] = P + L + 1
     return kp, vp, seq_len
+
+
+def token_insert(token_buf, prefix_len, out_tokens, accept_len):
+    """The next step's tokens on the device ("Accelerating Sonar", MTP-schedule section: a
+    kernel places the next token after the shift, with no CPU-GPU sync).
+
+    Reading (the page gives the idea, not the layout): row b of token_buf holds sequence b's
+    tokens by position, its root (the last accepted token) at P_b; the step appends its L_b
+    accepted tokens and then the bonus token, in that order, at positions P_b + 1 ..
+    P_b + L_b + 1 -- the bonus is the root of the next step, at the new sequence length.
+    Returns the new buffer; the input is not modified. A row too short raises."""
+    buf = np.array(token_buf, copy=True)
+    for b in range(buf.shape[0]):
+        P, L = int(prefix_len[b]), int(accept_len[b])
+        if P + L + 1 >= buf.shape[1]:
+            raise ValueError("token row too short for the step's tokens")
+        for i in range(L + 1):
+            buf[b, P + 1 + i] = out_tokens[b][i]
+    return buf

@@ -39,7 +39,7 @@ _SIGS = {
     "spec_accept": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P, _P]),
     "spec_kv_commit": (_I, [_I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "spec_accept_commit": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P,
-                                _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _Z, _P, _P]),
+                                _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _I, _P, _Z, _P, _P]),
     "spec_accept_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -170,17 +170,21 @@ def spec_kv_commit(k_tree, v_tree, path, accept_len, qo_indptr, page_table, pref
 
 def spec_accept_commit(mode, parent, draft_tokens, target_logits, qo_indptr, max_nodes, accept_len, path,
                        out_tokens, ws, k_tree, v_tree, page_table, prefix_len, k_pool, v_pool, seq_len_out=None,
-                       draft_logits=None, uniforms=None, temperature=1.0, flags=None, dev_status=None, stream=None):
-    """spec_accept then spec_kv_commit of the accepted paths, as one call."""
+                       draft_logits=None, uniforms=None, temperature=1.0, flags=None, dev_status=None, stream=None,
+                       token_buf=None):
+    """spec_accept then spec_kv_commit of the accepted paths, as one call; with `token_buf`
+    ([batch][stride] int32) also the step's tokens written after each sequence's root."""
     T, V = target_logits.shape
     _, hkv, d = k_tree.shape
     num_pages, _, ps, _ = k_pool.shape
+    stride = token_buf.shape[1] if token_buf is not None else 0
     st = load().spec_accept_commit(
         int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
         float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
         _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _dtype(k_tree), _ptr(k_tree), _ptr(v_tree),
         _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
-        _ptr(v_pool), hkv, d, _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+        _ptr(v_pool), hkv, d, _ptr(token_buf), stride, _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _stream(stream))
     return _check(st, "spec_accept_commit")
 
 

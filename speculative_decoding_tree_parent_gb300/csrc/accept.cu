@@ -270,6 +270,8 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
   int code = 0;
   if (L < 0 || L >= path_cap || L >= n || P < 0) {
     code = SPEC_ERR_INDEX;
+  } else if (ca.ins.token_buf != nullptr && P + L + 1 >= ca.ins.token_stride) {
+    code = SPEC_ERR_CAPACITY;  // the token row has no room for L + 1 tokens after P
   } else {
     for (int i = first + rank; i <= L; i += size) {
       const int node = node_at(i);
@@ -330,6 +332,9 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
     *reinterpret_cast<uint4*>(ca.k_pool + dst) = kv;
     *reinterpret_cast<uint4*>(ca.v_pool + dst) = vv;
   }
+  if (ca.ins.token_buf != nullptr)  // the accepted tokens and the bonus after the root
+    for (int i = rank; i <= L; i += size)
+      ca.ins.token_buf[(size_t)b * ca.ins.token_stride + P + 1 + i] = ca.ins.out_tokens[(size_t)b * path_cap + i];
   if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
 }
 
@@ -366,6 +371,7 @@ __device__ void root_stage(const CommitArgs& ca, int base, uint4* buf) {
 __device__ int root_write(const CommitArgs& ca, int b, int P, int n, int path_cap, const uint4* buf) {
   const int lane = threadIdx.x & 31;
   if (P < 0 || n < 1 || path_cap < 1) return -1;
+  if (ca.ins.token_buf != nullptr && P + path_cap >= ca.ins.token_stride) return -1;  // token room too
   const int lp0 = P / ca.page_size, lp1 = (P + path_cap - 1) / ca.page_size;
   if (lp1 - lp0 >= 32) return -1;
   int page = -1;
@@ -1127,7 +1133,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
 int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
                      const int32_t* accept_len, const int32_t* qo, const int32_t* page_table, int max_pages,
                      int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
-                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream);
+                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream, TokenInsert ins);
 
 // `commit` (nullable): also commit the accepted paths' K/V, as spec_kv_commit would right
 // after; greedy does it inside the acceptance kernel, stochastic with the commit kernel.
@@ -1147,7 +1153,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     if (e != SPEC_OK) return e;
     return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
                             ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
-                            ca.v_pool, batch, ca.hkv, ca.d, status, stream);
+                            ca.v_pool, batch, ca.hkv, ca.d, status, stream, ca.ins);
   }
   const int chunks = accept_chunks(total_nodes, vocab);
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
@@ -1208,7 +1214,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   if (ca.k_tree == nullptr) return SPEC_OK;
   return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
                           ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
-                          ca.v_pool, batch, ca.hkv, ca.d, status, stream);
+                          ca.v_pool, batch, ca.hkv, ca.d, status, stream, ca.ins);
 }
 
 }  // namespace specv

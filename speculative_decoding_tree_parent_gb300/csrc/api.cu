@@ -8,7 +8,7 @@ int launch_tree_mask(const int32_t* parent, const int32_t* qo, int batch, int to
 int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
                      const int32_t* accept_len, const int32_t* qo, const int32_t* page_table, int max_pages,
                      int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
-                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream);
+                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream, TokenInsert ins);
 int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl, const float* dl,
                   const float* uniforms, float temperature, int vocab, const int32_t* qo, int batch,
                   int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
@@ -45,7 +45,7 @@ using namespace specv;
 
 extern "C" {
 
-int spec_version(void) { return 100; }
+int spec_version(void) { return 110; }
 
 const char* spec_status_string(int status) {
   switch (status) {
@@ -191,14 +191,15 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
                        int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, int dtype,
                        const void* k_tree, const void* v_tree, const int32_t* page_table, int max_pages,
                        int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
-                       void* v_pool, int hkv, int d, void* ws, size_t ws_bytes, int32_t* dev_status,
-                       void* stream) {
+                       void* v_pool, int hkv, int d, int32_t* token_buf, int token_stride, void* ws,
+                       size_t ws_bytes, int32_t* dev_status, void* stream) {
   int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                         qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws, ws_bytes);
   if (rc != SPEC_OK) return rc;
   rc = check_commit(dtype, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages, num_pages,
                     page_size, prefix_len, k_pool, v_pool, batch, total_nodes, hkv, d);
   if (rc != SPEC_OK || batch == 0) return rc;
+  if (token_buf != nullptr && token_stride < 1) return SPEC_ERR_ARG;
   CommitArgs ca;
   ca.k_tree = static_cast<const uint8_t*>(k_tree);
   ca.v_tree = static_cast<const uint8_t*>(v_tree);
@@ -213,6 +214,7 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
   ca.hkv = hkv;
   ca.d = d;
   ca.elem_bytes = dtype == SPEC_F32 ? 4 : 2;
+  ca.ins = TokenInsert{out_tokens, token_buf, token_stride};
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
                        dev_status, static_cast<cudaStream_t>(stream), &ca);
@@ -228,7 +230,7 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
   const int elem = dtype == SPEC_F32 ? 4 : 2;
   return launch_kv_commit(elem, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
                           num_pages, page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
-                          static_cast<cudaStream_t>(stream));
+                          static_cast<cudaStream_t>(stream), TokenInsert{nullptr, nullptr, 0});
 }
 
 }  // extern "C"

@@ -40,6 +40,16 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Device-side insert of a step's tokens into each sequence's token buffer (the next step's
+// input, no host round trip): out_tokens[b][0 .. L] (the L accepted tokens, then the bonus,
+// which is the next root) go to token_buf[b][P + 1 .. P + L + 1], after the root at P.
+// token_buf == nullptr: no insert.
+struct TokenInsert {
+  const int32_t* out_tokens;  // [batch][path_cap]
+  int32_t* token_buf;         // [batch][token_stride]
+  int token_stride;
+};
+
 // Arguments of the KV commit when it runs fused after the acceptance (spec_accept_commit).
 struct CommitArgs {
   const uint8_t* k_tree;  // nullptr: no commit
@@ -51,6 +61,7 @@ struct CommitArgs {
   uint8_t* k_pool;
   uint8_t* v_pool;
   int hkv, d, elem_bytes;
+  TokenInsert ins;
 };
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }

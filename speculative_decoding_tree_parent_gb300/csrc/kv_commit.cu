@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     const int32_t* __restrict__ qo, const int32_t* __restrict__ page_table, int max_pages,
     int num_pages, int page_size, const int32_t* __restrict__ prefix_len,
     int32_t* __restrict__ seq_len_out, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
-    int hkv, int row_bytes, int32_t* status) {
+    int hkv, int row_bytes, int32_t* status, const TokenInsert ins) {
   const int b = blockIdx.x;
   __shared__ int s_ok;
   __shared__ int s_L;
@@ -48,6 +48,9 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     int ok = 1;
     if (L < 0 || L >= path_cap || L >= n || P < 0) {
       report(status, SPEC_ERR_INDEX);
+      ok = 0;
+    } else if (ins.token_buf != nullptr && P + L + 1 >= ins.token_stride) {
+      report(status, SPEC_ERR_CAPACITY);  // the token row has no room for L + 1 tokens after P
       ok = 0;
     }
     s_L = L;
@@ -95,6 +98,9 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(
     *reinterpret_cast<uint4*>(k_pool + dst) = kv;
     *reinterpret_cast<uint4*>(v_pool + dst) = vv;
   }
+  if (ins.token_buf != nullptr)  // the accepted tokens and the bonus after the root (room checked above)
+    for (int i = threadIdx.x; i <= L; i += blockDim.x)
+      ins.token_buf[(size_t)b * ins.token_stride + P + 1 + i] = __ldg(ins.out_tokens + (size_t)b * path_cap + i);
   if (threadIdx.x == 0 && seq_len_out != nullptr) seq_len_out[b] = P + L + 1;
 }
 
@@ -102,12 +108,12 @@ int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, con
                      int path_cap, const int32_t* accept_len, const int32_t* qo,
                      const int32_t* page_table, int max_pages, int num_pages, int page_size,
                      const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool, void* v_pool,
-                     int batch, int hkv, int d, int32_t* status, cudaStream_t stream) {
+                     int batch, int hkv, int d, int32_t* status, cudaStream_t stream, TokenInsert ins) {
   const int row_bytes = d * elem_bytes;
   if (launch_pdl(kv_commit_kernel, dim3(batch), dim3(256), 0, stream, static_cast<const uint8_t*>(k_tree),
                  static_cast<const uint8_t*>(v_tree), path, path_cap, accept_len, qo, page_table, max_pages,
                  num_pages, page_size, prefix_len, seq_len_out, static_cast<uint8_t*>(k_pool),
-                 static_cast<uint8_t*>(v_pool), hkv, row_bytes, status) != cudaSuccess)
+                 static_cast<uint8_t*>(v_pool), hkv, row_bytes, status, ins) != cudaSuccess)
     return SPEC_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -579,3 +579,134 @@ def test_accept_workspace_shared_across_sizes(inputs):
         for g, r in zip(got, refs[(id(db), mode)]):
             assert torch.equal(g, r), (mode, db.T)
     assert int(ws[:256].sum()) == 0
+
+
+# ------------------------------------------------------------------- 256-node trees
+
+def _large_tree_inputs(kind):
+    """256-node trees (four mask words): the Llama-3-8B head shape over two sequences, a
+    4096-token vocabulary; "eagle2" = best-first (wide and shallow), "random" = random
+    parents to depth 8 with draft tokens that often match the parent's target argmax."""
+    if kind == "eagle2":
+        sp = W.spec(2, batch=2, nodes=(256, 256), prefix=(700, 3000), vocab=4096, draft_noise=0.5,
+                    modes=("greedy", "stochastic"))
+    else:
+        sp = W.spec(2, batch=2, nodes=(256, 256), prefix=(700, 3000), vocab=4096, tree="random",
+                    agree_prob=0.9, bump=None, draft_noise=0.5, modes=("greedy", "stochastic"))
+    return W.generate(sp, 7)
+
+
+@pytest.mark.parametrize("kind", ["eagle2", "random"])
+def test_large_tree_path(kind):
+    inp = _large_tree_inputs(kind)
+    assert inp.max_nodes == 256 and inp.mask_words == 4
+    db = DeviceBatch(inp, mode="greedy")
+    db.build_mask()
+    db.attention()
+    torch.cuda.synchronize()
+    assert _status(db) == 0
+    mask, depth, words = _oracle_mask(inp)
+    assert np.array_equal(_mask_np(db), words)
+    assert np.array_equal(db.depth.cpu().numpy(), depth)
+    _attn_check(inp, db.out)
+    for mode in ("greedy", "stochastic"):
+        d2 = DeviceBatch(inp, mode=mode)
+        d2.accept_commit(mode)
+        torch.cuda.synchronize()
+        assert _status(d2) == 0
+        ref = _oracle_accept(inp, mode)
+        assert _accept_compare(d2, ref) == 0
+        k2, v2, seq = oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree,
+                                       inp.v_tree, ref.path, ref.accept_len, inp.qo_indptr, inp.page_size)
+        assert np.array_equal(d2.k_pool.float().cpu().numpy(), k2)
+        assert np.array_equal(d2.v_pool.float().cpu().numpy(), v2)
+        assert np.array_equal(d2.seq_len.cpu().numpy(), seq)
+    if kind == "random":
+        assert ref.accept_len.max() >= 3  # deep paths are exercised
+
+
+# ------------------------------------------------------------ next-step token insert
+
+def _deep_tokens(inp):
+    from dataclasses import replace
+    tokens = inp.draft_tokens.copy()
+    am = inp.target_logits.argmax(axis=1)
+    for b in range(inp.batch):
+        a, e = inp.qo_indptr[b], inp.qo_indptr[b + 1]
+        tokens[a + 1:e] = am[a + inp.parent[a + 1:e]]
+    return replace(inp, draft_tokens=tokens)
+
+
+@pytest.mark.parametrize("cfg,mode,deep", [(1, "greedy", False), (1, "greedy", True), (3, "greedy", False),
+                                           (5, "stochastic", False)])
+def test_accept_commit_token_insert(inputs, cfg, mode, deep):
+    """spec_accept_commit with a token buffer: after the call each row holds the old tokens
+    up to the root, then the step's accepted tokens and the bonus (the next root), and is
+    unchanged elsewhere -- the oracle's token_insert of the oracle's acceptance -- while the
+    K/V commit is that of the call without a buffer."""
+    inp = inputs(cfg)
+    if deep:
+        inp = _deep_tokens(inp)
+    db = DeviceBatch(inp, mode=mode)
+    stride = int(inp.prefix_len.max()) + inp.path_cap + 5
+    rng = np.random.default_rng(cfg)
+    buf0 = rng.integers(0, inp.vocab, (inp.batch, stride)).astype(np.int32)
+    buf = torch.from_numpy(buf0).cuda()
+    B.spec_accept_commit(B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY, db.parent, db.tokens,
+                         db.target_logits, db.qo, db.max_nodes, db.accept_len, db.path, db.out_tokens, db.acc_ws,
+                         db.k_tree, db.v_tree, db.page_table, db.prefix_len, db.k_pool, db.v_pool,
+                         seq_len_out=db.seq_len, draft_logits=db.draft_logits if mode == "stochastic" else None,
+                         uniforms=db.uniforms if mode == "stochastic" else None, temperature=inp.temperature,
+                         flags=db.flags, dev_status=db.status, token_buf=buf)
+    torch.cuda.synchronize()
+    assert _status(db) == 0
+    ref = _oracle_accept(inp, mode)
+    assert _accept_compare(db, ref) <= max(1, inp.batch // 20)   # oracle-flagged near-ties excluded
+    if deep:
+        assert ref.accept_len.max() >= 2
+    keep = ref.flags == 0
+    want = oracle.token_insert(buf0, inp.prefix_len, ref.out_tokens, ref.accept_len)
+    assert np.array_equal(buf.cpu().numpy()[keep], want[keep])
+    k2, v2, seq = oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree, inp.v_tree,
+                                   ref.path, ref.accept_len, inp.qo_indptr, inp.page_size)
+    if keep.all():
+        assert np.array_equal(db.k_pool.float().cpu().numpy(), k2)
+        assert np.array_equal(db.v_pool.float().cpu().numpy(), v2)
+        assert np.array_equal(db.seq_len.cpu().numpy(), seq)
+
+
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_accept_commit_token_insert_short_row(inputs, cfg):
+    """Token rows one position too short for the longest sequence's step: SPEC_ERR_CAPACITY,
+    the sequences without room left unwritten (K/V and tokens), the others committed and
+    inserted."""
+    inp = _deep_tokens(inputs(cfg))
+    db = DeviceBatch(inp)
+    ref = _oracle_accept(inp, "greedy")
+    need = inp.prefix_len.astype(np.int64) + ref.accept_len + 1   # last position written, per row
+    stride = int(need.max())                                      # that position is past the row
+    buf0 = np.full((inp.batch, stride), 7, np.int32)
+    buf = torch.from_numpy(buf0).cuda()
+    before_k, before_v = db.k_pool.clone(), db.v_pool.clone()
+    B.spec_accept_commit(B.SPEC_GREEDY, db.parent, db.tokens, db.target_logits, db.qo, db.max_nodes, db.accept_len,
+                         db.path, db.out_tokens, db.acc_ws, db.k_tree, db.v_tree, db.page_table, db.prefix_len,
+                         db.k_pool, db.v_pool, seq_len_out=db.seq_len, flags=db.flags, dev_status=db.status,
+                         token_buf=buf)
+    torch.cuda.synchronize()
+    assert _status(db) == -4   # SPEC_ERR_CAPACITY
+    assert _accept_compare(db, ref) == 0
+    got = buf.cpu().numpy()
+    fits = need < stride
+    assert (~fits).any()
+    assert np.array_equal(got[~fits], buf0[~fits])
+    if fits.any():
+        want = oracle.token_insert(buf0[fits], inp.prefix_len[fits], ref.out_tokens[fits], ref.accept_len[fits])
+        assert np.array_equal(got[fits], want)
+    kp, vp = db.k_pool.float().cpu().numpy(), db.v_pool.float().cpu().numpy()
+    kb, vb = before_k.float().cpu().numpy(), before_v.float().cpu().numpy()
+    for b in np.flatnonzero(~fits):
+        P = int(inp.prefix_len[b])
+        for i in range(int(ref.accept_len[b]) + 1):
+            page, row = inp.page_table[b, (P + i) // inp.page_size], (P + i) % inp.page_size
+            assert np.array_equal(kp[page, :, row], kb[page, :, row])
+            assert np.array_equal(vp[page, :, row], vb[page, :, row])

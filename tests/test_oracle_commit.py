@@ -49,3 +49,37 @@ def test_commit_logical_view_and_untouched_bytes():
     assert np.array_equal(by_slot(v2)[~touched], by_slot(vp)[~touched])
     # the inputs themselves are not modified
     assert not np.shares_memory(k2, kp)
+
+
+def test_token_insert_extends_each_sequence_by_its_emitted_tokens():
+    """After a step, reading row b up to the new length + 1 gives the old tokens up to the
+    root, then exactly the step's emitted tokens (accepted, then bonus): the sequence grows
+    by L + 1 tokens, the root stays where it was, and nothing else of the row changes."""
+    rng = np.random.default_rng(3)
+    B, stride = 4, 40
+    P = np.array([0, 7, 20, 33])
+    L = np.array([0, 3, 8, 2])
+    buf = rng.integers(0, 1000, (B, stride)).astype(np.int32)
+    out = np.full((B, 9), -1, np.int32)
+    emitted = []
+    for b in range(B):
+        toks = rng.integers(0, 1000, L[b] + 1)
+        out[b, : L[b] + 1] = toks
+        emitted.append(toks)
+    new = oracle.token_insert(buf, P, out, L)
+    for b in range(B):
+        n = P[b] + L[b] + 1               # the new sequence length (KV slots 0 .. P + L)
+        assert np.array_equal(new[b, : P[b] + 1], buf[b, : P[b] + 1])     # history and root
+        assert np.array_equal(new[b, P[b] + 1 : n + 1], emitted[b])       # the step's tokens
+        assert new[b, n] == emitted[b][-1]                                # next root = bonus
+        assert np.array_equal(new[b, n + 1 :], buf[b, n + 1 :])           # the rest untouched
+    assert not np.shares_memory(new, buf)
+
+
+def test_token_insert_rejects_a_short_row():
+    buf = np.zeros((1, 5), np.int32)
+    try:
+        oracle.token_insert(buf, [2], np.zeros((1, 9), np.int32), [2])   # needs positions 3 .. 5
+    except ValueError:
+        return
+    raise AssertionError("a row without room must be refused")
