@@ -351,6 +351,52 @@ def run_ours(args):
     assert e2e.device_status() == 0
     e2e_total = reduce_over_ranks(sum(e2e_ms), "max", ws, dev)
 
+    # ---- draft-tree construction on the device (spec_tree_expand) -------------------------
+    # One tree per sequence of the workload's shape (its node budget, top-10, depth 8) from
+    # seeded N(0, 2^2) draft logits rows, one per node; the max_nodes - 1 expansions are
+    # captured in one graph and timed after an L2 flush.
+    tree = None
+    n_tree = int(inp.max_nodes)
+    if n_tree > 1 and inp.batch * n_tree * inp.vocab * 4 <= (2 << 30):
+        from speculative_decoding_tree_parent_gb300 import binding as BIND
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(idx)
+        t_logits = torch.randn((inp.batch, n_tree, inp.vocab), generator=gen, device=dev) * 2.0
+        t_state = torch.zeros(BIND.spec_workspace_size(BIND.SPEC_OP_TREE, inp.batch, 0, n_tree, 0, 0, 0, 0, 0),
+                              dtype=torch.uint8, device=dev)
+        t_par = torch.empty((inp.batch, n_tree), dtype=torch.int32, device=dev)
+        t_tok = torch.empty_like(t_par)
+        t_nn = torch.empty(inp.batch, dtype=torch.int32, device=dev)
+        t_next = torch.empty_like(t_nn)
+        t_roots = torch.zeros(inp.batch, dtype=torch.int32, device=dev)
+
+        def build_tree():
+            BIND.spec_tree_init(t_roots, n_tree, t_state, t_par, t_tok, t_nn, t_next)
+            for _ in range(n_tree - 1):
+                BIND.spec_tree_expand(t_logits, n_tree, 10, 8, t_state, t_par, t_tok, t_nn, t_next,
+                                      row_stride=n_tree * inp.vocab, node_stride=inp.vocab)
+
+        with torch.cuda.stream(stream):
+            build_tree()
+        torch.cuda.synchronize()
+        g_tree = capture(build_tree)
+        tms = []
+        for r in range(max(args.warmup, 3) + 5):
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                flush_l2()
+                a_ev.record(stream)
+                g_tree.replay()
+                b_ev.record(stream)
+            b_ev.synchronize()
+            if r >= max(args.warmup, 3):
+                tms.append(a_ev.elapsed_time(b_ev) * 1e3)
+        assert int((t_next == -1).all().item()) == 1
+        t_us = statistics.median(tms)
+        tree = {"us_per_tree": t_us, "us_per_expand": t_us / (n_tree - 1), "nodes": n_tree, "sequences": inp.batch,
+                "topk": 10, "max_depth": 8, "vocab": inp.vocab,
+                "gbs": inp.batch * inp.vocab * 4 * (n_tree - 1) / (t_us * 1e-6) / 1e9}
+
     # ---- figures ------------------------------------------------------------------------
     wc = work_counts(inp, db.accept_len.cpu().numpy(), mode)
     hbm, tfl, tfl_sus, peak_kind = _peaks()
@@ -401,6 +447,7 @@ def run_ours(args):
                           "separate_us": (t_acc + t_com) * 1e6, "gbs": accom_gbs, "hbm_frac": accom_gbs / hbm,
                           "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
         "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
+        "draft_tree": tree,
         "roofline": roof,
         "e2e": {"value": job_throughput(tokens_all, e2e_total), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_total / args.steps},

@@ -92,11 +92,14 @@ typedef enum {
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 typedef enum { SPEC_GREEDY = 0, SPEC_STOCHASTIC = 1 } spec_mode;
-typedef enum { SPEC_OP_MASK = 0, SPEC_OP_ATTN = 1, SPEC_OP_ACCEPT = 2, SPEC_OP_COMMIT = 3 } spec_op;
+typedef enum { SPEC_OP_MASK = 0, SPEC_OP_ATTN = 1, SPEC_OP_ACCEPT = 2, SPEC_OP_COMMIT = 3,
+               SPEC_OP_TREE = 4 } spec_op;
 
 /* Bytes of workspace `op` needs for these sizes (0 when it needs none).
  * For SPEC_OP_ATTN the result depends on (batch, max_nodes, hq, hkv, d,
- * max_prefix, total_nodes); for SPEC_OP_ACCEPT on (batch, total_nodes, vocab).
+ * max_prefix, total_nodes); for SPEC_OP_ACCEPT on (batch, total_nodes, vocab); for
+ * SPEC_OP_TREE (the draft-tree state of spec_tree_init / spec_tree_expand) on
+ * (batch, max_nodes).
  * Unused arguments may be 0. Returns 0 for invalid sizes. */
 size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, int hq, int hkv,
                            int d, int max_prefix, int vocab);
@@ -275,6 +278,50 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
                        int32_t* seq_len_out, void* k_pool, void* v_pool, int hkv, int d,
                        int32_t* token_buf, int token_stride, void* ws, size_t ws_bytes,
                        int32_t* dev_status, void* stream);
+
+/*
+ * spec_tree_init / spec_tree_expand -- the EAGLE-2 dynamic draft tree, built on the device.
+ *   ("EAGLE-2 deep dive", section on the dynamic draft-tree algorithm: a node's confidence
+ *   is the product of the draft probabilities along its path; a priority queue pops the
+ *   best candidate as the next node; a node below the depth limit is expanded into its
+ *   top-k tokens, scored by the product, those at or below a threshold dropped; the tree
+ *   stops at the node budget.)
+ *   The draft model is the caller's: between two spec_tree_expand calls it writes the
+ *   logits row of each sequence's node awaiting expansion (next_node). A call reads that
+ *   row, computes p = softmax(row) and the top-k tokens (largest logit first, lower token
+ *   id on ties), pushes the k candidates with score = score(node) * p(token), then pops the
+ *   best candidate (largest score, the earlier push on ties) as node n_nodes (its parent and
+ *   token in parent_out / tokens_out); a popped node at the depth limit is not expanded and
+ *   the next best is popped, until one needs its expansion or max_nodes nodes exist. Node
+ *   ids therefore grow in pop order and parent[i] < i: parent_out / tokens_out feed
+ *   spec_build_tree_mask and the verification calls directly (row b = sequence b).
+ *
+ *   spec_tree_init: root_tokens int32 [batch] (the last accepted token of each sequence);
+ *     sets node 0 (parent -1, score 1), every other entry of parent_out / tokens_out to -1,
+ *     n_nodes_out = 1 and next_node = 0 (the root awaits its expansion; -1 if max_nodes = 1).
+ *   spec_tree_expand:
+ *     draft_logits  float; the row of sequence b for node u starts at
+ *                   draft_logits + b * row_stride + u * node_stride (elements). With the
+ *                   draft model writing one row per sequence: row_stride = vocab,
+ *                   node_stride = 0. Sequences whose next_node is -1 are skipped.
+ *     topk in [1, 16]; max_depth >= 1 (a node of that depth is not expanded);
+ *     threshold    candidates with score <= threshold are dropped (<= 0: none).
+ *     state        spec_workspace_size(SPEC_OP_TREE, batch, 0, max_nodes, ...) bytes,
+ *                  written by spec_tree_init; one state per tree under construction.
+ *     parent_out, tokens_out  int32 [batch][max_nodes] (in/out);  n_nodes_out, next_node
+ *                  int32 [batch] (out);  flags uint8 [batch] (out, nullable): bit 0 set
+ *                  when a pop's best two scores were within a relative 1e-6 (the
+ *                  probabilities are exp in fp32: such a pop could be ordered either way).
+ *   Scores: fp64 products of p(token) = exp(x - max) (fp32) / Z, Z summed in double-float.
+ *   Host errors as for the other calls; no device errors.
+ */
+int spec_tree_init(const int32_t* root_tokens, int batch, int max_nodes, void* state, size_t state_bytes,
+                   int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out, int32_t* next_node,
+                   uint8_t* flags, void* stream);
+int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride, long long node_stride,
+                     int batch, int max_nodes, int topk, int max_depth, double threshold, void* state,
+                     size_t state_bytes, int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out,
+                     int32_t* next_node, uint8_t* flags, int32_t* dev_status, void* stream);
 
 /*
  * spec_accept_noalloc — spec_accept for callers that cannot allocate device memory.

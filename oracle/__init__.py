@@ -29,6 +29,10 @@ Modules and the passages they follow (page title, then section):
               MTP-schedule sections (KV entries filled for accepted tokens; a kernel
               inserts the next token after the shift, with no CPU sync: token_insert).
 
+  draft_tree  "EAGLE-2 deep dive", section on the dynamic draft-tree algorithm (confidence =
+              product of draft probabilities along the path; a priority queue pops the
+              best candidate; nodes below the depth limit are expanded into top-k).
+
 Readings where the pages are silent are stated in each function's docstring.
 Every function here is pinned by `tests/test_oracle_*.py` against brute force,
 closed forms, textbook routines or hand-worked examples in `tests/golden/`.
@@ -38,6 +42,7 @@ from .tree_mask import ancestor_mask, ancestor_mask_batch, pack_mask_words
 from .attention import tree_verify_attention, tree_verify_attention_rows, gather_prefix
 from .accept import greedy_accept, stochastic_accept, AcceptResult
 from .commit import kv_commit, token_insert
+from .draft_tree import best_first_tree, topk_softmax
 
 __all__ = [
     "ancestor_mask",
@@ -51,4 +56,6 @@ __all__ = [
     "AcceptResult",
     "kv_commit",
     "token_insert",
+    "best_first_tree",
+    "topk_softmax",
 ]

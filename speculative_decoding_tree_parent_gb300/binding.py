@@ -18,14 +18,15 @@ from . import build as _build
 SPEC_OK = 0
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_GREEDY, SPEC_STOCHASTIC = 0, 1
-SPEC_OP_MASK, SPEC_OP_ATTN, SPEC_OP_ACCEPT, SPEC_OP_COMMIT = 0, 1, 2, 3
+SPEC_OP_MASK, SPEC_OP_ATTN, SPEC_OP_ACCEPT, SPEC_OP_COMMIT, SPEC_OP_TREE = 0, 1, 2, 3, 4
 STATUS = {
     0: "SPEC_OK", -1: "SPEC_ERR_ARG", -2: "SPEC_ERR_PARENT", -3: "SPEC_ERR_PAGE", -4: "SPEC_ERR_CAPACITY",
     -5: "SPEC_ERR_WORKSPACE", -6: "SPEC_ERR_UNSUPPORTED", -7: "SPEC_ERR_CUDA", -8: "SPEC_ERR_TIMEOUT",
     -9: "SPEC_ERR_INDEX",
 }
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
-           "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc")
+           "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
+           "spec_tree_init", "spec_tree_expand")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -41,6 +42,9 @@ _SIGS = {
     "spec_accept_commit": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P,
                                 _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _I, _P, _Z, _P, _P]),
     "spec_accept_noalloc": (_I, [_I, _P, _P, _P, _P, _P, _F, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "spec_tree_init": (_I, [_P, _I, _I, _P, _Z, _P, _P, _P, _P, _P, _P]),
+    "spec_tree_expand": (_I, [_P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _I, _I, _I, ctypes.c_double, _P, _Z,
+                              _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -199,3 +203,25 @@ def spec_accept_noalloc(mode, parent, draft_tokens, target_logits, qo_indptr, ma
         float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
         _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _ptr(dev_status), _stream(stream))
     return _check(st, "spec_accept_noalloc")
+
+
+def spec_tree_init(root_tokens, max_nodes, state, parent_out, tokens_out, n_nodes_out, next_node, flags=None,
+                   stream=None):
+    """Start one draft tree per sequence at its root token (see include/spec_verify.h)."""
+    st = load().spec_tree_init(_ptr(root_tokens), root_tokens.numel(), int(max_nodes), _ptr(state),
+                               state.numel() * state.element_size(), _ptr(parent_out), _ptr(tokens_out),
+                               _ptr(n_nodes_out), _ptr(next_node), _ptr(flags), _stream(stream))
+    return _check(st, "spec_tree_init")
+
+
+def spec_tree_expand(draft_logits, max_nodes, topk, max_depth, state, parent_out, tokens_out, n_nodes_out,
+                     next_node, row_stride, node_stride, threshold=0.0, flags=None, dev_status=None, stream=None):
+    """One expansion of every sequence's draft tree from the draft logits rows (vocabulary =
+    the last dimension of draft_logits; strides in elements)."""
+    V = draft_logits.shape[-1]
+    st = load().spec_tree_expand(_ptr(draft_logits), V, int(row_stride), int(node_stride), next_node.numel(),
+                                 int(max_nodes), int(topk), int(max_depth), float(threshold), _ptr(state),
+                                 state.numel() * state.element_size(), _ptr(parent_out), _ptr(tokens_out),
+                                 _ptr(n_nodes_out), _ptr(next_node), _ptr(flags), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_tree_expand")
+

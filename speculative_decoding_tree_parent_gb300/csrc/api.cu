@@ -1,6 +1,7 @@
 // C ABI of libspecverify: argument checks on the host, then kernel dispatch.
 // Every entry point is asynchronous on the caller's stream and allocates nothing.
 #include "attn_common.cuh"
+#include "draft_tree.cuh"
 
 namespace specv {
 int launch_tree_mask(const int32_t* parent, const int32_t* qo, int batch, int total_nodes, int max_nodes,
@@ -73,6 +74,9 @@ size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, in
     case SPEC_OP_ACCEPT:
       if (vocab <= 0) return 0;
       return accept_ws_bytes(batch, total_nodes, vocab);
+    case SPEC_OP_TREE:
+      if (max_nodes < 1 || max_nodes > kMaxNodes) return 0;
+      return tree_state_bytes(batch, max_nodes);
     default:
       return 0;
   }
@@ -231,6 +235,35 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
   return launch_kv_commit(elem, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
                           num_pages, page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
                           static_cast<cudaStream_t>(stream), TokenInsert{nullptr, nullptr, 0});
+}
+
+
+int spec_tree_init(const int32_t* root_tokens, int batch, int max_nodes, void* state, size_t state_bytes,
+                   int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out, int32_t* next_node,
+                   uint8_t* flags, void* stream) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes) return SPEC_ERR_ARG;
+  if (batch == 0) return SPEC_OK;
+  if (!root_tokens || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
+  if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
+  TreeArgs a{static_cast<uint8_t*>(state), max_nodes, 1, 1, 0.0, parent_out, tokens_out, n_nodes_out, next_node,
+             flags, nullptr};
+  return launch_tree_init(root_tokens, batch, a, static_cast<cudaStream_t>(stream));
+}
+
+int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride, long long node_stride, int batch,
+                     int max_nodes, int topk, int max_depth, double threshold, void* state, size_t state_bytes,
+                     int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out, int32_t* next_node,
+                     uint8_t* flags, int32_t* dev_status, void* stream) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes || vocab < 1 || topk < 1 || topk > 16 ||
+      max_depth < 1 || row_stride < 0 || node_stride < 0)
+    return SPEC_ERR_ARG;
+  if (batch == 0) return SPEC_OK;
+  if (!draft_logits || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
+  if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
+  TreeArgs a{static_cast<uint8_t*>(state), max_nodes, topk, max_depth, threshold, parent_out, tokens_out,
+             n_nodes_out, next_node, flags, dev_status};
+  return launch_tree_expand(draft_logits, vocab, (long)row_stride, (long)node_stride, batch, a,
+                            static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

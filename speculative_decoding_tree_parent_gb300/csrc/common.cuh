@@ -64,6 +64,36 @@ struct CommitArgs {
   TokenInsert ins;
 };
 
+// Double-float arithmetic: an fp32 pair (hi, lo) carrying about 48 significant bits,
+// for sums that must stay accurate without fp64 in loops (its rate is low on this part).
+struct F2 {
+  float hi, lo;
+};
+// Double-float sum. Its first step is exact (two-sum), so a + b and b + a give the same
+// bits: every lane of a butterfly ends with the same total.
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const float s = a.hi + b.hi;
+  const float v = s - a.hi;
+  float e = (a.hi - (s - v)) + (b.hi - v);
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return F2{hi, e - (hi - s)};
+}
+__device__ __forceinline__ F2 f2_warp_sum(F2 x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    x = f2_add(x, F2{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)});
+  return x;
+}
+
+__device__ __forceinline__ double f2_to_d(F2 x) { return (double)x.hi + (double)x.lo; }
+__device__ __forceinline__ F2 d_to_f2(double x) {
+  const float hi = (float)x;
+  return F2{hi, (float)(x - (double)hi)};
+}
+// a > b for normalised double-float values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
