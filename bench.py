@@ -464,6 +464,72 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- tree-size sweep
+
+def run_tree_sweep(args):
+    """Verification step cost by batch and draft-tree size ("EAGLE-2 deep dive", production
+    section: past about 32 concurrent requests verification turns compute-bound, so the tree
+    should shrink 64 -> 32 -> 16 as the batch grows, and speculation stop above 64). Each
+    case: the Llama-3-8B head shape, 2048-token prefixes, EAGLE-2 trees of N nodes, a
+    128256-token vocabulary (device-generated N(0,1) logits; the acceptance reads every row
+    once, whatever its values), one step = mask + attention + greedy accept + commit, timed
+    as CUDA-graph replays after an L2 flush. Reports the cost side only: the benefit side
+    (tokens accepted per step) needs the draft model, which is outside this path."""
+    import torch
+
+    from speculative_decoding_tree_parent_gb300 import binding as BIND
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_BYTES, dtype=torch.uint8, device=dev)
+    vocab = 128256
+    rows = []
+    for batch in (1, 8, 32, 64, 128):
+        for n in (64, 32, 16):
+            inp = W.generate(W.spec(3, batch=batch, nodes=(n, n), vocab=256, prefix=(2048, 2048)),
+                             3000 + batch * 100 + n)
+            db = DeviceBatch(inp, device=dev, mode="greedy")
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(batch * 1000 + n)
+            db.target_logits = torch.randn((inp.total_nodes, vocab), generator=gen, device=dev)
+            acc_ws = BIND.spec_workspace_size(BIND.SPEC_OP_ACCEPT, inp.batch, inp.total_nodes, inp.max_nodes,
+                                              0, 0, 0, 0, vocab)
+            db.acc_ws = torch.zeros(max(acc_ws, 256), dtype=torch.uint8, device=dev)
+            with torch.cuda.stream(stream):
+                db.step("greedy")
+            torch.cuda.synchronize()
+            assert db.device_status() == 0
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                db.step("greedy")
+            ts = []
+            for r in range(args.warmup + args.steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                b.synchronize()
+                if r >= args.warmup:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(ts)
+            rows.append({"batch": batch, "tree_nodes": n, "step_us": us, "us_per_sequence": us / batch,
+                         "tree_tokens_per_s": inp.total_nodes / (us * 1e-6),
+                         "mean_prefix": float(inp.prefix_len.mean())})
+            del db, g
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": "verification step us by batch and draft-tree size (cost side)",
+                      "unit": "us", "higher_is_better": False, "data": "synthetic",
+                      "config": {"workload": "Llama-3-8B head shape, prefix 2048, EAGLE-2 trees, vocab 128256, "
+                                             "greedy + commit",
+                                 "timing": "one step per CUDA-graph replay after an L2 flush, median"},
+                      "table": rows}), flush=True)
+
+
 # ----------------------------------------------------------------------------- oracle arm
 
 def _oracle_step(inp, oracle, mode="greedy"):
@@ -550,6 +616,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tree-sweep", action="store_true",
+                    help="print the verification step cost by batch and draft-tree size (64 / 32 / 16) instead")
     ap.add_argument("--workload", type=int, default=CONFIG_INDEX, choices=sorted(WORKLOADS),
                     help="workload index (default: the Llama-3-8B-shaped single-sequence verify the headline "
                          "is quoted on; the others are its parity cases, timed here for kernel scaling)")
@@ -558,6 +626,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.tree_sweep:
+        run_tree_sweep(args)
     else:
         run_ours(args)
 
