@@ -258,7 +258,7 @@ __device__ int greedy_walk_warp_staged(int b, int n, const int* parent, const in
 // unwritten.
 // Rows `first` .. L are copied (first = 1 when the root row went early, see
 // commit_root_early, whose P is then passed as P_pre; P_pre < 0: P is read here).
-template <bool kCta>
+template <bool kCta, bool kIns>
 __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, int L, const int* spath,
                                 const int32_t* gpath, int path_cap, int32_t* status, int first = 0,
                                 int P_pre = -1) {
@@ -270,7 +270,7 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
   int code = 0;
   if (L < 0 || L >= path_cap || L >= n || P < 0) {
     code = SPEC_ERR_INDEX;
-  } else if (ca.ins.token_buf != nullptr && P + L + 1 >= ca.ins.token_stride) {
+  } else if (kIns && P + L + 1 >= ca.ins.token_stride) {
     code = SPEC_ERR_CAPACITY;  // the token row has no room for L + 1 tokens after P
   } else {
     for (int i = first + rank; i <= L; i += size) {
@@ -332,7 +332,7 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
     *reinterpret_cast<uint4*>(ca.k_pool + dst) = kv;
     *reinterpret_cast<uint4*>(ca.v_pool + dst) = vv;
   }
-  if (ca.ins.token_buf != nullptr)  // the accepted tokens and the bonus after the root
+  if (kIns)  // the accepted tokens and the bonus after the root
     for (int i = rank; i <= L; i += size)
       ca.ins.token_buf[(size_t)b * ca.ins.token_stride + P + 1 + i] = ca.ins.out_tokens[(size_t)b * path_cap + i];
   if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
@@ -368,10 +368,11 @@ __device__ void root_stage(const CommitArgs& ca, int base, uint4* buf) {
 
 // The staged root rows of sequence b to slot P, when every reachable slot's page is valid
 // (each lane stores the chunks its own copies staged). Returns P when written, else -1.
+template <bool kIns>
 __device__ int root_write(const CommitArgs& ca, int b, int P, int n, int path_cap, const uint4* buf) {
   const int lane = threadIdx.x & 31;
   if (P < 0 || n < 1 || path_cap < 1) return -1;
-  if (ca.ins.token_buf != nullptr && P + path_cap >= ca.ins.token_stride) return -1;  // token room too
+  if (kIns && P + path_cap >= ca.ins.token_stride) return -1;  // token room too
   const int lp0 = P / ca.page_size, lp1 = (P + path_cap - 1) / ca.page_size;
   if (lp1 - lp0 >= 32) return -1;
   int page = -1;
@@ -395,7 +396,7 @@ __device__ int root_write(const CommitArgs& ca, int b, int P, int n, int path_ca
 }
 
 // (five CTAs per SM: the streaming loop needs the occupancy, the final CTA's epilogue may spill)
-template <bool kVec>
+template <bool kVec, bool kIns>
 __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     const float* __restrict__ logits, int vocab, int gchunks, int tasks, const int32_t* __restrict__ qo,
     int batch, int total_nodes, const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
@@ -588,7 +589,7 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
   if (early && warp == kRootWarp) {  // while warps 0 .. batch - 1 walk
     cp_async_wait_all();
     for (int b = 0; b < batch; ++b) {
-      const int r = root_write(ca, b, __shfl_sync(0xffffffffu, root_P, b), __shfl_sync(0xffffffffu, root_n, b),
+      const int r = root_write<kIns>(ca, b, __shfl_sync(0xffffffffu, root_P, b), __shfl_sync(0xffffffffu, root_n, b),
                                path_cap, root_buf(b));
       if (lane == 0) s_root_P[b] = r;
     }
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     for (int b = 0; b < batch; ++b) {
       const int base = __ldg(qo + b);
       const int rootP = early ? s_root_P[b] : -1;
-      commit_sequence<true>(ca, b, base, __ldg(qo + b + 1) - base, staged ? s_len[b] : accept_len[b],
+      commit_sequence<true, kIns>(ca, b, base, __ldg(qo + b + 1) - base, staged ? s_len[b] : accept_len[b],
                             in_smem ? s_cpath[b] : nullptr, path + (size_t)b * path_cap, path_cap, status,
                             rootP >= 0 ? 1 : 0, rootP);
       __syncthreads();
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
   } else {
     for (int b = warp; b < batch; b += kAcceptThreads / 32) {
       const int base = __ldg(qo + b);
-      commit_sequence<false>(ca, b, base, __ldg(qo + b + 1) - base, accept_len[b], nullptr,
+      commit_sequence<false, kIns>(ca, b, base, __ldg(qo + b + 1) - base, accept_len[b], nullptr,
                              path + (size_t)b * path_cap, path_cap, status);
     }
   }
@@ -1141,9 +1142,13 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     int* am = reinterpret_cast<int*>(wb + w.results);
     const int gch = greedy_chunks(vocab);
     const int tasks = total_nodes * gch;
-    static int per_sm[2] = {0, 0};
-    auto kern = vec ? accept_greedy_kernel<true> : accept_greedy_kernel<false>;
-    int& occ = per_sm[vec ? 1 : 0];
+    static int per_sm[4] = {0, 0, 0, 0};
+    // (the token insert is a separate instance: calls without a token buffer run code that
+    // carries none of it, which keeps the streaming kernel's registers as they were)
+    const bool ins = ca.ins.token_buf != nullptr;
+    auto kern = vec ? (ins ? accept_greedy_kernel<true, true> : accept_greedy_kernel<true, false>)
+                    : (ins ? accept_greedy_kernel<false, true> : accept_greedy_kernel<false, false>);
+    int& occ = per_sm[(vec ? 1 : 0) + (ins ? 2 : 0)];
     if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAcceptThreads, 0) != cudaSuccess ||
                      occ < 1))
       occ = 1;
