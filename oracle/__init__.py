@@ -32,6 +32,10 @@ Modules and the passages they follow (page title, then section):
   draft_tree  "EAGLE-2 deep dive", section on the dynamic draft-tree algorithm (confidence =
               product of draft probabilities along the path; a priority queue pops the
               best candidate; nodes below the depth limit are expanded into top-k).
+  fp8         "EAGLE-3 paper explainer" (0h-n0), operations section, model-optimisation list
+              (quantisation and PagedAttention KV-cache tuning to cut GPU memory): the E4M3
+              codes and per-KV-head scales of an FP8 paged KV cache, used by attention and
+              commit when a `kv_scale` is given.
 
 Readings where the pages are silent are stated in each function's docstring.
 Every function here is pinned by `tests/test_oracle_*.py` against brute force,
@@ -43,6 +47,7 @@ from .attention import tree_verify_attention, tree_verify_attention_rows, gather
 from .accept import greedy_accept, stochastic_accept, AcceptResult
 from .commit import kv_commit, token_insert
 from .draft_tree import best_first_tree, topk_softmax
+from .fp8 import e4m3_decode, e4m3_encode, kv_quantize, kv_dequantize
 
 __all__ = [
     "ancestor_mask",
@@ -58,4 +63,8 @@ __all__ = [
     "token_insert",
     "best_first_tree",
     "topk_softmax",
+    "e4m3_decode",
+    "e4m3_encode",
+    "kv_quantize",
+    "kv_dequantize",
 ]

@@ -17,10 +17,23 @@ what the definition above implies and what "Accelerating Sonar through
 speculation", EAGLE section, motivates (a custom mask over the whole sequence
 is what slows attention).
 
-All arithmetic is float64 on the given (bf16-representable or fp32) inputs.
+All arithmetic is float64 on the given (bf16-representable or fp32) inputs. With an FP8
+cache (`kv_scale` given), the pools hold E4M3 codes and a prefix key or value is the code's
+value times its KV head's scale (oracle.fp8); the tree K/V stay as given.
 """
 
 import numpy as np
+
+from .fp8 import kv_dequantize
+
+
+def _prefix_values(pool, page_table_row, length, page_size, scale):
+    """Gathered prefix slots [length, heads, D] in float64, dequantised when scale is given
+    (scale [heads])."""
+    x = gather_prefix(pool, page_table_row, length, page_size)
+    if scale is None:
+        return x.astype(np.float64)
+    return kv_dequantize(x, np.asarray(scale, np.float32)[None, :, None])
 
 
 def gather_prefix(pool: np.ndarray, page_table_row: np.ndarray, length: int, page_size: int) -> np.ndarray:
@@ -45,13 +58,14 @@ def _one_head(qrows, K, V, allow, sm_scale):
 
 def tree_verify_attention(q, k_pool, v_pool, page_table, prefix_len, k_tree, v_tree,
                           mask, qo_indptr, hq, hkv, sm_scale=None, page_size=16,
-                          seqs=None):
+                          seqs=None, kv_scale=None):
     """Full oracle attention.
 
     q [T, Hq, D]; k_pool/v_pool [pages, Hkv, page_size, D]; page_table [B, max_pages];
     prefix_len [B]; k_tree/v_tree [T, Hkv, D]; mask bool [T, >= N_b] (sequence-local
     columns); qo_indptr [B+1]. Returns (o float64 [T, Hq, D], lse float64 [T, Hq]).
-    `seqs` restricts the work to some sequences (other rows stay NaN).
+    `seqs` restricts the work to some sequences (other rows stay NaN). `kv_scale` [2, Hkv]
+    (K scales, then V scales): the pools hold E4M3 codes.
     """
     q = np.asarray(q, np.float64)
     T, Hq, D = q.shape
@@ -69,8 +83,8 @@ def tree_verify_attention(q, k_pool, v_pool, page_table, prefix_len, k_tree, v_t
         if n == 0:
             continue
         P = int(prefix_len[b])
-        Kp = gather_prefix(k_pool, page_table[b], P, page_size).astype(np.float64)
-        Vp = gather_prefix(v_pool, page_table[b], P, page_size).astype(np.float64)
+        Kp = _prefix_values(k_pool, page_table[b], P, page_size, None if kv_scale is None else kv_scale[0])
+        Vp = _prefix_values(v_pool, page_table[b], P, page_size, None if kv_scale is None else kv_scale[1])
         K = np.concatenate([Kp, np.asarray(k_tree[a:e], np.float64)], axis=0)
         V = np.concatenate([Vp, np.asarray(v_tree[a:e], np.float64)], axis=0)
         allow = np.concatenate([np.ones((n, P), bool), np.asarray(mask[a:e, :n], bool)], axis=1)
@@ -83,11 +97,12 @@ def tree_verify_attention(q, k_pool, v_pool, page_table, prefix_len, k_tree, v_t
 
 
 def tree_verify_attention_rows(rows, q, k_pool, v_pool, page_table, prefix_len, k_tree, v_tree,
-                               mask, qo_indptr, hq, hkv, sm_scale=None, page_size=16):
+                               mask, qo_indptr, hq, hkv, sm_scale=None, page_size=16, kv_scale=None):
     """Oracle output for selected (node t, head h) rows only, one at a time.
 
     Used on full-size workloads where the whole oracle would take too long.
-    Returns (o float64 [len(rows), D], lse float64 [len(rows)]).
+    Returns (o float64 [len(rows), D], lse float64 [len(rows)]). `kv_scale` as in
+    tree_verify_attention.
     """
     q = np.asarray(q)
     D = q.shape[2]
@@ -106,8 +121,10 @@ def tree_verify_attention_rows(rows, q, k_pool, v_pool, page_table, prefix_len, 
         key = (b, g)
         if key not in cache:
             P = int(prefix_len[b])
-            Kp = gather_prefix(k_pool[:, g : g + 1], page_table[b], P, page_size)[:, 0].astype(np.float64)
-            Vp = gather_prefix(v_pool[:, g : g + 1], page_table[b], P, page_size)[:, 0].astype(np.float64)
+            ks = None if kv_scale is None else [kv_scale[0][g]]
+            vs = None if kv_scale is None else [kv_scale[1][g]]
+            Kp = _prefix_values(k_pool[:, g : g + 1], page_table[b], P, page_size, ks)[:, 0]
+            Vp = _prefix_values(v_pool[:, g : g + 1], page_table[b], P, page_size, vs)[:, 0]
             K = np.concatenate([Kp, np.asarray(k_tree[a:e, g], np.float64)], axis=0)
             V = np.concatenate([Vp, np.asarray(v_tree[a:e, g], np.float64)], axis=0)
             cache = {key: (K, V, P)}

@@ -17,10 +17,16 @@ pool is left as it was.
 
 import numpy as np
 
+from .fp8 import kv_quantize
+
 
 def kv_commit(k_pool, v_pool, page_table, prefix_len, k_tree, v_tree, path, accept_len,
-              qo_indptr, page_size=16):
-    """Returns (new k_pool, new v_pool, seq_len int32 [B]); the inputs are not modified."""
+              qo_indptr, page_size=16, kv_scale=None):
+    """Returns (new k_pool, new v_pool, seq_len int32 [B]); the inputs are not modified.
+
+    With `kv_scale` [2, Hkv] the pools hold E4M3 codes: a committed row of KV head g is
+    written as the codes of k_tree / kv_scale[0][g] (and v_tree / kv_scale[1][g]), the
+    division in fp32 (oracle.fp8.kv_quantize)."""
     kp = np.array(k_pool, copy=True)
     vp = np.array(v_pool, copy=True)
     qo = np.asarray(qo_indptr, np.int64)
@@ -36,8 +42,12 @@ def kv_commit(k_pool, v_pool, page_table, prefix_len, k_tree, v_tree, path, acce
             page = int(page_table[b][slot // page_size])
             if page < 0 or page >= kp.shape[0]:
                 raise ValueError("no cache page for a committed slot")
-            kp[page, :, slot % page_size, :] = k_tree[a + node]
-            vp[page, :, slot % page_size, :] = v_tree[a + node]
+            if kv_scale is None:
+                kp[page, :, slot % page_size, :] = k_tree[a + node]
+                vp[page, :, slot % page_size, :] = v_tree[a + node]
+            else:
+                kp[page, :, slot % page_size, :] = kv_quantize(k_tree[a + node], np.asarray(kv_scale[0])[:, None])
+                vp[page, :, slot % page_size, :] = kv_quantize(v_tree[a + node], np.asarray(kv_scale[1])[:, None])
         seq_len[b] = P + L + 1
     return kp, vp, seq_len
 
