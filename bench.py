@@ -117,13 +117,15 @@ def work_counts(inp, accept_len=None, mode="greedy"):
                      + inp.total_nodes * inp.hkv * inp.d * esz * 2  # tree K and V
                      + inp.total_nodes * inp.hq * inp.d * esz * 2   # Q in, O out
                      + inp.total_nodes * inp.mask_words * 8)
+    # FP8 cache: one byte per prefix K/V element (the tree K/V, Q and O stay bf16)
+    attn_bytes_fp8kv = attn_bytes - int(P.sum() * inp.hkv * inp.d * (esz - 1) * 2)
     # one pass over every node's logits (target, and draft too for stochastic acceptance)
     accept_bytes = int(inp.total_nodes * inp.vocab * 4 * (2 if mode == "stochastic" else 1))
     commit_bytes = 0
     if accept_len is not None:
         commit_bytes = int(((np.asarray(accept_len) + 1) * inp.hkv * inp.d * esz * 2 * 2).sum())
-    return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, accept_bytes=accept_bytes, commit_bytes=commit_bytes,
-                tokens=int(inp.total_nodes))
+    return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, attn_bytes_fp8kv=attn_bytes_fp8kv,
+                accept_bytes=accept_bytes, commit_bytes=commit_bytes, tokens=int(inp.total_nodes))
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -266,6 +268,22 @@ def run_ours(args):
                "accept_commit": capture(over_reps("accept_commit"))}
     launches = db.launches_per_step(mode)
     splits, tc = db.attn_plan()
+    attn_launches = 2 if splits > 1 else 1
+    # per-call graphs: mask 1, attention, accept (1 greedy, 2 stochastic), commit 1, fused call
+    call_launches = 1 + attn_launches + (2 if mode == "stochastic" else 1) + 1 + (launches - 1 - attn_launches)
+    # the same attention over an FP8 (E4M3) copy of the pool, on its own replicas (tensor-core
+    # shapes only): prefix K/V bytes halve
+    reps8 = []
+    if tc and inp.dtype == "bf16":
+        reps8 = [DeviceBatch(inp, device=dev, mode=mode, kv_fp8=True) for _ in range(R)]
+        with torch.cuda.stream(stream):
+            for rep in reps8:
+                rep.build_mask()
+                rep.attention()
+        torch.cuda.synchronize()
+        assert all(rep.device_status() == 0 for rep in reps8)
+        g_calls["attention_fp8kv"] = capture(lambda: [rep.attention() for rep in reps8])
+        call_launches += attn_launches
 
     def flush_l2():
         """Write a buffer larger than L2, then read it back: the L2 then holds none of the
@@ -404,6 +422,13 @@ def run_ours(args):
     tokens_all = reduce_over_ranks(wc["tokens"], "sum", ws, dev) * args.steps
     value = job_throughput(tokens_all, total_ms)
     t_attn = statistics.mean(call_ms["attention"]) / 1e3
+    attn8 = None
+    if "attention_fp8kv" in call_ms:
+        t8 = statistics.mean(call_ms["attention_fp8kv"]) / 1e3
+        b8 = wc["attn_bytes_fp8kv"]
+        attn8 = {"us": t8 * 1e6, "tokens_per_s": wc["tokens"] / t8, "gbs": b8 / t8 / 1e9,
+                 "roofline_frac": max(wc["attn_flops"] / (tfl * 1e12), b8 / (hbm * 1e9)) / t8,
+                 "tflops": wc["attn_flops"] / t8 / 1e12, "bytes": b8, "kv": "e4m3 codes + fp32 scale per KV head"}
     t_acc = statistics.mean(call_ms["accept"]) / 1e3
     t_com = statistics.mean(call_ms["commit"]) / 1e3
     attn_gbs = wc["attn_bytes"] / t_attn / 1e9
@@ -447,12 +472,13 @@ def run_ours(args):
                           "separate_us": (t_acc + t_com) * 1e6, "gbs": accom_gbs, "hbm_frac": accom_gbs / hbm,
                           "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
         "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
+        "attn_fp8kv": attn8,
         "draft_tree": tree,
         "roofline": roof,
         "e2e": {"value": job_throughput(tokens_all, e2e_total), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_total / args.steps},
-        # launches in the timed region: full-step replays + per-call replays (each call's kernels once)
-        "gpu_launches": 2 * launches * args.steps,   # step replays + per-call replays, R steps each
+        # launches in the timed region: full-step replays + per-call replays, R steps each
+        "gpu_launches": (launches + call_launches) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

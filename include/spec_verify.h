@@ -11,7 +11,9 @@
  *   spec_kv_commit         the accepted path's K/V written into the paged cache
  *
  * spec_accept_commit runs the last two as one call (the same results, one kernel
- * boundary fewer).
+ * boundary fewer). spec_tree_verify_attn_kv8 and spec_kv_commit_kv8 are the attention
+ * and the commit over an FP8 (E4M3) paged cache; spec_tree_init / spec_tree_expand build
+ * the draft tree on the device.
  *
  * Sources of the operations (page title, then section):
  *   "EAGLE-2 deep dive" (techknowgenie): architecture section (all tree tokens
@@ -346,6 +348,57 @@ int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_to
                         int total_nodes, int max_nodes, int path_cap, int32_t* accept_len,
                         int32_t* path, int32_t* out_tokens, uint8_t* flags, int32_t* dev_status,
                         void* stream);
+
+/*
+ * FP8 KV cache: spec_tree_verify_attn_kv8 / spec_kv_commit_kv8.
+ *   ("EAGLE-3 paper explainer" (0h-n0), operations section, model-optimisation list:
+ *   quantisation and PagedAttention KV-cache tuning to cut GPU memory. The page names no
+ *   format; this library reads it as follows.)
+ *   The paged pool holds E4M3 codes, as the OCP 8-bit floating-point format defines them:
+ *   1 sign, 4 exponent (bias 7) and 3 mantissa bits, subnormals at exponent 0, S.1111.111
+ *   = NaN, largest magnitude 448. Code c of KV head g stands for
+ *   value(c) * kv_scale[0][g] in K and value(c) * kv_scale[1][g] in V.
+ *   kv_scale   float32 [2][hkv], device memory: K scales, then V scales. Each scale must
+ *              be positive, finite and normal. A scale is read on the device at every
+ *              call, so it may change between replays of a captured graph.
+ *   k_pool, v_pool  uint8 [num_pages][hkv][page_size][d] codes, 16-byte aligned.
+ *   The tree's own K/V (k_tree, v_tree), q and out stay bf16.
+ *
+ * spec_tree_verify_attn_kv8 — spec_tree_verify_attn (same arguments minus dtype, plus
+ *   kv_scale) over an FP8 pool. The result is the attention of the definition with every
+ *   prefix key and value replaced by its dequantised value; the tree keys are used as
+ *   given. The tensor-core path only: d = 128, page_size = 16, hq / hkv dividing 128;
+ *   other shapes return SPEC_ERR_UNSUPPORTED. The workspace is spec_workspace_size(
+ *   SPEC_OP_ATTN, ...) for the same sizes. Errors as for spec_tree_verify_attn; q, k_tree,
+ *   v_tree, out and (with a prefix) the pools must be 16-byte aligned (else SPEC_ERR_ARG).
+ *   NaN codes in the pool make the affected rows NaN.
+ */
+int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                              const float* kv_scale, int num_pages, int page_size,
+                              const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                              int max_prefix, const void* k_tree, const void* v_tree,
+                              const uint64_t* mask, const int32_t* qo_indptr, int batch,
+                              int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale,
+                              void* out, float* lse, void* ws, size_t ws_bytes, int32_t* dev_status,
+                              void* stream);
+
+/*
+ * spec_kv_commit_kv8 — spec_kv_commit from bf16 tree rows into an FP8 pool.
+ *   Every element x of a committed row of KV head g is written as the E4M3 code nearest to
+ *   x / scale (the division in IEEE fp32, then round to nearest, ties to the even code).
+ *   Finite quotients beyond +-448 saturate to +-448. scale = kv_scale[0][g] for K,
+ *   kv_scale[1][g] for V. Arguments, checks and device errors are those of spec_kv_commit
+ *   with dtype = SPEC_BF16 for the tree rows. d must be a multiple of 16 (else
+ *   SPEC_ERR_UNSUPPORTED). kv_scale must not be NULL (SPEC_ERR_ARG).
+ *   For a fused greedy acceptance + commit into an FP8 pool, call spec_accept and then
+ *   this call on the same stream.
+ */
+int spec_kv_commit_kv8(const void* k_tree, const void* v_tree, const float* kv_scale,
+                       const int32_t* path, int path_cap, const int32_t* accept_len,
+                       const int32_t* qo_indptr, const int32_t* page_table, int max_pages,
+                       int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out,
+                       uint8_t* k_pool, uint8_t* v_pool, int batch, int total_nodes, int hkv, int d,
+                       int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

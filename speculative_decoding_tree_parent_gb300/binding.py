@@ -26,7 +26,7 @@ STATUS = {
 }
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
            "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
-           "spec_tree_init", "spec_tree_expand")
+           "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -45,6 +45,9 @@ _SIGS = {
     "spec_tree_init": (_I, [_P, _I, _I, _P, _Z, _P, _P, _P, _P, _P, _P]),
     "spec_tree_expand": (_I, [_P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _I, _I, _I, ctypes.c_double, _P, _Z,
                               _P, _P, _P, _P, _P, _P, _P]),
+    "spec_tree_verify_attn_kv8": (_I, [_P, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                       _I, _F, _P, _P, _P, _Z, _P, _P]),
+    "spec_kv_commit_kv8": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 _lib = None
@@ -225,3 +228,38 @@ def spec_tree_expand(draft_logits, max_nodes, topk, max_depth, state, parent_out
                                  _ptr(n_nodes_out), _ptr(next_node), _ptr(flags), _ptr(dev_status), _stream(stream))
     return _check(st, "spec_tree_expand")
 
+
+
+def spec_tree_verify_attn_kv8(q, k_pool, v_pool, kv_scale, page_table, prefix_len, max_prefix, k_tree, v_tree,
+                              mask, qo_indptr, max_nodes, out, lse=None, ws=None, sm_scale=0.0, dev_status=None,
+                              stream=None):
+    """Tree-verify attention over an FP8 cache: k_pool/v_pool uint8 E4M3 codes
+    [pages,Hkv,16,128], kv_scale float32 [2,Hkv] (K scales, then V scales); q, k_tree,
+    v_tree and out bf16."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_pool, torch.uint8, "k_pool (E4M3 codes)")
+    _need(v_pool, torch.uint8, "v_pool (E4M3 codes)")
+    _need(kv_scale, torch.float32, "kv_scale")
+    T, hq, d = q.shape
+    num_pages, hkv, ps, _ = k_pool.shape
+    st = load().spec_tree_verify_attn_kv8(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(kv_scale), num_pages, ps, _ptr(page_table), page_table.shape[1],
+        _ptr(prefix_len), int(max_prefix), _ptr(k_tree), _ptr(v_tree), _ptr(mask), _ptr(qo_indptr),
+        qo_indptr.numel() - 1, T, int(max_nodes), hq, hkv, d, float(sm_scale), _ptr(out), _ptr(lse),
+        _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_tree_verify_attn_kv8")
+
+
+def spec_kv_commit_kv8(k_tree, v_tree, kv_scale, path, accept_len, qo_indptr, page_table, prefix_len, k_pool,
+                       v_pool, seq_len_out=None, dev_status=None, stream=None):
+    """Commit of bf16 tree K/V rows into an FP8 cache (E4M3 codes of x / scale)."""
+    _need(k_tree, torch.bfloat16, "k_tree")
+    _need(k_pool, torch.uint8, "k_pool (E4M3 codes)")
+    _need(kv_scale, torch.float32, "kv_scale")
+    T, hkv, d = k_tree.shape
+    num_pages, _, ps, _ = k_pool.shape
+    st = load().spec_kv_commit_kv8(
+        _ptr(k_tree), _ptr(v_tree), _ptr(kv_scale), _ptr(path), path.shape[1], _ptr(accept_len), _ptr(qo_indptr),
+        _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
+        _ptr(v_pool), qo_indptr.numel() - 1, T, hkv, d, _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_kv_commit_kv8")

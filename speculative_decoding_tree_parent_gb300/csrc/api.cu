@@ -9,7 +9,8 @@ int launch_tree_mask(const int32_t* parent, const int32_t* qo, int batch, int to
 int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
                      const int32_t* accept_len, const int32_t* qo, const int32_t* page_table, int max_pages,
                      int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
-                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream, TokenInsert ins);
+                     void* v_pool, int batch, int hkv, int d, int32_t* status, cudaStream_t stream, TokenInsert ins,
+                     const float* kv_scale);
 int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl, const float* dl,
                   const float* uniforms, float temperature, int vocab, const int32_t* qo, int batch,
                   int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
@@ -26,7 +27,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                    const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
                    int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
-                   void* ws, int32_t* status, cudaStream_t stream);
+                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale);
 
 constexpr int kMaxNodes = 1024;
 
@@ -46,7 +47,7 @@ using namespace specv;
 
 extern "C" {
 
-int spec_version(void) { return 110; }
+int spec_version(void) { return 111; }
 
 const char* spec_status_string(int status) {
   switch (status) {
@@ -132,7 +133,7 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
       aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree) && aligned16(out))
     return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                           k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale,
-                          out, lse, ws, dev_status, st);
+                          out, lse, ws, dev_status, st, nullptr);
   return launch_attn_simt(dtype, q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len,
                           max_prefix, k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d,
                           sm_scale, out, lse, ws, dev_status, st);
@@ -234,7 +235,50 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
   const int elem = dtype == SPEC_F32 ? 4 : 2;
   return launch_kv_commit(elem, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages,
                           num_pages, page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
-                          static_cast<cudaStream_t>(stream), TokenInsert{nullptr, nullptr, 0});
+                          static_cast<cudaStream_t>(stream), TokenInsert{nullptr, nullptr, 0}, nullptr);
+}
+
+int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool, const float* kv_scale,
+                              int num_pages, int page_size, const int32_t* page_table, int max_pages,
+                              const int32_t* prefix_len, int max_prefix, const void* k_tree, const void* v_tree,
+                              const uint64_t* mask, const int32_t* qo_indptr, int batch, int total_nodes,
+                              int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse, void* ws,
+                              size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (batch < 0 || total_nodes < 0 || max_nodes < 1 || max_nodes > kMaxNodes || max_prefix < 0 ||
+      num_pages < 0 || max_pages < 0)
+    return SPEC_ERR_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
+  if (!attn_tc_supported(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (batch == 0 || total_nodes == 0) return SPEC_OK;
+  if (!q || !k_tree || !v_tree || !mask || !qo_indptr || !prefix_len || !out || !kv_scale) return SPEC_ERR_ARG;
+  if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
+    return SPEC_ERR_ARG;
+  if ((long)max_pages * page_size < max_prefix) return SPEC_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out) ||
+      (max_prefix > 0 && (!aligned16(k_pool) || !aligned16(v_pool))))
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
+  if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
+  return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
+                        k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale, out,
+                        lse, ws, dev_status, static_cast<cudaStream_t>(stream), kv_scale);
+}
+
+int spec_kv_commit_kv8(const void* k_tree, const void* v_tree, const float* kv_scale, const int32_t* path,
+                       int path_cap, const int32_t* accept_len, const int32_t* qo_indptr, const int32_t* page_table,
+                       int max_pages, int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out,
+                       uint8_t* k_pool, uint8_t* v_pool, int batch, int total_nodes, int hkv, int d,
+                       int32_t* dev_status, void* stream) {
+  // the tree rows are bf16 (d * 2 bytes), the pool rows d codes: d a multiple of 16
+  const int rc = check_commit(SPEC_BF16, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table,
+                              max_pages, num_pages, page_size, prefix_len, k_pool, v_pool, batch, total_nodes, hkv, d);
+  if (rc != SPEC_OK || batch == 0) return rc;
+  if (d % 16 != 0) return SPEC_ERR_UNSUPPORTED;
+  if (!kv_scale) return SPEC_ERR_ARG;
+  return launch_kv_commit(2, k_tree, v_tree, path, path_cap, accept_len, qo_indptr, page_table, max_pages, num_pages,
+                          page_size, prefix_len, seq_len_out, k_pool, v_pool, batch, hkv, d, dev_status,
+                          static_cast<cudaStream_t>(stream), TokenInsert{nullptr, nullptr, 0}, kv_scale);
 }
 
 

@@ -29,6 +29,15 @@
 //               TMEM only when the running max grows by more than 2^8.
 // S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
 // does. Every wait is bounded.
+// FP8 cache (attn_tc_kernel<true>): the pool holds E4M3 codes ([page][Hkv][16][128] bytes,
+// a 2 KB tile per (page, head)) with an fp32 scale per KV head for K and for V. Prefix
+// pages are TMA-loaded into a 3-stage ring of 16 KB code stages (half the bytes of bf16),
+// and four more warps (11-14) widen each stage into the bf16 ring, in the swizzled layout
+// TMA would have written, with integer ops and a packed multiply (no conversion-pipe
+// instructions). The conversion is exact: every E4M3 value is a bf16 value. The
+// scales never touch the operands. The K scale multiplies the prefix blocks' score scale.
+// The V scale is folded into the exponent of those blocks' P (2^(s - m + log2 v_scale)),
+// and their row sum is divided by it. Tree blocks are bf16 and TMA-loaded as before.
 // When the keys are split (a short batch cannot fill 152 SMs otherwise), each split CTA
 // writes a partial per tile (O / l rounded to bf16 plus the split's log2-sum-exp;
 // coalesced, L2-resident) and a small merge kernel, launched with programmatic
@@ -49,6 +58,9 @@ constexpr int kTcD = 128;
 constexpr int kTcStages = 4;
 constexpr int kTiles = 2;
 constexpr int kTcThreads = 64 + kTiles * 128 + 32;  // + one more MMA-issuing warp
+constexpr int kMma1Warp = kTcThreads / 32 - 1;     // the MMA issuer of tile 1
+constexpr int kCvtWarps = 4;                       // FP8 cache: code -> bf16 converters
+constexpr int kF8Stages = 3;
 constexpr float kRescaleThr = 8.0f;            // log2 units: P entries stay <= 2^8
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s) before a wait gives up
 
@@ -56,14 +68,24 @@ constexpr uint32_t kQSlab = kTcRows * 128;                  // 16 KB: 128 rows x
 constexpr uint32_t kQTile = 2 * kQSlab;
 constexpr uint32_t kKVSlab = kTcKeys * 128;                 // 8 KB: 64 keys x 64 bf16
 constexpr uint32_t kStageBytes = 4 * kKVSlab;               // K (2 slabs) + V (2 slabs)
+constexpr uint32_t kF8Stage = 2 * kTcKeys * kTcD;           // 16 KB: K codes, then V codes
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kTiles * kQTile;
-constexpr uint32_t kOffBar = kOffKV + kTcStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;       // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;                         // per tile: S0 | S1 | O (P aliases S)
 constexpr uint32_t kIdescQK = tc::idesc_bf16(kTcRows, kTcKeys, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(kTcRows, kTcD, 1);
-static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
+
+// Shared-memory plan and block size of the bf16-cache (false) and FP8-cache (true) kernels.
+template <bool kFp8>
+struct TcCfg {
+  static constexpr int kStages = kFp8 ? 3 : kTcStages;      // bf16 K/V ring
+  static constexpr int kThreads = kTcThreads + (kFp8 ? 32 * kCvtWarps : 0);
+  static constexpr uint32_t kOffF8 = kOffKV + kStages * kStageBytes;
+  static constexpr uint32_t kOffBar = kOffF8 + (kFp8 ? kF8Stages * kF8Stage : 0);
+  static constexpr uint32_t kSmem = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static constexpr int kFullCount = kFp8 ? kCvtWarps : 1;   // arrivals that fill a bf16 stage
+};
+static_assert(TcCfg<false>::kSmem <= 232448 && TcCfg<true>::kSmem <= 232448, "shared memory over the per-CTA limit");
 
 struct TcParams {
   const int32_t* page_table;
@@ -79,15 +101,18 @@ struct TcParams {
   uint4* part_o;       // split partials [tile group][S][128 rows][16 chunks]: O / l in bf16, 8 per chunk,
                        // chunk c of row r at position c ^ (r % 16)
   float* part_lse;     // [tile group][S][128 rows]: log2-sum-exp of the split's scores (-inf: empty)
+  const float* kv_scale;  // FP8 cache: [2][Hkv] K then V scales (unused with a bf16 cache)
   int32_t* status;
 };
 
 struct TcBars {
   uint64_t q_full, kv_full[kTcStages], kv_empty[kTcStages];
   uint64_t s_full[kTiles][2], p_full[kTiles], pv_done[kTiles], mma_fin[kTiles];
+  uint64_t f8_full[kF8Stages], f8_empty[kF8Stages];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(TcBars) <= 256, "barrier block over its reserved bytes");
 
 // One lane waits, the whole warp gets the answer: keeps warp-collective tcgen05.ld/st
 // and __syncwarp on a converged warp even when a wait gives up.
@@ -100,6 +125,28 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Four E4M3 codes (byte i = element i) -> four bf16 (lo: elements 0, 1; hi: 2, 3), exactly.
+// One byte permute puts each code in the low byte of a 16-bit lane with its sign replicated
+// in the high byte; a shift and a mask then leave s | eeee << 7 | mmm << 4, the bf16 whose
+// value is the code's times 2^-120 (the exponent biases, 127 and 7, differ by 120; zero and
+// the subnormals line up as zero and subnormals). One packed bf16 multiply by 2^120 gives
+// the value: every E4M3 value is a bf16 value, so the product is exact. (A NaN code, which
+// a cache does not hold, reads as +-480.)
+__device__ __forceinline__ uint32_t e4m3x2_lanes_to_bf16x2(uint32_t h) {
+  const uint32_t x = (h << 4) & 0x87F087F0u;
+  uint32_t y;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(x), "r"(0x7B807B80u));  // 2^120 in both lanes
+  return y;
+}
+
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(w));  // [sgn b1, b1, sgn b0, b0]
+  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(w));  // [sgn b3, b3, sgn b2, b2]
+  lo = e4m3x2_lanes_to_bf16x2(a);
+  hi = e4m3x2_lanes_to_bf16x2(b);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -135,13 +182,16 @@ __device__ __forceinline__ TcSplit tc_split(int P, int N, int splits, int s) {
   return r;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <bool kFp8>
+__global__ void __launch_bounds__(TcCfg<kFp8>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
                    const __grid_constant__ CUtensorMap tm_vt, const TcParams p) {
+  using Cfg = TcCfg<kFp8>;
+  constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  TcBars& bars = *reinterpret_cast<TcBars*>(smem + kOffBar);
+  TcBars& bars = *reinterpret_cast<TcBars*>(smem + Cfg::kOffBar);
   const uint32_t s_base = tc::smem_u32(smem);
 
   const int split = blockIdx.x, pair = blockIdx.y, bg = blockIdx.z;
@@ -195,6 +245,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto bar_sf = [&](int t, int s) { return tc::smem_u32(&bars.s_full[t][s]); };
     auto bar_pf = [&](int t) { return tc::smem_u32(&bars.p_full[t]); };
     auto bar_pv = [&](int t) { return tc::smem_u32(&bars.pv_done[t]); };
+    auto bar_f8f = [&](int s) { return tc::smem_u32(&bars.f8_full[s]); };
+    auto bar_f8e = [&](int s) { return tc::smem_u32(&bars.f8_empty[s]); };
     volatile int* abort = &bars.abort;
 
     // Page ids of the producer's next 8 blocks, one per lane (lane l: block 8k + l/4,
@@ -214,16 +266,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     int pg_cur = 0, pg_nxt = 0;
 
-    // K/V block j into ring stage j % kTcStages (the warp's lanes each issue one copy);
-    // called for j = 0, 1, 2, ... in order by the whole producer warp
+    // K/V block j into ring stage j % kStages (the warp's lanes each issue one copy);
+    // called for j = 0, 1, 2, ... in order by the whole producer warp. With an FP8 cache the
+    // producer loads only the prefix blocks, into code stage j % kF8Stages; the converter
+    // warps fill every bf16 stage (the tree blocks by TMA), so each ring has one filler that
+    // waits for every phase of its "empty" barriers in order (a filler running two uses
+    // ahead of a barrier would pass a parity wait one phase early).
     auto load_block = [&](int j) {
-      const int st = j % kTcStages;
+      const int st = j % kStages;
       const uint32_t dst0 = s_base + kOffKV + st * kStageBytes;
       if ((j & 7) == 0 && j > 0) {
         pg_cur = pg_nxt;
         pg_nxt = fetch_pages((j >> 3) + 1);
       }
       const int page_here = __shfl_sync(0xffffffffu, pg_cur, ((j & 7) << 2) + ((lane >> 2) & 3));
+      if (kFp8 && j < npb) {
+        const int s8 = j % kF8Stages;
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar_f8f(s8), kF8Stage);
+        __syncwarp();
+        if (lane < 16 && (lane & 3) < 2) {  // page lane >> 2, K (lane & 1 == 0) or V
+          const int pp = lane >> 2, isv = lane & 1;
+          const uint32_t dst = s_base + Cfg::kOffF8 + s8 * kF8Stage + isv * (kF8Stage / 2) + pp * 2048;
+          tc::tma_load_4d(dst, isv ? &tm_vp : &tm_kp, bar_f8f(s8), 0, 0, g, page_here);
+        }
+        return;
+      }
       if (lane == 0) tc::mbar_arrive_expect_tx(bar_kvf(st), kStageBytes);
       __syncwarp();
       if (j < npb) {
@@ -248,10 +315,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       pg_nxt = fetch_pages(1);
       if (lane == 0) {
         tc::mbar_init(bar_q, 1);
-        for (int s = 0; s < kTcStages; ++s) {
-          tc::mbar_init(bar_kvf(s), 1);
+        for (int s = 0; s < kStages; ++s) {
+          tc::mbar_init(bar_kvf(s), Cfg::kFullCount);
           tc::mbar_init(bar_kve(s), ntiles);  // released by each tile's PV
         }
+        if (kFp8)
+          for (int s = 0; s < kF8Stages; ++s) {
+            tc::mbar_init(bar_f8f(s), 1);
+            tc::mbar_init(bar_f8e(s), kCvtWarps);  // released by each converter warp
+          }
         for (int t = 0; t < kTiles; ++t) {
           tc::mbar_init(bar_sf(t, 0), 1);
           tc::mbar_init(bar_sf(t, 1), 1);
@@ -269,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       __syncwarp();
-      load_block(0);
+      if (!kFp8 || npb > 0) load_block(0);
     } else if (warp == 1) {
       tc::tmem_alloc(tc::smem_u32(&bars.tmem_base), kTmemCols);
       tc::tmem_relinquish();
@@ -281,23 +353,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
       // ---------------------------------------------------------------- TMA producer
-      int issued = 1;
-      for (int j = 1; j < nb; ++j) {
-        if (!warp_wait(bar_kve(j % kTcStages), ((j / kTcStages) & 1) ^ 1, abort)) {
+      const int n_own = kFp8 ? npb : nb;  // blocks this warp loads
+      int issued = n_own > 0 ? 1 : 0;
+      for (int j = 1; j < n_own; ++j) {
+        const uint32_t bar_free = kFp8 ? bar_f8e(j % kF8Stages) : bar_kve(j % kStages);
+        const int parity = kFp8 ? ((j / kF8Stages) & 1) ^ 1 : ((j / kStages) & 1) ^ 1;
+        if (!warp_wait(bar_free, parity, abort)) {
           if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
           break;
         }
         load_block(j);
         issued = j + 1;
       }
-      // leave no copy in flight: the last stages issued must have landed
+      // leave no copy in flight: the last stages issued must have landed (the last
+      // kF8Stages code stages, or the last kStages bf16 stages, are all distinct)
       if (lane == 0 && *abort) {
         int zero = 0;
-        for (int j = max(0, issued - kTcStages); j < issued; ++j)
-          tc::mbar_wait(bar_kvf(j % kTcStages), (j / kTcStages) & 1, &zero, kWaitLimit);
+        const int win = kFp8 ? kF8Stages : kStages;
+        for (int j = max(0, issued - win); j < issued; ++j) {
+          if (kFp8) tc::mbar_wait(bar_f8f(j % kF8Stages), (j / kF8Stages) & 1, &zero, kWaitLimit);
+          else tc::mbar_wait(bar_kvf(j % kStages), (j / kStages) & 1, &zero, kWaitLimit);
+        }
         tc::mbar_wait(bar_q, 0, &zero, kWaitLimit);
       }
-    } else if (warp == 1 || warp == kTcThreads / 32 - 1) {
+    } else if (warp == 1 || warp == kMma1Warp) {
       // ---------------------------------------------------------------- MMA issuers
       // One issuing thread per M-tile (warp 1: tile 0, the last warp: tile 1): a thread
       // issues one tcgen05.mma about every 100 cycles whatever the shape, so two issuers
@@ -306,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0 && t < ntiles) {
         const uint32_t qbuf = s_base + kOffQ + t * kQTile;
         auto qk = [&](int j) {
-          const uint32_t kbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes;
+          const uint32_t kbuf = s_base + kOffKV + (j % kStages) * kStageBytes;
 #pragma unroll
           for (int k = 0; k < kTcD / 16; ++k) {
             const uint64_t a = tc::sdesc_sw128(qbuf + (k >> 2) * kQSlab + (k & 3) * 32, 16, 1024);
@@ -323,15 +402,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int j = 0; ok && j < nb; ++j) {
           if (j + 1 < nb) {  // S of the next block while the softmax works on this one
-            const int st = (j + 1) % kTcStages;
-            if (!tc::mbar_wait(bar_kvf(st), ((j + 1) / kTcStages) & 1, abort, kWaitLimit)) {
+            const int st = (j + 1) % kStages;
+            if (!tc::mbar_wait(bar_kvf(st), ((j + 1) / kStages) & 1, abort, kWaitLimit)) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
             qk(j + 1);
           }
-          const uint32_t vbuf = s_base + kOffKV + (j % kTcStages) * kStageBytes + 2 * kKVSlab;
+          const uint32_t vbuf = s_base + kOffKV + (j % kStages) * kStageBytes + 2 * kKVSlab;
           if (!tc::mbar_wait(bar_pf(t), j & 1, abort, kWaitLimit)) {
             ok = false;
             break;
@@ -346,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             (j > 0 || k > 0) ? 1u : 0u);
           }
           tc::mma_commit(bar_pv(t));
-          tc::mma_commit(bar_kve(j % kTcStages));
+          tc::mma_commit(bar_kve(j % kStages));
         }
         if (!ok) report(p.status, SPEC_ERR_TIMEOUT);
         // every MMA this thread issued has completed before TMEM is released
@@ -356,11 +435,92 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::mbar_wait(bar_fin, 0, &zero, kWaitLimit);
       }
       __syncwarp();
+    } else if (kFp8 && warp >= kTcThreads / 32) {
+      // ---------------------------------------------------------------- FP8 converters
+      // The four warps fill every bf16 stage, block by block; each warp first waits for the
+      // stage's previous use to be consumed (every phase in order), then adds its arrival.
+      // Prefix block j: its 16 KB of codes (TMA, 128-byte swizzle: 16-byte chunk c of key
+      // row r at c ^ (r % 8)) become the bf16 stage the MMAs read (slab d / 64, row r,
+      // chunk (d % 64) / 8 at chunk ^ (r % 8)). A thread widens one 16-code chunk into two
+      // bf16 chunks per step; the 8 lanes of a quarter-warp take 8 consecutive rows, so
+      // their loads and stores land in 8 distinct bank groups. Tree block j: the first
+      // converter warp TMA-loads the bf16 rows (expecting their bytes), the others arrive.
+      const int ct = threadIdx.x - kTcThreads;
+      const bool tma_warp = warp == kTcThreads / 32;
+      int tree_issued = npb;  // tree blocks npb .. tree_issued - 1 were loaded by this warp
+      for (int j = 0; j < nb; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !warp_wait(bar_kve(st), ((j / kStages) & 1) ^ 1, abort)) {
+          if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
+          break;
+        }
+        if (j >= npb) {
+          if (tma_warp) {
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar_kvf(st), kStageBytes);
+            __syncwarp();
+            if (lane < 4) {
+              const int tb = sr.tb_lo + (j - npb);
+              const int slab = lane & 1, isv = lane >> 1;
+              const uint32_t dst = s_base + kOffKV + st * kStageBytes + isv * 2 * kKVSlab + slab * kKVSlab;
+              tc::tma_load_3d(dst, isv ? &tm_vt : &tm_kt, bar_kvf(st), slab * 64, g, base + tb * 64);
+            }
+            tree_issued = j + 1;
+          } else if (lane == 0) {
+            tc::mbar_arrive(bar_kvf(st));
+          }
+          continue;
+        }
+        const int s8 = j % kF8Stages;
+        if (!warp_wait(bar_f8f(s8), (j / kF8Stages) & 1, abort)) {
+          if (lane == 0) report(p.status, SPEC_ERR_TIMEOUT);
+          break;
+        }
+        const uint8_t* src = smem + Cfg::kOffF8 + s8 * kF8Stage;
+        uint8_t* dst = smem + kOffKV + st * kStageBytes;
+#pragma unroll
+        for (int it = 0; it < (int)(kF8Stage / 16) / (32 * kCvtWarps); ++it) {
+          const int id = it * (32 * kCvtWarps) + ct;
+          const int isv = id >> 9, cid = id & 511;
+          const int r = (cid & 7) | ((cid >> 6) << 3);  // key row of the block
+          const int cc = (cid >> 3) & 7;                // codes 16 cc .. 16 cc + 15
+          const uint4 w = *reinterpret_cast<const uint4*>(src + isv * (kF8Stage / 2) + r * 128 + ((cc ^ (r & 7)) << 4));
+          uint4 a, b2;
+          e4m3x4_to_bf16x4(w.x, a.x, a.y);
+          e4m3x4_to_bf16x4(w.y, a.z, a.w);
+          e4m3x4_to_bf16x4(w.z, b2.x, b2.y);
+          e4m3x4_to_bf16x4(w.w, b2.z, b2.w);
+          uint8_t* row = dst + isv * 2 * kKVSlab + (cc >> 2) * kKVSlab + r * 128;
+          const int ch = (cc & 3) * 2;
+          *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = a;
+          *reinterpret_cast<uint4*>(row + (((ch + 1) ^ (r & 7)) << 4)) = b2;
+        }
+        tc::fence_proxy_async_smem();  // the tensor cores read these stores through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(bar_kvf(st));
+          tc::mbar_arrive(bar_f8e(s8));
+        }
+      }
+      // leave no tree copy in flight (the last kStages blocks use distinct stages)
+      if (tma_warp && lane == 0 && *abort) {
+        int zero = 0;
+        for (int j = max(npb, tree_issued - kStages); j < tree_issued; ++j)
+          tc::mbar_wait(bar_kvf(j % kStages), (j / kStages) & 1, &zero, kWaitLimit);
+      }
     } else if (tile < ntiles) {
       // ---------------------------------------------------------------- softmax warps
       const uint32_t t_lane = tbase + tile * 256 + ((uint32_t)((warp & 3) * 32) << 16);
       const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
       const float sl2 = p.scale_log2;
+      // FP8 cache: prefix scores scale by the K scale; prefix P carries the V scale in its
+      // exponent and its row sum is divided by it
+      float sl2_pre = sl2, lvs_pre = 0.f, ivs_pre = 1.f;
+      if (kFp8) {
+        const float ks = __ldg(p.kv_scale + g), vs = __ldg(p.kv_scale + p.hkv + g);
+        sl2_pre = sl2 * ks;
+        lvs_pre = log2f(vs);
+        ivs_pre = 1.f / vs;
+      }
       float m_run = -INFINITY, l = 0.f;
       bool ok = true;
       // the first tree block's mask word, fetched while the prefix blocks stream (the mask
@@ -400,7 +560,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mx2 = fmaxf(mx2, sv[c + 2]);
           mx3 = fmaxf(mx3, sv[c + 3]);
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;  // sm_scale > 0
+        const bool pre8 = kFp8 && j < npb;
+        const float sc = pre8 ? sl2_pre : sl2;
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;  // sm_scale, scales > 0
         float alpha = 1.f;
         bool rescale = false;
         if (mx > -INFINITY && (m_run == -INFINITY || mx > m_run + kRescaleThr)) {
@@ -408,15 +570,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m_run = mx;
           rescale = j > 0;
         }
-        const float negm = m_run == -INFINITY ? 0.f : -m_run;  // all scores are -inf then
+        float negm = m_run == -INFINITY ? 0.f : -m_run;  // all scores are -inf then
+        if (pre8) negm += lvs_pre;
         uint32_t packed[kTcKeys / 2];
         float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
         for (int c = 0; c < kTcKeys; c += 4) {
-          const float p0 = ex2_approx(fmaf(sv[c], sl2, negm));
-          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, negm));
-          const float p2 = ex2_approx(fmaf(sv[c + 2], sl2, negm));
-          const float p3 = ex2_approx(fmaf(sv[c + 3], sl2, negm));
+          const float p0 = ex2_approx(fmaf(sv[c], sc, negm));
+          const float p1 = ex2_approx(fmaf(sv[c + 1], sc, negm));
+          const float p2 = ex2_approx(fmaf(sv[c + 2], sc, negm));
+          const float p3 = ex2_approx(fmaf(sv[c + 3], sc, negm));
           r0 += p0;
           r1 += p1;
           r2 += p2;
@@ -424,7 +587,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           packed[c >> 1] = pack_bf16x2(p0, p1);
           packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
         }
-        l = l * alpha + ((r0 + r1) + (r2 + r3));
+        float rsum = (r0 + r1) + (r2 + r3);
+        if (pre8) rsum *= ivs_pre;
+        l = l * alpha + rsum;
         if (j >= 1) {  // PV of the previous block done: O is stable
           if (!warp_wait(bar_pv(tile), (j - 1) & 1, abort)) {
             ok = false;
@@ -600,15 +765,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle, zero fill out of bounds; dims/box innermost first.
-static bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                        const cuuint32_t* box) {
+// Tensor map with 128-byte swizzle and zero fill out of bounds; dims/box innermost first.
+static bool encode_tiled(CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(m, type, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                        const cuuint32_t* box) {
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
 }
 
 bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max_nodes) {
@@ -671,8 +841,9 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                    const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
                    int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
-                   void* ws, int32_t* status, cudaStream_t stream) {
+                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale) {
   (void)ps;
+  const bool fp8 = kv_scale != nullptr;
   (void)d;
   const int G = hq / hkv;
   CUtensorMap tm_q, tm_kp, tm_vp, tm_kt, tm_vt;
@@ -689,22 +860,32 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
     if (!encode_bf16(&tm_kt, k_tree, 3, dims, str, box)) return SPEC_ERR_CUDA;
     if (!encode_bf16(&tm_vt, v_tree, 3, dims, str, box)) return SPEC_ERR_CUDA;
   }
-  if (max_prefix > 0 && num_pages > 0 && k_pool != nullptr && v_pool != nullptr) {
+  if (max_prefix > 0 && num_pages > 0 && k_pool != nullptr && v_pool != nullptr && !fp8) {
     const cuuint64_t dims[4] = {(cuuint64_t)kTcD, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
     const cuuint64_t str[3] = {(cuuint64_t)kTcD * 2, (cuuint64_t)16 * kTcD * 2, (cuuint64_t)hkv * 16 * kTcD * 2};
     const cuuint32_t box[4] = {64, 16, 1, 1};
     if (!encode_bf16(&tm_kp, k_pool, 4, dims, str, box)) return SPEC_ERR_CUDA;
     if (!encode_bf16(&tm_vp, v_pool, 4, dims, str, box)) return SPEC_ERR_CUDA;
+  } else if (max_prefix > 0 && num_pages > 0 && k_pool != nullptr && v_pool != nullptr) {
+    // E4M3 codes: one 16-token x 128-code tile (2 KB) per (page, head), 128-byte rows
+    const cuuint64_t dims[4] = {(cuuint64_t)kTcD, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    const cuuint64_t str[3] = {(cuuint64_t)kTcD, (cuuint64_t)16 * kTcD, (cuuint64_t)hkv * 16 * kTcD};
+    const cuuint32_t box[4] = {(cuuint32_t)kTcD, 16, 1, 1};
+    if (!encode_tiled(&tm_kp, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 4, dims, str, box)) return SPEC_ERR_CUDA;
+    if (!encode_tiled(&tm_vp, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 4, dims, str, box)) return SPEC_ERR_CUDA;
   } else {  // no prefix anywhere: the pool maps are never used
     tm_kp = tm_kt;
     tm_vp = tm_vt;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return SPEC_ERR_CUDA;
-    attr_set = true;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[fp8]) {
+    const cudaError_t e =
+        fp8 ? cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   TcCfg<true>::kSmem)
+            : cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   TcCfg<false>::kSmem);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    attr_set[fp8] = true;
   }
   const int splits = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
   const int mtiles = tc_mtiles(max_nodes, G);
@@ -729,11 +910,12 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   uint8_t* wb = static_cast<uint8_t*>(ws);
   prm.part_o = splits > 1 ? reinterpret_cast<uint4*>(wb + w.o) : nullptr;
   prm.part_lse = splits > 1 ? reinterpret_cast<float*>(wb + w.ml) : nullptr;
+  prm.kv_scale = kv_scale;
   prm.status = status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(splits, ceil_div(mtiles, kTiles), batch * hkv);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(fp8 ? TcCfg<true>::kThreads : TcCfg<false>::kThreads);
+  cfg.dynamicSmemBytes = fp8 ? TcCfg<true>::kSmem : TcCfg<false>::kSmem;
   cfg.stream = stream;
   // programmatic serialization: the prologue (barriers, TMEM, Q and first K/V loads)
   // overlaps the mask kernel; the softmax waits for it before the first tree block
@@ -742,8 +924,9 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_tc_kernel, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm) != cudaSuccess)
-    return SPEC_ERR_CUDA;
+  const cudaError_t le = fp8 ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm)
+                            : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm);
+  if (le != cudaSuccess) return SPEC_ERR_CUDA;
   if (splits > 1) {
     TcMergeParams mp;
     mp.part_o = prm.part_o;

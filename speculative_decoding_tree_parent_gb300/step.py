@@ -21,8 +21,11 @@ def _t(a, dtype, device):
 class DeviceBatch:
     """Device-resident buffers of one batch and the calls of one verification step."""
 
-    def __init__(self, inp, device="cuda", mode=None, pool_dtype=None):
+    def __init__(self, inp, device="cuda", mode=None, kv_fp8=False):
+        """kv_fp8: hold the paged pool as E4M3 codes with per-KV-head scales
+        (workloads.fp8_pool) and run the FP8-cache attention and commit calls."""
         self.inp = inp
+        self.kv_fp8 = bool(kv_fp8)
         self.device = device
         fdt = torch.float32 if inp.dtype == "f32" else torch.bfloat16
         self.fdt = fdt
@@ -34,8 +37,17 @@ class DeviceBatch:
         self.q = _t(inp.q, fdt, dev)
         self.k_tree = _t(inp.k_tree, fdt, dev)
         self.v_tree = _t(inp.v_tree, fdt, dev)
-        self.k_pool = _t(inp.k_pool, fdt, dev)
-        self.v_pool = _t(inp.v_pool, fdt, dev)
+        if self.kv_fp8:
+            from .workloads import fp8_pool
+            kc, vc, sc = fp8_pool(inp)
+            self.k_pool = _t(kc, torch.uint8, dev)
+            self.v_pool = _t(vc, torch.uint8, dev)
+            self.kv_scale = _t(sc, torch.float32, dev)
+            self.kv_codes = (kc, vc, sc)
+        else:
+            self.k_pool = _t(inp.k_pool, fdt, dev)
+            self.v_pool = _t(inp.v_pool, fdt, dev)
+            self.kv_scale = None
         self.page_table = _t(inp.page_table, torch.int32, dev)
         self.prefix_len = _t(inp.prefix_len, torch.int32, dev)
         self.target_logits = _t(inp.target_logits, torch.float32, dev)
@@ -93,6 +105,11 @@ class DeviceBatch:
                                       stream)
 
     def attention(self, stream=None, sm_scale=0.0):
+        if self.kv_fp8:
+            return B.spec_tree_verify_attn_kv8(self.q, self.k_pool, self.v_pool, self.kv_scale, self.page_table,
+                                               self.prefix_len, self.max_prefix, self.k_tree, self.v_tree,
+                                               self.mask, self.qo, self.max_nodes, self.out, self.lse, self.attn_ws,
+                                               sm_scale, self.status, stream)
         return B.spec_tree_verify_attn(self.q, self.k_pool, self.v_pool, self.page_table, self.prefix_len,
                                        self.max_prefix, self.k_tree, self.v_tree, self.mask, self.qo,
                                        self.max_nodes, self.out, self.lse, self.attn_ws, sm_scale, self.status,
@@ -108,12 +125,19 @@ class DeviceBatch:
                              flags=self.flags, dev_status=self.status, stream=stream)
 
     def commit(self, stream=None):
+        if self.kv_fp8:
+            return B.spec_kv_commit_kv8(self.k_tree, self.v_tree, self.kv_scale, self.path, self.accept_len, self.qo,
+                                        self.page_table, self.prefix_len, self.k_pool, self.v_pool, self.seq_len,
+                                        self.status, stream)
         return B.spec_kv_commit(self.k_tree, self.v_tree, self.path, self.accept_len, self.qo, self.page_table,
                                 self.prefix_len, self.k_pool, self.v_pool, self.seq_len, self.status, stream)
 
     def accept_commit(self, mode=None, stream=None):
-        """spec_accept then spec_kv_commit, as the one fused call."""
+        """spec_accept then spec_kv_commit, as the one fused call (two calls with an FP8 cache)."""
         mode = mode or self.mode
+        if self.kv_fp8:
+            self.accept(mode, stream)
+            return self.commit(stream)
         m = B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY
         return B.spec_accept_commit(m, self.parent, self.tokens, self.target_logits, self.qo, self.max_nodes,
                                     self.accept_len, self.path, self.out_tokens, self.acc_ws, self.k_tree,
@@ -137,12 +161,12 @@ class DeviceBatch:
     def launches_per_step(self, mode=None, fused=True):
         """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the keys are
         split), then accept 1 (greedy) or 2 (stochastic) and commit 1 -- except that the fused
-        greedy call of up to 4 sequences commits inside its acceptance kernel."""
+        greedy call of up to 4 sequences commits inside its acceptance kernel (bf16 cache)."""
         mode = mode or self.mode
         splits, _ = self.attn_plan()
         attn = 2 if splits > 1 else 1
         acc = 2 if mode == "stochastic" else 1
-        commit = 0 if (fused and mode != "stochastic" and self.B <= 4) else 1
+        commit = 0 if (fused and mode != "stochastic" and self.B <= 4 and not self.kv_fp8) else 1
         return 1 + attn + acc + commit
 
     def attn_plan(self):

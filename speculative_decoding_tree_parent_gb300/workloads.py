@@ -433,3 +433,21 @@ def subset(inp: VerifyInputs, seqs: Sequence[int]) -> VerifyInputs:
         draft_logits=pick(inp.draft_logits),
         uniforms=pick(inp.uniforms),
     )
+
+
+def fp8_pool(inp: VerifyInputs):
+    """Input for the FP8-cache calls: (k_codes, v_codes, kv_scale) drawn from the workload's
+    own pool. kv_scale float32 [2, Hkv] is each KV head's largest |value| / 448 (K, then V);
+    the codes (uint8, the pool's shape) are torch's float8_e4m3fn cast of value / scale, a
+    library routine used here only to lay out test data."""
+    import torch
+
+    scales = []
+    codes = []
+    for pool in (inp.k_pool, inp.v_pool):
+        amax = np.abs(pool).max(axis=(0, 2, 3)).astype(np.float32)
+        s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        x = torch.from_numpy(np.ascontiguousarray(pool, np.float32) / s[None, :, None, None])
+        codes.append(x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        scales.append(s)
+    return codes[0], codes[1], np.stack(scales).astype(np.float32)
