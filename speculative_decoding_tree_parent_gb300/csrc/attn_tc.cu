@@ -803,16 +803,38 @@ static int sm_count() {
 
 static int tc_mtiles(int max_nodes, int G) { return ceil_div(max_nodes * G, kTcRows); }
 
-// Key splits per CTA work item (sequence, KV head, pair of M-tiles): enough that the
-// items x splits CTAs (one per SM: 225 KB of shared memory each) cover the SMs when the
-// batch alone does not, never more CTAs than SMs (the split merge needs them all
-// resident), at least two key blocks per split, at most 32 splits.
+// Key splits per CTA work item (sequence, KV head, pair of M-tiles), from the sizes alone
+// (the per-sequence lengths stay on the device). One CTA fits on an SM (over 197 KB of
+// shared memory).
+// - Fewer items than SMs: enough splits that the items x splits CTAs cover the SMs, never
+//   more CTAs than SMs.
+// - Otherwise the CTAs run in waves. The count S in 1..8 minimises
+//   ceil(items * S / SMs) * (ceil(blocks / S) + 4), where blocks = the longest sequence's
+//   key blocks and 4 blocks stand for a CTA's fixed cost (prologue, partials, merge share).
+//   A batch of long sequences of equal length then stops losing its last, partly filled
+//   wave.
+// At least two key blocks per split, at most 32 splits. The split merge waits for the
+// whole attention grid (programmatic launch releases it only once every attention CTA
+// has started), so any number of waves is safe.
 int attn_splits_tc(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
   if (hkv <= 0 || hq % hkv) return 1;
   const int G = hq / hkv;
   const long items = (long)batch * hkv * ceil_div(tc_mtiles(max_nodes, G), kTiles);
   const int blocks = ceil_div(max_prefix, kTcKeys) + ceil_div(max_nodes, kTcKeys);
-  long s = items > 0 ? sm_count() / items : 1;
+  const long sms = sm_count();
+  long s = 1;
+  if (items > 0 && items < sms) {
+    s = sms / items;
+  } else if (items > 0) {
+    long best = -1;
+    for (long c = 1; c <= 8; ++c) {
+      const long cost = ((items * c + sms - 1) / sms) * ((blocks + c - 1) / c + 4);
+      if (best < 0 || cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
+  }
   if (s > blocks / 2) s = blocks / 2;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : (int)s;
