@@ -618,6 +618,14 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
 
 // ---------------------------------------------------------------- stochastic: statistics
 
+// 2^x by the hardware approximation (used on the statistics pass, where every value of a
+// chunk is exponentiated once)
+__device__ __forceinline__ float ex2a(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Online max / compensated sum of exp((x - m) * invT) over a stream of values.
 struct OnlineExp {
   float m = -INFINITY, s = 0.f, comp = 0.f;
@@ -684,24 +692,28 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
       mp = fmaxf(mp, fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w)));
       mq = fmaxf(mq, fmaxf(fmaxf(d[u].x, d[u].y), fmaxf(d[u].z, d[u].w)));
     }
+    // one ex2.approx per value of (x - m) / T in log2 units: x - m first, so the terms near
+    // the max keep their exponent exactly; a term's relative error is then that of
+    // ex2.approx (a few parts in 10^7), and the sums stay compensated
+    const float k2 = invT * 1.4426950408889634f;  // log2(e) / T
     if (mp != -INFINITY) {
       ep.m = mp;
 #pragma unroll
       for (int u = 0; u < kVecPerThread; ++u) {
-        ep.kahan(expf((a[u].x - mp) * invT));
-        ep.kahan(expf((a[u].y - mp) * invT));
-        ep.kahan(expf((a[u].z - mp) * invT));
-        ep.kahan(expf((a[u].w - mp) * invT));
+        ep.kahan(ex2a((a[u].x - mp) * k2));
+        ep.kahan(ex2a((a[u].y - mp) * k2));
+        ep.kahan(ex2a((a[u].z - mp) * k2));
+        ep.kahan(ex2a((a[u].w - mp) * k2));
       }
     }
     if (mq != -INFINITY) {
       eq.m = mq;
 #pragma unroll
       for (int u = 0; u < kVecPerThread; ++u) {
-        eq.kahan(expf((d[u].x - mq) * invT));
-        eq.kahan(expf((d[u].y - mq) * invT));
-        eq.kahan(expf((d[u].z - mq) * invT));
-        eq.kahan(expf((d[u].w - mq) * invT));
+        eq.kahan(ex2a((d[u].x - mq) * k2));
+        eq.kahan(ex2a((d[u].y - mq) * k2));
+        eq.kahan(ex2a((d[u].z - mq) * k2));
+        eq.kahan(ex2a((d[u].w - mq) * k2));
       }
     }
   } else {
