@@ -262,15 +262,23 @@ def run_ours(args):
                 getattr(rep, name)(mode) if name in ("accept", "accept_commit") else getattr(rep, name)()
         return run
 
+    # the step: mask, attention, fused acceptance + commit. The attention that builds the
+    # mask itself (spec_tree_verify_attn_parents) is timed per call beside it; in a step the
+    # separate mask kernel overlaps the attention's prologue and is the faster of the two.
     g_step = capture(lambda: [rep.step(mode) for rep in reps])
     g_calls = {"mask": capture(over_reps("build_mask")), "attention": capture(over_reps("attention")),
                "accept": capture(over_reps("accept")), "commit": capture(over_reps("commit")),
                "accept_commit": capture(over_reps("accept_commit"))}
+    with_parents = db.fused_mask_ok()
+    if with_parents:
+        g_calls["attention_parents"] = capture(over_reps("attention_parents"))
     launches = db.launches_per_step(mode)
     splits, tc = db.attn_plan()
     attn_launches = 2 if splits > 1 else 1
     # per-call graphs: mask 1, attention, accept (1 greedy, 2 stochastic), commit 1, fused call
-    call_launches = 1 + attn_launches + (2 if mode == "stochastic" else 1) + 1 + (launches - 1 - attn_launches)
+    # (+ the attention with the mask inside)
+    call_launches = 1 + attn_launches + (2 if mode == "stochastic" else 1) + 1 + \
+        (launches - 1 - attn_launches) + (attn_launches if with_parents else 0)
     # the same attention over an FP8 (E4M3) copy of the pool, on its own replicas (tensor-core
     # shapes only): prefix K/V bytes halve
     reps8 = []
@@ -463,6 +471,7 @@ def run_ours(args):
                          f"({R} x {wc['attn_bytes'] + wc['accept_bytes'] >> 20} MB); L2 also flushed before each replay "
                          f"(a 256 MB buffer written, then read back, so no dirty flush lines remain)",
                    "timing": f"CUDA-graph replay of {R} steps, CUDA events on the launching stream",
+                   "step": "mask, attention, acceptance + KV commit",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
         "attn": {"tokens_per_s": wc["tokens"] / t_attn, "tflops": attn_tflops, "gbs": attn_gbs,
                  "roofline_frac": attn_roof, "us": t_attn * 1e6, "flops": wc["attn_flops"],
@@ -472,6 +481,7 @@ def run_ours(args):
                           "separate_us": (t_acc + t_com) * 1e6, "gbs": accom_gbs, "hbm_frac": accom_gbs / hbm,
                           "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
         "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
+        "attn_with_mask_us": statistics.mean(call_ms["attention_parents"]) * 1e3 if with_parents else None,
         "attn_fp8kv": attn8,
         "draft_tree": tree,
         "roofline": roof,

@@ -350,6 +350,31 @@ int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_to
                         void* stream);
 
 /*
+ * spec_tree_verify_attn_parents — spec_tree_verify_attn with the tree given as its parent
+ *   array instead of a mask: the mask step runs inside the attention call.
+ *   ("EAGLE-2 deep dive", core-implementation section: a node's mask row is the node and
+ *   every ancestor up to the root.)
+ *   Arguments: those of spec_tree_verify_attn, minus dtype (bf16 only) and mask, plus
+ *   parent  int32 [total_nodes]  sequence-local parents, as for spec_build_tree_mask.
+ *   The result equals spec_build_tree_mask followed by spec_tree_verify_attn on the same
+ *   stream: for each in-tree key block, every query row derives its ancestor bits by
+ *   walking parent links (staged in shared memory), with no mask buffer in between.
+ *   - Device error SPEC_ERR_PARENT for a parent array that is not a tree; the affected
+ *     rows then see no tree keys.
+ *   - The tensor-core path only: d = 128, page_size = 16, hq / hkv dividing 128; other
+ *     shapes return SPEC_ERR_UNSUPPORTED (use the two calls).
+ *   - The parent array is read after the PDL wait, so it may come from the kernel just
+ *     before. No depth output.
+ */
+int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                                  int page_size, const int32_t* page_table, int max_pages,
+                                  const int32_t* prefix_len, int max_prefix, const void* k_tree,
+                                  const void* v_tree, const int32_t* parent, const int32_t* qo_indptr,
+                                  int batch, int total_nodes, int max_nodes, int hq, int hkv, int d,
+                                  float sm_scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * FP8 KV cache: spec_tree_verify_attn_kv8 / spec_kv_commit_kv8.
  *   ("EAGLE-3 paper explainer" (0h-n0), operations section, model-optimisation list:
  *   quantisation and PagedAttention KV-cache tuning to cut GPU memory. The page names no

@@ -26,7 +26,8 @@ STATUS = {
 }
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
            "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
-           "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8")
+           "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8",
+           "spec_tree_verify_attn_parents")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -47,6 +48,8 @@ _SIGS = {
                               _P, _P, _P, _P, _P, _P, _P]),
     "spec_tree_verify_attn_kv8": (_I, [_P, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                        _I, _F, _P, _P, _P, _Z, _P, _P]),
+    "spec_tree_verify_attn_parents": (_I, [_P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                           _I, _F, _P, _P, _P, _Z, _P, _P]),
     "spec_kv_commit_kv8": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 
@@ -263,3 +266,20 @@ def spec_kv_commit_kv8(k_tree, v_tree, kv_scale, path, accept_len, qo_indptr, pa
         _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
         _ptr(v_pool), qo_indptr.numel() - 1, T, hkv, d, _ptr(dev_status), _stream(stream))
     return _check(st, "spec_kv_commit_kv8")
+
+
+def spec_tree_verify_attn_parents(q, k_pool, v_pool, page_table, prefix_len, max_prefix, k_tree, v_tree, parent,
+                                  qo_indptr, max_nodes, out, lse=None, ws=None, sm_scale=0.0, dev_status=None,
+                                  stream=None):
+    """Tree-verify attention with the ancestor bits built in-kernel from the parent array
+    (bf16, tensor-core shapes)."""
+    _need(q, torch.bfloat16, "q")
+    _need(parent, torch.int32, "parent")
+    T, hq, d = q.shape
+    num_pages, hkv, ps, _ = k_pool.shape
+    st = load().spec_tree_verify_attn_parents(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), num_pages, ps, _ptr(page_table), page_table.shape[1],
+        _ptr(prefix_len), int(max_prefix), _ptr(k_tree), _ptr(v_tree), _ptr(parent), _ptr(qo_indptr),
+        qo_indptr.numel() - 1, T, int(max_nodes), hq, hkv, d, float(sm_scale), _ptr(out), _ptr(lse),
+        _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_tree_verify_attn_parents")

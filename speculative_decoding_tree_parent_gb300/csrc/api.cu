@@ -27,7 +27,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                    const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
                    int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
-                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale);
+                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale, const int32_t* parent);
 
 constexpr int kMaxNodes = 1024;
 
@@ -133,7 +133,7 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
       aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree) && aligned16(out))
     return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                           k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale,
-                          out, lse, ws, dev_status, st, nullptr);
+                          out, lse, ws, dev_status, st, nullptr, nullptr);
   return launch_attn_simt(dtype, q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len,
                           max_prefix, k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d,
                           sm_scale, out, lse, ws, dev_status, st);
@@ -262,7 +262,35 @@ int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_
   if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
   return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                         k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale, out,
-                        lse, ws, dev_status, static_cast<cudaStream_t>(stream), kv_scale);
+                        lse, ws, dev_status, static_cast<cudaStream_t>(stream), kv_scale, nullptr);
+}
+
+int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                                  int page_size, const int32_t* page_table, int max_pages,
+                                  const int32_t* prefix_len, int max_prefix, const void* k_tree,
+                                  const void* v_tree, const int32_t* parent, const int32_t* qo_indptr, int batch,
+                                  int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                  void* stream) {
+  if (batch < 0 || total_nodes < 0 || max_nodes < 1 || max_nodes > kMaxNodes || max_prefix < 0 ||
+      num_pages < 0 || max_pages < 0)
+    return SPEC_ERR_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
+  if (!attn_tc_supported(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (batch == 0 || total_nodes == 0) return SPEC_OK;
+  if (!q || !k_tree || !v_tree || !parent || !qo_indptr || !prefix_len || !out) return SPEC_ERR_ARG;
+  if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
+    return SPEC_ERR_ARG;
+  if ((long)max_pages * page_size < max_prefix) return SPEC_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out) ||
+      (max_prefix > 0 && (!aligned16(k_pool) || !aligned16(v_pool))))
+    return SPEC_ERR_ARG;
+  const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
+  if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
+  return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
+                        k_tree, v_tree, nullptr, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale, out,
+                        lse, ws, dev_status, static_cast<cudaStream_t>(stream), nullptr, parent);
 }
 
 int spec_kv_commit_kv8(const void* k_tree, const void* v_tree, const float* kv_scale, const int32_t* path,

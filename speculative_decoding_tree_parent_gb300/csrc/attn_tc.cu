@@ -61,6 +61,7 @@ constexpr int kTcThreads = 64 + kTiles * 128 + 32;  // + one more MMA-issuing wa
 constexpr int kMma1Warp = kTcThreads / 32 - 1;     // the MMA issuer of tile 1
 constexpr int kCvtWarps = 4;                       // FP8 cache: code -> bf16 converters
 constexpr int kF8Stages = 3;
+constexpr int kParMax = 1024;                      // nodes per tree (parent array staged in smem)
 constexpr float kRescaleThr = 8.0f;            // log2 units: P entries stay <= 2^8
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s) before a wait gives up
 
@@ -75,23 +76,27 @@ constexpr uint32_t kTmemCols = 512;                         // per tile: S0 | S1
 constexpr uint32_t kIdescQK = tc::idesc_bf16(kTcRows, kTcKeys, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(kTcRows, kTcD, 1);
 
-// Shared-memory plan and block size of the bf16-cache (false) and FP8-cache (true) kernels.
-template <bool kFp8>
+// Shared-memory plan and block size of the bf16-cache (false) and FP8-cache (true) kernels;
+// kPar: the variant that builds the ancestor bits from the parent array (bf16 cache).
+template <bool kFp8, bool kPar = false>
 struct TcCfg {
   static constexpr int kStages = kFp8 ? 3 : kTcStages;      // bf16 K/V ring
   static constexpr int kThreads = kTcThreads + (kFp8 ? 32 * kCvtWarps : 0);
   static constexpr uint32_t kOffF8 = kOffKV + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffF8 + (kFp8 ? kF8Stages * kF8Stage : 0);
-  static constexpr uint32_t kSmem = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static constexpr uint32_t kOffPar = kOffBar + 256;          // parent arrays, one per tile
+  static constexpr uint32_t kSmem = kOffPar + (kPar ? kTiles * kParMax * 4 : 0) + 1024;  // + alignment slack
   static constexpr int kFullCount = kFp8 ? kCvtWarps : 1;   // arrivals that fill a bf16 stage
 };
-static_assert(TcCfg<false>::kSmem <= 232448 && TcCfg<true>::kSmem <= 232448, "shared memory over the per-CTA limit");
+static_assert(TcCfg<false>::kSmem <= 232448 && TcCfg<true>::kSmem <= 232448 && TcCfg<false, true>::kSmem <= 232448,
+              "shared memory over the per-CTA limit");
 
 struct TcParams {
   const int32_t* page_table;
   int max_pages, num_pages;
   const int32_t* prefix_len;
-  const uint64_t* mask;
+  const uint64_t* mask;   // ancestor bitsets [T][mask_words], or
+  const int32_t* parent;  // the parent array (mask == nullptr): the bits come from a walk
   int mask_words;
   const int32_t* qo;
   int hq, hkv, G, splits, mtiles;
@@ -120,6 +125,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort, kWaitLimit) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// the 128 softmax threads of one tile (barrier 1 + tile; 0 is __syncthreads)
+__device__ __forceinline__ void tile_bar_sync(int tile) {
+  if (tile == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -182,12 +193,13 @@ __device__ __forceinline__ TcSplit tc_split(int P, int N, int splits, int s) {
   return r;
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(TcCfg<kFp8>::kThreads, 1)
+template <bool kFp8, bool kPar>
+__global__ void __launch_bounds__(TcCfg<kFp8, kPar>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                    const __grid_constant__ CUtensorMap tm_vp, const __grid_constant__ CUtensorMap tm_kt,
                    const __grid_constant__ CUtensorMap tm_vt, const TcParams p) {
-  using Cfg = TcCfg<kFp8>;
+  static_assert(!(kFp8 && kPar), "the FP8-cache kernel takes a mask");
+  using Cfg = TcCfg<kFp8, kPar>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -510,7 +522,7 @@ __global__ void __launch_bounds__(TcCfg<kFp8>::kThreads, 1)
     } else if (tile < ntiles) {
       // ---------------------------------------------------------------- softmax warps
       const uint32_t t_lane = tbase + tile * 256 + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint64_t* mrow = p.mask + (size_t)(base + node_l) * p.mask_words;
+      const uint64_t* mrow = p.mask != nullptr ? p.mask + (size_t)(base + node_l) * p.mask_words : nullptr;
       const float sl2 = p.scale_log2;
       // FP8 cache: prefix scores scale by the K scale; prefix P carries the V scale in its
       // exponent and its row sum is divided by it
@@ -523,13 +535,43 @@ __global__ void __launch_bounds__(TcCfg<kFp8>::kThreads, 1)
       }
       float m_run = -INFINITY, l = 0.f;
       bool ok = true;
-      // the first tree block's mask word, fetched while the prefix blocks stream (the mask
-      // may come from the kernel launched just before this one: wait for it first)
+      // The first tree block's mask word, fetched while the prefix blocks stream (the mask
+      // may come from the kernel launched just before this one: wait for it first). Given
+      // the parent array instead, the tile's 128 threads stage it in shared memory and each
+      // row's bits for a tree block come from a walk up its ancestors ("EAGLE-2 deep
+      // dive", core-implementation section: a node's mask row is the node and every
+      // ancestor up to the root), checked as the mask kernel checks them.
       uint64_t bits_next = 0ull;
+      const int32_t* spar = reinterpret_cast<const int32_t*>(smem + Cfg::kOffPar) + tile * kParMax;
       if (nb > npb) {
         pdl_wait();
-        if (row_valid) bits_next = __ldcg(mrow + sr.tb_lo);
+        if (kPar) {
+          int32_t* sp = const_cast<int32_t*>(spar);
+          for (int i = threadIdx.x & 127; i < N; i += 128) sp[i] = __ldcg(p.parent + base + i);
+          tile_bar_sync(tile);  // every softmax thread of the tile reaches this
+        } else if (row_valid) {
+          bits_next = __ldcg(mrow + sr.tb_lo);
+        }
       }
+      // ancestor bits of this row among tree keys 64 tb .. 64 tb + 63 (ids fall along the
+      // walk, so it stops below the block; the walk for block 0 reaches the root)
+      auto walk_bits = [&](int tb) -> uint64_t {
+        const int lo = tb * kTcKeys;
+        uint64_t bits = 0ull;
+        int cur = node_l;
+        while (true) {
+          if (cur < lo) break;
+          if (cur < lo + kTcKeys) bits |= 1ull << (cur - lo);
+          const int pp = spar[cur];
+          if (cur == 0 ? pp != -1 : (pp < 0 || pp >= cur)) {
+            report(p.status, SPEC_ERR_PARENT);
+            return 0ull;
+          }
+          if (cur == 0) break;
+          cur = pp;
+        }
+        return bits;
+      };
       for (int j = 0; j < nb; ++j) {
         if (!warp_wait(bar_sf(tile, j & 1), (j >> 1) & 1, abort)) {
           ok = false;
@@ -547,8 +589,13 @@ __global__ void __launch_bounds__(TcCfg<kFp8>::kThreads, 1)
             for (int c = 0; c < kTcKeys; ++c) sv[c] = c < nvalid ? sv[c] : -INFINITY;
           }
         } else {  // tree block: ancestor bits
-          const uint64_t bits = bits_next;
-          if (row_valid && j + 1 < nb) bits_next = __ldcg(mrow + sr.tb_lo + (j + 1 - npb));
+          uint64_t bits;
+          if (kPar) {
+            bits = row_valid ? walk_bits(sr.tb_lo + (j - npb)) : 0ull;
+          } else {
+            bits = bits_next;
+            if (row_valid && j + 1 < nb) bits_next = __ldcg(mrow + sr.tb_lo + (j + 1 - npb));
+          }
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c] = ((bits >> c) & 1ull) ? sv[c] : -INFINITY;
         }
@@ -863,7 +910,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                    const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
                    int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
-                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale) {
+                   void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale, const int32_t* parent) {
   (void)ps;
   const bool fp8 = kv_scale != nullptr;
   (void)d;
@@ -899,15 +946,19 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
     tm_kp = tm_kt;
     tm_vp = tm_vt;
   }
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[fp8]) {
+  const bool par = mask == nullptr && parent != nullptr;
+  const int variant = fp8 ? 1 : par ? 2 : 0;
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[variant]) {
     const cudaError_t e =
-        fp8 ? cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   TcCfg<true>::kSmem)
-            : cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   TcCfg<false>::kSmem);
+        variant == 1   ? cudaFuncSetAttribute(attn_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              TcCfg<true>::kSmem)
+        : variant == 2 ? cudaFuncSetAttribute(attn_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              TcCfg<false, true>::kSmem)
+                       : cudaFuncSetAttribute(attn_tc_kernel<false, false>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<false>::kSmem);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    attr_set[fp8] = true;
+    attr_set[variant] = true;
   }
   const int splits = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
   const int mtiles = tc_mtiles(max_nodes, G);
@@ -917,6 +968,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.num_pages = num_pages;
   prm.prefix_len = prefix_len;
   prm.mask = mask;
+  prm.parent = par ? parent : nullptr;
   prm.mask_words = (max_nodes + 63) >> 6;
   prm.qo = qo;
   prm.hq = hq;
@@ -937,7 +989,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(splits, ceil_div(mtiles, kTiles), batch * hkv);
   cfg.blockDim = dim3(fp8 ? TcCfg<true>::kThreads : TcCfg<false>::kThreads);
-  cfg.dynamicSmemBytes = fp8 ? TcCfg<true>::kSmem : TcCfg<false>::kSmem;
+  cfg.dynamicSmemBytes = variant == 1 ? TcCfg<true>::kSmem : variant == 2 ? TcCfg<false, true>::kSmem : TcCfg<false>::kSmem;
   cfg.stream = stream;
   // programmatic serialization: the prologue (barriers, TMEM, Q and first K/V loads)
   // overlaps the mask kernel; the softmax waits for it before the first tree block
@@ -946,8 +998,10 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t le = fp8 ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm)
-                            : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm);
+  const cudaError_t le =
+      variant == 1   ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true, false>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm)
+      : variant == 2 ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<false, true>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm)
+                     : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false, false>, tm_q, tm_kp, tm_vp, tm_kt, tm_vt, prm);
   if (le != cudaSuccess) return SPEC_ERR_CUDA;
   if (splits > 1) {
     TcMergeParams mp;

@@ -115,6 +115,17 @@ class DeviceBatch:
                                        self.max_nodes, self.out, self.lse, self.attn_ws, sm_scale, self.status,
                                        stream)
 
+    def attention_parents(self, stream=None, sm_scale=0.0):
+        """The attention with the mask step inside it (ancestor bits from the parent array)."""
+        return B.spec_tree_verify_attn_parents(self.q, self.k_pool, self.v_pool, self.page_table, self.prefix_len,
+                                               self.max_prefix, self.k_tree, self.v_tree, self.parent, self.qo,
+                                               self.max_nodes, self.out, self.lse, self.attn_ws, sm_scale,
+                                               self.status, stream)
+
+    def fused_mask_ok(self):
+        """Whether the attention call can build the mask itself (tensor-core shapes, bf16 cache)."""
+        return not self.kv_fp8 and self.inp.dtype == "bf16" and self.attn_plan()[1] == 1
+
     def accept(self, mode=None, stream=None):
         mode = mode or self.mode
         m = B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY
@@ -146,19 +157,24 @@ class DeviceBatch:
                                     uniforms=self.uniforms if m else None, temperature=self.inp.temperature,
                                     flags=self.flags, dev_status=self.status, stream=stream)
 
-    def step(self, mode=None, stream=None, fused=True):
+    def step(self, mode=None, stream=None, fused=True, fuse_mask=False):
         """One full verification step: mask, attention, then acceptance + KV commit (one fused
-        call, or the two separate ones). Returns the number of kernel launches issued."""
-        self.build_mask(stream)
-        self.attention(stream)
+        call, or the two separate ones). fuse_mask: the attention call builds the mask itself
+        (spec_tree_verify_attn_parents), where the shapes allow. Returns the number of kernel
+        launches issued."""
+        if fuse_mask and self.fused_mask_ok():
+            self.attention_parents(stream)
+        else:
+            self.build_mask(stream)
+            self.attention(stream)
         if fused:
             self.accept_commit(mode, stream)
         else:
             self.accept(mode, stream)
             self.commit(stream)
-        return self.launches_per_step(mode, fused)
+        return self.launches_per_step(mode, fused, fuse_mask)
 
-    def launches_per_step(self, mode=None, fused=True):
+    def launches_per_step(self, mode=None, fused=True, fuse_mask=False):
         """Kernel launches of one step: mask 1, attention 1 (+1 merge kernel when the keys are
         split), then accept 1 (greedy) or 2 (stochastic) and commit 1 -- except that the fused
         greedy call of up to 4 sequences commits inside its acceptance kernel (bf16 cache)."""
@@ -167,7 +183,8 @@ class DeviceBatch:
         attn = 2 if splits > 1 else 1
         acc = 2 if mode == "stochastic" else 1
         commit = 0 if (fused and mode != "stochastic" and self.B <= 4 and not self.kv_fp8) else 1
-        return 1 + attn + acc + commit
+        mask = 0 if (fuse_mask and self.fused_mask_ok()) else 1
+        return mask + attn + acc + commit
 
     def attn_plan(self):
         inp = self.inp
