@@ -11,9 +11,11 @@
  *   spec_kv_commit         the accepted path's K/V written into the paged cache
  *
  * spec_accept_commit runs the last two as one call (the same results, one kernel
- * boundary fewer). spec_tree_verify_attn_kv8 and spec_kv_commit_kv8 are the attention
- * and the commit over an FP8 (E4M3) paged cache; spec_tree_init / spec_tree_expand build
- * the draft tree on the device.
+ * boundary fewer). spec_tree_verify_attn_parents runs the first two as one call (the mask
+ * built inside the attention from the parent array). spec_tree_verify_attn_kv8 and
+ * spec_kv_commit_kv8 are the attention and the commit over an FP8 (E4M3) paged cache;
+ * spec_tree_init / spec_tree_expand build the draft tree on the device;
+ * spec_accept_noalloc is spec_accept without a workspace argument.
  *
  * Sources of the operations (page title, then section):
  *   "EAGLE-2 deep dive" (techknowgenie): architecture section (all tree tokens
@@ -58,16 +60,18 @@
  *     serialization, so a call may begin while the kernel enqueued before it
  *     is still running. Every kernel waits for that predecessor before it
  *     writes anything and before it reads what the predecessor may write,
- *     with one exception: spec_tree_verify_attn reads q, k_pool, v_pool,
- *     k_tree, v_tree, page_table, prefix_len and qo_indptr (everything but
- *     the mask) before that wait. If the kernel enqueued just before it
+ *     with one exception: spec_tree_verify_attn (and its _kv8 and _parents
+ *     forms) reads q, k_pool, v_pool, k_tree, v_tree, page_table, prefix_len,
+ *     qo_indptr and kv_scale (everything but the mask or parent array)
+ *     before that wait. If the kernel enqueued just before it
  *     writes one of those and signals its dependents early (the
  *     griddepcontrol.launch_dependents instruction), put an event or another
  *     kernel between the two. Kernels that never signal early (the usual
  *     case) need nothing. Of this library's kernels, the ones that signal
- *     early write only mask and depth (spec_build_tree_mask), out and lse
- *     (the attention's split merge) and the acceptance results (greedy
- *     spec_accept); the commit kernels, which write the pool, never do.
+ *     early write only mask and depth (spec_build_tree_mask), out, lse and
+ *     the workspace (the attention and its split merge), the workspace (the
+ *     stochastic statistics) and the acceptance results (greedy spec_accept);
+ *     the commit kernels, which write the pool, never do.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
