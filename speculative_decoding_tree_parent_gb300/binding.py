@@ -240,6 +240,8 @@ def spec_tree_verify_attn_kv8(q, k_pool, v_pool, kv_scale, page_table, prefix_le
     [pages,Hkv,16,128], kv_scale float32 [2,Hkv] (K scales, then V scales); q, k_tree,
     v_tree and out bf16."""
     _need(q, torch.bfloat16, "q")
+    for t, what in ((k_tree, "k_tree"), (v_tree, "v_tree"), (out, "out")):
+        _need(t, torch.bfloat16, what)
     _need(k_pool, torch.uint8, "k_pool (E4M3 codes)")
     _need(v_pool, torch.uint8, "v_pool (E4M3 codes)")
     _need(kv_scale, torch.float32, "kv_scale")
@@ -257,7 +259,9 @@ def spec_kv_commit_kv8(k_tree, v_tree, kv_scale, path, accept_len, qo_indptr, pa
                        v_pool, seq_len_out=None, dev_status=None, stream=None):
     """Commit of bf16 tree K/V rows into an FP8 cache (E4M3 codes of x / scale)."""
     _need(k_tree, torch.bfloat16, "k_tree")
+    _need(v_tree, torch.bfloat16, "v_tree")
     _need(k_pool, torch.uint8, "k_pool (E4M3 codes)")
+    _need(v_pool, torch.uint8, "v_pool (E4M3 codes)")
     _need(kv_scale, torch.float32, "kv_scale")
     T, hkv, d = k_tree.shape
     num_pages, _, ps, _ = k_pool.shape
@@ -274,6 +278,8 @@ def spec_tree_verify_attn_parents(q, k_pool, v_pool, page_table, prefix_len, max
     """Tree-verify attention with the ancestor bits built in-kernel from the parent array
     (bf16, tensor-core shapes)."""
     _need(q, torch.bfloat16, "q")
+    for t, what in ((k_tree, "k_tree"), (v_tree, "v_tree"), (out, "out"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, torch.bfloat16, what)
     _need(parent, torch.int32, "parent")
     T, hq, d = q.shape
     num_pages, hkv, ps, _ = k_pool.shape
