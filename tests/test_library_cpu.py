@@ -61,3 +61,35 @@ def test_attn_plan(lib):
         binding.spec_attn_plan(binding.SPEC_BF16, 1, 16, 4, 1, 96, 16, 128)   # head dim 96
     with pytest.raises(binding.SpecError):
         binding.spec_attn_plan(binding.SPEC_BF16, 1, 2000, 4, 1, 128, 16, 128)  # > 1024 nodes
+
+
+def test_host_argument_checks_of_the_newer_entry_points(lib):
+    """Checks that return before any device work: sizes, null pointers, unsupported shapes.
+    The pointers passed are never dereferenced (each call returns at its host check)."""
+    fake = ctypes.c_void_p(256)  # a non-null address the calls below never touch
+    # draft tree: top-k beyond 16, a zero depth, a node budget beyond 1024, a short state
+    st = lib.spec_tree_expand(fake, 1000, 1000, 1000, 1, 8, 17, 4, 0.0, fake, 1 << 20, fake, fake, fake, fake,
+                              None, None, None)
+    assert st == -1
+    st = lib.spec_tree_expand(fake, 1000, 1000, 1000, 1, 8, 4, 0, 0.0, fake, 1 << 20, fake, fake, fake, fake,
+                              None, None, None)
+    assert st == -1
+    assert lib.spec_tree_init(fake, 1, 2000, fake, 1 << 20, fake, fake, fake, fake, None, None) == -1
+    need = binding.spec_workspace_size(binding.SPEC_OP_TREE, 2, 0, 64, 0, 0, 0, 0, 0)
+    assert need > 0
+    assert lib.spec_tree_init(fake, 2, 64, fake, need - 1, fake, fake, fake, fake, None, None) == -5
+    # FP8 commit: head dim not a multiple of 16, then a missing scale array
+    args = lambda d, scale: (fake, fake, scale, fake, 9, fake, fake, fake, 4, 4, 16, fake, None, fake, fake, 1, 4,
+                             8, d, None, None)
+    assert lib.spec_kv_commit_kv8(*args(24, fake)) == -6
+    assert lib.spec_kv_commit_kv8(*args(32, None)) == -1
+    # attention forms: an empty batch is a no-op, a head count that the KV heads do not
+    # divide is refused before anything else
+    common = lambda hq, hkv: (fake, fake, fake, 4, 16, fake, 4, fake, 64, fake, fake, fake, fake, 1, 4, 4, hq, hkv,
+                              128, 0.0, fake, None, None, 0, None, None)
+    assert lib.spec_tree_verify_attn_parents(*common(30, 8)) == -1
+    c = list(common(32, 8))
+    c[13] = 0   # batch 0
+    assert lib.spec_tree_verify_attn_parents(*c) in (0, -6)   # no work, or no tensor-core path on this host
+    kv8 = (fake, fake, fake, fake) + common(30, 8)[3:]
+    assert lib.spec_tree_verify_attn_kv8(*kv8) == -1
