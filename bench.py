@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -185,10 +186,18 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- traffic record
 
+def _code_only(text):
+    """The source with its comments removed and its whitespace collapsed: an edit to a
+    comment leaves the compiled kernel, and so its recorded traffic, as it was."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def _kernel_digest(files):
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

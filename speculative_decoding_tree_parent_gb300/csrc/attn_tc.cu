@@ -29,16 +29,21 @@
 //               TMEM only when the running max grows by more than 2^8.
 // S is double-buffered in TMEM, so QK of block j+1 runs while the softmax of block j
 // does. Every wait is bounded.
-// FP8 cache (attn_tc_kernel<true>): the pool holds E4M3 codes ([page][Hkv][16][128] bytes,
-// a 2 KB tile per (page, head)) with an fp32 scale per KV head for K and for V. Prefix
-// pages are TMA-loaded into a 3-stage ring of 16 KB code stages (half the bytes of bf16),
-// and four more warps (11-14) widen each stage into the bf16 ring, in the swizzled layout
-// TMA would have written, with integer ops and a packed multiply (no conversion-pipe
-// instructions). The conversion is exact: every E4M3 value is a bf16 value. The
-// scales never touch the operands. The K scale multiplies the prefix blocks' score scale.
-// The V scale is folded into the exponent of those blocks' P (2^(s - m + log2 v_scale)),
-// and their row sum is divided by it. Tree blocks are bf16 and TMA-loaded as before.
-// When the keys are split (a short batch cannot fill 152 SMs otherwise), each split CTA
+// The kernel has three instances: attn_tc_kernel<false, false> (bf16 cache, mask given),
+// <true, false> (FP8 cache) and <false, true> (bf16 cache; the ancestor bits come from a
+// walk of the parent array, staged in shared memory, instead of a mask).
+// FP8 cache: the pool holds E4M3 codes ([page][Hkv][16][128] bytes, a 2 KB tile per
+// (page, head)) with an fp32 scale per KV head for K and for V. The producer TMA-loads the
+// prefix pages into a 3-stage ring of 16 KB code stages (half the bytes of bf16). Four
+// more warps (11-14) widen each stage into a 3-stage bf16 ring, in the swizzled layout TMA
+// would have written, with integer ops and a packed multiply (no conversion-pipe
+// instructions); they also TMA-load the bf16 tree blocks, so one party fills every bf16
+// stage and waits for each of its phases in order. The conversion is exact: every E4M3
+// value is a bf16 value. The scales never touch the operands. The K scale multiplies the
+// prefix blocks' score scale. The V scale is folded into the exponent of those blocks' P
+// (2^(s - m + log2 v_scale)), and their row sum is divided by it.
+// Keys are split when a short batch cannot fill 152 SMs otherwise, and for larger batches
+// when the waves of CTAs end better split (the host's wave model). Each split CTA
 // writes a partial per tile (O / l rounded to bf16 plus the split's log2-sum-exp;
 // coalesced, L2-resident) and a small merge kernel, launched with programmatic
 // serialization so it is resident before this grid ends, combines them by log-sum-exp.
