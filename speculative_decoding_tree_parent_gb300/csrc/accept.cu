@@ -21,7 +21,8 @@
 // Stochastic, two launches:
 //   accept_stats_kernel    grid = chunks x nodes. Per chunk of a row of target and
 //                          draft logits: max and sum of exp((x - max) / T) (fp32
-//                          elements, Kahan compensated, fp64 across threads). The walk
+//                          elements from ex2.approx, Kahan compensated per thread,
+//                          double-float across threads, stored in fp64). The walk
 //                          merges a node's chunk partials when it visits the node.
 //   accept_walk_kernel     one 8-CTA cluster per sequence. The decisions at a node
 //                          need sums over the vocabulary of the residual
