@@ -400,7 +400,7 @@ int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void*
  *   other shapes return SPEC_ERR_UNSUPPORTED. The workspace is spec_workspace_size(
  *   SPEC_OP_ATTN, ...) for the same sizes. Errors as for spec_tree_verify_attn; q, k_tree,
  *   v_tree, out and (with a prefix) the pools must be 16-byte aligned (else SPEC_ERR_ARG).
- *   NaN codes in the pool make the affected rows NaN.
+ *   The pool must hold finite codes: a NaN code (S.1111.111) is read as +-480.
  */
 int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
                               const float* kv_scale, int num_pages, int page_size,
