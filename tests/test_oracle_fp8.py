@@ -153,3 +153,22 @@ def test_fp8_commit_writes_quantised_rows_only():
             assert np.array_equal(kp[page, g, r], _torch_encode(kt[node, g] / scale[0, g]))
             assert np.array_equal(vp[page, g, r], _torch_encode(vt[node, g] / scale[1, g]))
     assert np.array_equal(kp[~touched], kc[~touched]) and np.array_equal(vp[~touched], vc[~touched])
+
+
+def test_workload_fp8_pool_is_the_pool_in_codes():
+    """The generator's FP8 pools (test data): no NaN codes, one positive scale per KV head
+    for K and for V (max|x| / 448), and every dequantised value within E4M3 rounding
+    (half a unit in the last place: relative 2^-4, or 2^-10 absolute near zero) of the
+    bf16 pool it came from."""
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    inp = W.generate(W.spec(3, batch=2, prefix=(100, 300), nodes=(8, 8), vocab=64, tree="random",
+                            agree_prob=0.5), seed=4)
+    kc, vc, sc = W.fp8_pool(inp)
+    assert kc.shape == inp.k_pool.shape and kc.dtype == np.uint8 and vc.dtype == np.uint8
+    assert sc.shape == (2, inp.hkv) and (sc > 0).all()
+    for codes, pool, s in ((kc, inp.k_pool, sc[0]), (vc, inp.v_pool, sc[1])):
+        assert not ((codes & 0x7F) == 0x7F).any()
+        x = pool.astype(np.float64) / s.astype(np.float64)[None, :, None, None]
+        d = F.e4m3_decode(codes)
+        assert np.all(np.abs(d - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10) * 1.0001)
+        assert np.isclose(np.abs(x).max(), 448.0, rtol=1e-6)
