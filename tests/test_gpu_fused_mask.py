@@ -13,13 +13,12 @@ from speculative_decoding_tree_parent_gb300 import binding as B
 from speculative_decoding_tree_parent_gb300 import workloads as W
 from speculative_decoding_tree_parent_gb300.step import DeviceBatch
 
+import attn_tolerance as AT
+
 pytestmark = pytest.mark.gpu
 
 if not torch.cuda.is_available():  # collected on CPU machines, skipped there
     pytest.skip("needs a GPU", allow_module_level=True)
-
-BF16_REL = 2.0 ** -7
-
 
 def _both(inp):
     sep = DeviceBatch(inp)
@@ -54,11 +53,8 @@ def test_fused_mask_trees_and_shapes(prefix, nodes, tree, hq):
     sep, fused = _both(inp)
     assert torch.equal(sep.out, fused.out)
     mask, _ = oracle.ancestor_mask_batch(inp.parent, inp.qo_indptr, inp.max_nodes)
-    ref, _ = oracle.tree_verify_attention(inp.q, inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len,
-                                          inp.k_tree, inp.v_tree, mask, inp.qo_indptr, inp.hq, inp.hkv)
-    err = np.abs(fused.out.float().cpu().numpy() - ref).max()
-    vmax = max(np.abs(inp.v_tree).max(), np.abs(inp.v_pool).max())
-    assert err <= BF16_REL * vmax, (err, BF16_REL * vmax)
+    ref, _, A = AT.reference(inp, mask)
+    AT.check(fused.out.float().cpu().numpy(), ref, A, "attention with the mask inside")
 
 
 def test_fused_mask_reports_a_bad_parent():

@@ -3,9 +3,10 @@
 Bars: masks, accepted lengths, paths, tokens and committed KV bytes bit-exact;
 stochastic decisions exact except sequences the oracle flags as near-ties
 (|u - ratio| <= 1e-6 or a bonus threshold within 1e-6 of a CDF boundary);
-attention max-abs-error <= 1e-4 (fp32 inputs) and <= 2e-2 (bf16 inputs), plus a
-tighter bound derived from bf16 arithmetic on inputs whose softmax is peaked
-enough that a wrong mask bit would show.
+attention max-abs-error <= 1e-4 (fp32 inputs) and <= 2e-2 (bf16 inputs), plus, for
+bf16, the per-element bound derived from the kernel's bf16 roundings
+(attn_tolerance: (2^-8 + 2^-12) * sum_k p_k |v_k| + 2^-9 |o|), which a zeroed output
+or one missing key split fails on every workload (negative controls on the host).
 """
 
 import numpy as np
@@ -17,16 +18,17 @@ from speculative_decoding_tree_parent_gb300 import binding as B
 from speculative_decoding_tree_parent_gb300 import workloads as W
 from speculative_decoding_tree_parent_gb300.step import DeviceBatch
 
+import attn_tolerance as AT
+from attn_cases import LONG, long_inputs, sample_rows as _sample_rows, sensitive as _sensitive
+
 pytestmark = pytest.mark.gpu
 
 if not torch.cuda.is_available():  # collected on CPU machines, skipped there
     pytest.skip("needs a GPU", allow_module_level=True)
 
 FP32_TOL = 1e-4
-BF16_TOL = 2e-2
-# derived: P is rounded to bf16 (relative 2^-9) before the PV product and the output
-# is rounded to bf16 (relative 2^-9): |error| <= 2^-9 (max|v| + 2 |o|) <= 2^-7 max|v|
-BF16_REL = 2.0 ** -7
+# bf16: the per-element bound of attn_tolerance, |gpu - oracle| <= (2^-8 + 2^-12) A + 2^-9 |o|
+# with A = the oracle's attention over |V| (and the stated 2e-2 bar)
 
 
 @pytest.fixture(scope="module")
@@ -103,30 +105,54 @@ def test_mask_rejects_bad_parent():
     assert got[2] == 0 and got[0] == 1 and got[1] == 3 and got[4] == 1 and got[5] == 3
 
 
+def test_mask_capacity_error_zeroes_rows():
+    """A sequence longer than max_nodes: SPEC_ERR_CAPACITY, and its rows are written all-zero
+    with depth -1 (a mask buffer holding an earlier call's bits keeps none of them); the
+    other sequence's rows are the oracle's."""
+    rng = np.random.default_rng(11)
+    sizes = [70, 10]
+    par = np.concatenate([[-1] + [int(rng.integers(0, i)) for i in range(1, m)] for m in sizes]).astype(np.int32)
+    qo = np.array([0, 70, 80], np.int32)
+    mask = torch.full((80, 1), -1, dtype=torch.int64, device="cuda")
+    depth = torch.full((80,), 5, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.spec_build_tree_mask(torch.from_numpy(par).cuda(), torch.from_numpy(qo).cuda(), 64, mask, depth, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -4
+    got = mask.cpu().numpy().view(np.uint64)[:, 0]
+    d = depth.cpu().numpy()
+    assert (got[:70] == 0).all() and (d[:70] == -1).all()
+    m, dd = oracle.ancestor_mask_batch(par[70:], np.array([0, 10], np.int32), 64)
+    assert np.array_equal(got[70:], oracle.pack_mask_words(m, 1)[:, 0])
+    assert np.array_equal(d[70:], dd)
+
+
 # -------------------------------------------------------------------------- attention
 
-def _attn_check(inp, o_gpu, rows=None, derived=True):
-    """Compare GPU output rows (all, or (t, h) samples) with the oracle."""
+def _attn_check(inp, o_gpu, rows=None, splits=None):
+    """Compare GPU output rows (all, or (t, h) samples) with the oracle. fp32 inputs: max-abs
+    error <= 1e-4. bf16 inputs: the per-element bound of attn_tolerance; given the call's
+    key-split count, also its negative controls (a zeroed output and one missing split's
+    keys must fail the same check)."""
     mask, _, _ = _oracle_mask(inp)
-    if rows is None:
-        ref, lse = oracle.tree_verify_attention(inp.q, inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len,
-                                                inp.k_tree, inp.v_tree, mask, inp.qo_indptr, inp.hq, inp.hkv)
-        got = o_gpu.float().cpu().numpy().astype(np.float64)
-        vmax = max(np.abs(inp.v_tree).max(), np.abs(inp.v_pool).max())
-    else:
-        ref, lse = oracle.tree_verify_attention_rows(rows, inp.q, inp.k_pool, inp.v_pool, inp.page_table,
-                                                     inp.prefix_len, inp.k_tree, inp.v_tree, mask, inp.qo_indptr,
-                                                     inp.hq, inp.hkv)
-        o = o_gpu.float().cpu().numpy()
-        got = np.stack([o[t, h] for t, h in rows]).astype(np.float64)
-        vmax = max(np.abs(inp.v_tree).max(), np.abs(inp.v_pool).max())
-    err = np.abs(got - ref).max()
+    o = o_gpu.float().cpu().numpy().astype(np.float64)
+    got = o if rows is None else np.stack([o[t, h] for t, h in rows])
     if inp.dtype == "f32":
+        if rows is None:
+            ref, lse = oracle.tree_verify_attention(inp.q, inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len,
+                                                    inp.k_tree, inp.v_tree, mask, inp.qo_indptr, inp.hq, inp.hkv)
+        else:
+            ref, lse = oracle.tree_verify_attention_rows(rows, inp.q, inp.k_pool, inp.v_pool, inp.page_table,
+                                                         inp.prefix_len, inp.k_tree, inp.v_tree, mask,
+                                                         inp.qo_indptr, inp.hq, inp.hkv)
+        err = np.abs(got - ref).max()
         assert err <= FP32_TOL, err
-    else:
-        assert err <= BF16_TOL, err
-        if derived:
-            assert err <= BF16_REL * vmax, (err, BF16_REL * vmax)
+        assert np.abs(ref).max() > 100 * FP32_TOL   # a zeroed output would fail
+        return err, ref, lse
+    ref, lse, A = AT.reference(inp, mask, rows)
+    err = AT.check(got, ref, A, inp.name)
+    if splits is not None:
+        AT.negative_controls(inp, mask, ref, A, splits, rows)
     return err, ref, lse
 
 
@@ -138,21 +164,8 @@ def test_attention_config_full(inputs, cfg):
     db.attention()
     torch.cuda.synchronize()
     assert _status(db) == 0
-    err, ref, lse = _attn_check(inp, db.out)
+    err, ref, lse = _attn_check(inp, db.out, splits=db.attn_plan()[0])
     np.testing.assert_allclose(db.lse.cpu().numpy(), lse, atol=1e-3 if inp.dtype == "bf16" else 1e-5)
-
-
-def _sample_rows(inp, n, seed):
-    rng = np.random.default_rng(seed)
-    T, hq = inp.total_nodes, inp.hq
-    rows = {(0, 0), (T - 1, hq - 1), (T - 1, 0)}
-    for b in range(min(inp.batch, 8)):
-        a, e = inp.qo_indptr[b], inp.qo_indptr[b + 1]
-        rows.add((int(e - 1), int(rng.integers(0, hq))))
-        rows.add((int(a), int(rng.integers(0, hq))))
-    while len(rows) < n:
-        rows.add((int(rng.integers(0, T)), int(rng.integers(0, hq))))
-    return sorted(rows)
 
 
 @pytest.mark.parametrize("cfg,n", [(3, 48), (4, 24), (5, 64)])
@@ -163,44 +176,8 @@ def test_attention_config_sampled(inputs, cfg, n):
     db.attention()
     torch.cuda.synchronize()
     assert _status(db) == 0
-    _attn_check(inp, db.out, rows=_sample_rows(inp, n, cfg))
+    _attn_check(inp, db.out, rows=_sample_rows(inp, n, cfg), splits=db.attn_plan()[0])
     assert torch.isfinite(db.out.float()).all()
-
-
-def _sensitive(dtype, hq, hkv, d, prefixes, sizes, seed, scale=1.0, tree="random"):
-    """Small batch with peaked softmax (unscaled N(0,1) Q/K) and short prefixes, so the
-    tree keys carry real weight and any wrong mask bit moves the output."""
-    sp = W.spec(1, dtype=dtype, batch=len(prefixes), hq=hq, hkv=hkv, d=d, vocab=64, prefix=(0, 0),
-                nodes=(1, 1), qkv_scale=scale, page_layout="shuffled", extra_pages=3)
-    inp = W.generate(sp, seed)
-    # rebuild with per-sequence prefix / tree sizes
-    rng = np.random.default_rng(seed)
-    parents, qo = [], [0]
-    for n in sizes:
-        if tree == "chain":
-            p = np.arange(-1, n - 1)
-        else:
-            p = np.array([-1] + [int(rng.integers(max(0, i - 8), i)) for i in range(1, n)])
-        parents.append(p)
-        qo.append(qo[-1] + n)
-    T = qo[-1]
-    ps = 16
-    need = [-(-(P + n) // ps) for P, n in zip(prefixes, sizes)]
-    total = sum(need) + 3
-    ids = rng.permutation(total)
-    pt = np.full((len(sizes), max(need)), -1, np.int32)
-    off = 0
-    for b in range(len(sizes)):
-        pt[b, : need[b]] = ids[off : off + need[b]]
-        off += need[b]
-    f = (lambda x: W.round_to_bf16(x)) if dtype == "bf16" else (lambda x: x)
-    g = lambda *s: f((rng.standard_normal(s) * scale).astype(np.float32))
-    from dataclasses import replace
-    return replace(inp, qo_indptr=np.array(qo, np.int32), parent=np.concatenate(parents).astype(np.int32),
-                   draft_tokens=np.zeros(T, np.int32), q=g(T, hq, d), k_tree=g(T, hkv, d), v_tree=g(T, hkv, d),
-                   k_pool=g(total, hkv, ps, d), v_pool=g(total, hkv, ps, d), page_table=pt,
-                   prefix_len=np.array(prefixes, np.int32), target_logits=np.zeros((T, 64), np.float32),
-                   draft_logits=None, uniforms=None, max_depth=int(max(sizes)))
 
 
 SENSITIVE = [
@@ -224,8 +201,21 @@ def test_attention_sensitive(case):
     db.attention()
     torch.cuda.synchronize()
     assert _status(db) == 0
-    err, ref, lse = _attn_check(inp, db.out)
+    err, ref, lse = _attn_check(inp, db.out, splits=db.attn_plan()[0])
     np.testing.assert_allclose(db.lse.cpu().numpy(), lse, atol=2e-2 if dtype == "bf16" else 1e-4)
+
+
+@pytest.mark.parametrize("name", sorted(LONG))
+def test_attention_long_prefix_peaked(name):
+    inp, rows = long_inputs(name)
+    db = DeviceBatch(inp)
+    splits = db.attn_plan()[0]
+    assert splits >= 4, splits
+    db.build_mask()
+    db.attention()
+    torch.cuda.synchronize()
+    assert _status(db) == 0
+    _attn_check(inp, db.out, rows=rows, splits=splits)
 
 
 def test_attention_chain_equals_causal():
@@ -368,6 +358,40 @@ def test_accept_greedy_ties_and_duplicates(seed, Bn, V, nmax):
     # a second call reuses the workspace (counters must have been reset)
     db.accept("greedy")
     torch.cuda.synchronize()
+    assert _accept_compare(db, ref) == 0
+
+
+def test_accept_greedy_signed_zero_maximum():
+    """Rows whose maximum is zero, held as -0.0 and +0.0 at different indices, some in
+    different 4096-logit tasks of a 128256-token row: -0.0 == +0.0, so the argmax is the
+    lowest index holding either (np.argmax's rule, the oracle's), whatever the sign bits."""
+    V = 128256
+    cases = [((5, -0.0), (70000, 0.0)),      # -0 first (task 0), +0 in task 17
+             ((100, 0.0), (9000, -0.0)),     # +0 first
+             ((4095, -0.0), (4096, 0.0)),    # either side of the first task boundary
+             ((3, -0.0), (7, 0.0))]          # one task
+    T = len(cases)
+    logits = np.full((T, V), -1.0, np.float32)
+    for r, ((i0, v0), (i1, v1)) in enumerate(cases):
+        logits[r, i0] = v0
+        logits[r, i1] = v1
+    am = [c[0][0] for c in cases]
+    assert list(np.argmax(logits, axis=1)) == am
+    # a chain whose draft tokens are the argmaxes of the rows above them: every node accepted
+    parent = np.arange(-1, T - 1, dtype=np.int32)
+    tokens = np.array([0] + am[:-1], np.int32)
+    sp = W.spec(1, batch=1)
+    inp = W.generate(sp)
+    from dataclasses import replace
+    inp = replace(inp, qo_indptr=np.array([0, T], np.int32), parent=parent, draft_tokens=tokens,
+                  target_logits=logits, vocab=V, q=np.zeros((T, 4, 64), np.float32),
+                  k_tree=np.zeros((T, 1, 64), np.float32), v_tree=np.zeros((T, 1, 64), np.float32), max_depth=T)
+    ref = _oracle_accept(inp, "greedy")
+    assert ref.accept_len[0] == T - 1 and ref.out_tokens[0, T - 1] == am[-1]
+    db = DeviceBatch(inp)
+    db.accept("greedy")
+    torch.cuda.synchronize()
+    assert _status(db) == 0
     assert _accept_compare(db, ref) == 0
 
 
