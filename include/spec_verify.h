@@ -112,8 +112,9 @@ size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, in
 
 /* Launch plan spec_tree_verify_attn uses for these sizes (informational; the pages
  * have no counterpart): *splits = number of key splits (> 1 adds a merge kernel),
- * *tensor_cores = 1 when the tcgen05 kernel runs, 0 for the CUDA-core kernel.
- * Returns SPEC_OK or SPEC_ERR_ARG / SPEC_ERR_UNSUPPORTED like the call would. */
+ * *tensor_cores = 1 when the tcgen05 kernel runs (every bf16 call with d = 128), 0 for
+ * the CUDA-core kernel (fp32 inputs, or d = 64). Returns SPEC_OK or SPEC_ERR_ARG /
+ * SPEC_ERR_UNSUPPORTED like the call would. */
 int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, int page_size,
                    int max_prefix, int* splits, int* tensor_cores);
 
@@ -140,8 +141,9 @@ int spec_version(void);
  *              t = node j of t's sequence is t itself or an ancestor of t. Bits of
  *              node ids >= the sequence's node count are 0.
  *   depth      int32 [total_nodes] (out, nullable)  parent links to the root (root 0).
- *   Device errors: SPEC_ERR_PARENT (row left all-zero), SPEC_ERR_CAPACITY
- *   (sequence longer than max_nodes; its rows are not written).
+ *   Device errors: SPEC_ERR_PARENT (that row written all-zero, depth -1),
+ *   SPEC_ERR_CAPACITY (sequence longer than max_nodes: its rows written all-zero,
+ *   depth -1, so no earlier call's bits remain for a later attention to read).
  */
 int spec_build_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int batch,
                          int total_nodes, int max_nodes, uint64_t* mask, int32_t* depth,
@@ -170,8 +172,12 @@ int spec_build_tree_mask(const int32_t* parent, const int32_t* qo_indptr, int ba
  *   k_tree, v_tree  [total_nodes][hkv][d]  K/V of the tree tokens themselves.
  *   mask       uint64 [total_nodes][ceil(max_nodes/64)]  from spec_build_tree_mask.
  *   qo_indptr  int32 [batch+1]; max_nodes >= every sequence's node count.
- *   hq % hkv == 0; d in {64, 128}; page_size a multiple of 8 (16 for the bf16
- *   tensor-core path); sm_scale <= 0 selects 1/sqrt(d).
+ *   hq % hkv == 0; d in {64, 128}; sm_scale <= 0 selects 1/sqrt(d).
+ *   Kernels: bf16 with d = 128 runs on the tensor-core kernel and on nothing else. It
+ *   needs page_size 16 and hq / hkv dividing 128 (else SPEC_ERR_UNSUPPORTED), q, k_pool,
+ *   v_pool, k_tree, v_tree and out 16-byte aligned (else SPEC_ERR_ARG), and the driver's
+ *   tensor-map encoder (else SPEC_ERR_CUDA). fp32 inputs, and d = 64, run on the
+ *   CUDA-core kernel (page_size a multiple of 8).
  *   out        [total_nodes][hq][d] (out)
  *   lse        float [total_nodes][hq] (out, nullable)  natural-log log-sum-exp.
  *   ws         workspace of spec_workspace_size(SPEC_OP_ATTN, ...) bytes (key-split
@@ -341,7 +347,10 @@ int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride,
  *   - Limit: sizes whose workspace (spec_workspace_size(SPEC_OP_ACCEPT, ...)) exceeds
  *     4 MiB return SPEC_ERR_WORKSPACE at once (e.g. 128256-token rows: up to ~10K nodes).
  *   - Set-up: the first call on a device, with that device current, looks up the array's
- *     device address; make that first call before any stream capture.
+ *     device address; make that first call before any stream capture. The address is
+ *     kept for the life of the process: do not use this entry point on a device after
+ *     cudaDeviceReset (the array is then reloaded elsewhere).
+ *   - Host checks are spec_accept's (the same argument errors, the same limits).
  *   - Every call zeroes the array's counters on `stream` first, then runs the kernels.
  *   - All calls share the one array: calls that may overlap on the GPU (different
  *     streams, or different host threads) race and must be serialised by the caller.

@@ -53,7 +53,6 @@ namespace specv {
 constexpr int kAcceptThreads = 256;
 constexpr int kWalkThreads = 512;
 constexpr int kWalkCluster = 8;
-constexpr int kMaxTreeNodes = 1024;
 constexpr double kTieEps = 1e-6;    // ratio test near-tie band (absolute)
 constexpr double kBonusEps = 1e-8;  // bonus draw near-tie band (relative to the residual's total)
 
@@ -113,9 +112,11 @@ __device__ __forceinline__ void arg_better(float& v, int& i, float v2, int i2) {
 
 // (value, index) as one 64-bit key whose unsigned order is the argmax order: larger
 // value first, then the lower index (the index is stored complemented). Every real key
-// is > 0, so 0 marks an empty slot.
+// is > 0, so 0 marks an empty slot. -0.0 is keyed as +0.0: the two compare equal, so a
+// row whose maximum is zero takes the lowest index holding either (the order bits alone
+// would put -0.0 below +0.0 and let a later task's +0.0 win).
 __device__ __forceinline__ unsigned long long arg_key(float v, int i) {
-  unsigned u = __float_as_uint(v);
+  unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
   u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)u << 32) | (unsigned)(~i);
 }
@@ -1155,20 +1156,22 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     int* am = reinterpret_cast<int*>(wb + w.results);
     const int gch = greedy_chunks(vocab);
     const int tasks = total_nodes * gch;
-    static int per_sm[4] = {0, 0, 0, 0};
+    static PerDevice per_sm[4], sm_n;
     // (the token insert is a separate instance: calls without a token buffer run code that
     // carries none of it, which keeps the streaming kernel's registers as they were)
     const bool ins = ca.ins.token_buf != nullptr;
     auto kern = vec ? (ins ? accept_greedy_kernel<true, true> : accept_greedy_kernel<true, false>)
                     : (ins ? accept_greedy_kernel<false, true> : accept_greedy_kernel<false, false>);
-    int& occ = per_sm[(vec ? 1 : 0) + (ins ? 2 : 0)];
-    if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kAcceptThreads, 0) != cudaSuccess ||
-                     occ < 1))
-      occ = 1;
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess)
-      return SPEC_ERR_CUDA;
+    const int occ = per_device(per_sm[(vec ? 1 : 0) + (ins ? 2 : 0)], [kern](int) {
+      int o = 0;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kAcceptThreads, 0) == cudaSuccess && o > 0 ? o
+                                                                                                               : 1;
+    });
+    const int sms = per_device(sm_n, [](int dev) {
+      int v = 0;
+      return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
+    });
+    if (occ == 0 || sms == 0) return SPEC_ERR_CUDA;
     // one wave, every CTA with the same number of tasks
     const int per_cta = ceil_div(tasks, occ * sms);
     const int grid_n = ceil_div(tasks, per_cta);
@@ -1189,13 +1192,14 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   // dynamic shared memory of the walk: each CTA's slice of p and q (when it fits)
   const int per_cta = ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
   const size_t walk_smem = per_cta <= kWalkStage ? 2 * sizeof(float) * (size_t)per_cta : 0;
-  static bool walk_attr = false;
-  if (!walk_attr) {
-    if (cudaFuncSetAttribute(accept_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(2 * sizeof(float) * kWalkStage)) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    walk_attr = true;
-  }
+  static PerDevice walk_attr;  // the raised shared-memory limit, set once per device
+  if (per_device(walk_attr, [](int) {
+        return cudaFuncSetAttribute(accept_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(2 * sizeof(float) * kWalkStage)) == cudaSuccess
+                   ? 1
+                   : 0;
+      }) == 0)
+    return SPEC_ERR_CUDA;
   if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), walk_smem, stream, parent,
                  tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, (const StatPartial*)part, chunks,
                  accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
@@ -1214,10 +1218,10 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
 //
 // Some callers cannot allocate device memory at all: a runtime that hands out only the
 // tensors it owns, a plugin host with no allocator of its own, a serving loop that
-// forbids allocation once it is running. For them spec_accept_noalloc runs the same
-// kernels as spec_accept with its scratch (counters, chunk partials, per-node results)
-// in the file-scope array below, of fixed size kNoAllocScratchBytes. Every GPU that
-// loads the library holds that array until the process exits.
+// forbids allocation once it is running. For them spec_accept_noalloc (api.cu) runs the
+// same kernels as spec_accept with its scratch (counters, chunk partials, per-node
+// results) in the file-scope array below, of fixed size kNoAllocScratchBytes. Every GPU
+// that loads the library holds that array until the process exits.
 namespace specv {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
@@ -1225,9 +1229,9 @@ static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchB
 
 // Device address of g_accept_scratch for the current device. The symbol's host-side
 // name is only a stand-in, so the address is asked of the runtime, once per device,
-// with that device current. Returns nullptr when the lookup fails.
+// with that device current (the answer stays valid until the device's context is
+// destroyed, e.g. by cudaDeviceReset). Returns nullptr when the lookup fails.
 static void* noalloc_scratch() {
-  constexpr int kMaxDevices = 64;
   static void* ptrs[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
@@ -1241,31 +1245,18 @@ static void* noalloc_scratch() {
   return ptrs[dev];
 }
 
-}  // namespace specv
-
-extern "C" int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_tokens,
-                                   const float* target_logits, const float* draft_logits, const float* uniforms,
-                                   float temperature, int vocab, const int32_t* qo_indptr, int batch,
-                                   int total_nodes, int max_nodes, int path_cap, int32_t* accept_len,
-                                   int32_t* path, int32_t* out_tokens, uint8_t* flags, int32_t* dev_status,
-                                   void* stream) {
-  using namespace specv;
-  if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
-  if (batch < 0 || total_nodes < 0 || vocab <= 0 || path_cap < 1 || max_nodes < 1 || max_nodes > kMaxTreeNodes)
-    return SPEC_ERR_ARG;
-  if (batch == 0) return SPEC_OK;
-  if (total_nodes < batch) return SPEC_ERR_ARG;
-  if (!parent || !draft_tokens || !target_logits || !qo_indptr || !accept_len || !path || !out_tokens)
-    return SPEC_ERR_ARG;
-  if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
+// The fixed scratch as the workspace of an acceptance call of these sizes: SPEC_ERR_WORKSPACE
+// when they need more than it holds, SPEC_ERR_CUDA when its address cannot be had. Its
+// counters and argmax slots are zeroed on `stream` (the array keeps the previous call's
+// contents), so the kernels find them as a fresh workspace would have them.
+int accept_noalloc_scratch(int batch, int total_nodes, int vocab, cudaStream_t stream, void** ws) {
   const AcceptWs w = AcceptWs::make(batch, total_nodes, accept_chunks(total_nodes, vocab));
-  if (w.total > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;  // sizes beyond the fixed scratch
-  void* ws = noalloc_scratch();
-  if (ws == nullptr) return SPEC_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the counters must start at zero
-  if (cudaMemsetAsync(ws, 0, w.partials, st) != cudaSuccess) return SPEC_ERR_CUDA;
-  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
-                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, st, nullptr);
+  if (w.total > kNoAllocScratchBytes) return SPEC_ERR_WORKSPACE;
+  void* p = noalloc_scratch();
+  if (p == nullptr) return SPEC_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, w.partials, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  *ws = p;
+  return SPEC_OK;
 }
+
+}  // namespace specv

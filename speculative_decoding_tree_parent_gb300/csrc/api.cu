@@ -16,12 +16,14 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
                   int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
                   uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream, const CommitArgs* commit);
 size_t accept_ws_bytes(int batch, int total_nodes, int vocab);
+int accept_noalloc_scratch(int batch, int total_nodes, int vocab, cudaStream_t stream, void** ws);
 int launch_attn_simt(int dtype, const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
                      const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
                      const void* k_tree, const void* v_tree, const uint64_t* mask, const int32_t* qo, int batch,
                      int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
                      void* ws, int32_t* status, cudaStream_t stream);
-bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max_nodes);
+bool attn_tc_shape(int dtype, int hq, int hkv, int d, int page_size, int max_nodes);
+bool attn_tc_ready();
 size_t attn_tc_ws_bytes(int batch, int max_nodes, int hq, int hkv, int max_prefix);
 int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, int max_prefix,
@@ -29,7 +31,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                    int total_nodes, int max_nodes, int hq, int hkv, int d, float sm_scale, void* out, float* lse,
                    void* ws, int32_t* status, cudaStream_t stream, const float* kv_scale, const int32_t* parent);
 
-constexpr int kMaxNodes = 1024;
+constexpr int kMaxNodes = kMaxTreeNodes;
 
 static size_t attn_ws_bytes(int batch, int total_nodes, int max_nodes, int hq, int hkv, int d, int max_prefix) {
   const int rows = total_nodes * hq;
@@ -40,6 +42,10 @@ static size_t attn_ws_bytes(int batch, int total_nodes, int max_nodes, int hq, i
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// bf16 inputs with head dim 128 run on the tensor-core kernel and nowhere else; the
+// CUDA-core kernel serves fp32 inputs and head dim 64.
+static bool attn_wants_tc(int dtype, int d) { return dtype == SPEC_BF16 && d == 128; }
 
 }  // namespace specv
 
@@ -91,7 +97,8 @@ int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, 
     return SPEC_ERR_ARG;
   if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
-  const bool tc = attn_tc_supported(dtype, hq, hkv, d, page_size, max_nodes);
+  const bool tc = attn_wants_tc(dtype, d);
+  if (tc && !attn_tc_shape(dtype, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   *tensor_cores = tc ? 1 : 0;
   *splits = tc ? attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix)
                : attn_splits_simt(batch, max_nodes, hq, hkv, max_prefix);
@@ -120,31 +127,38 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
   if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+  const bool tc = attn_wants_tc(dtype, d);
+  if (tc && !attn_tc_shape(dtype, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
   if (!q || !k_tree || !v_tree || !mask || !qo_indptr || !prefix_len || !out) return SPEC_ERR_ARG;
   if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
     return SPEC_ERR_ARG;
   if ((long)max_pages * page_size < max_prefix) return SPEC_ERR_ARG;
+  if (tc && (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(out) ||
+             (max_prefix > 0 && (!aligned16(k_pool) || !aligned16(v_pool)))))
+    return SPEC_ERR_ARG;  // TMA copies need 16-byte aligned tensors
   const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
   if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (attn_tc_supported(dtype, hq, hkv, d, page_size, max_nodes) && aligned16(q) && aligned16(k_pool) &&
-      aligned16(v_pool) && aligned16(k_tree) && aligned16(v_tree) && aligned16(out))
+  if (tc) {
+    if (!attn_tc_ready()) return SPEC_ERR_CUDA;
     return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                           k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale,
                           out, lse, ws, dev_status, st, nullptr, nullptr);
+  }
   return launch_attn_simt(dtype, q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len,
                           max_prefix, k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d,
                           sm_scale, out, lse, ws, dev_status, st);
 }
 
-// Host checks of spec_accept's arguments (SPEC_OK when they pass).
-static int check_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
-                        const float* draft_logits, const float* uniforms, float temperature, int vocab,
-                        const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
-                        const int32_t* accept_len, const int32_t* path, const int32_t* out_tokens, const void* ws,
-                        size_t ws_bytes) {
+// Host checks of spec_accept's arguments other than the workspace (SPEC_OK when they pass);
+// spec_accept_noalloc makes the same checks.
+static int check_accept_args(int mode, const int32_t* parent, const int32_t* draft_tokens,
+                             const float* target_logits, const float* draft_logits, const float* uniforms,
+                             float temperature, int vocab, const int32_t* qo_indptr, int batch, int total_nodes,
+                             int max_nodes, int path_cap, const int32_t* accept_len, const int32_t* path,
+                             const int32_t* out_tokens) {
   if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
   if (batch < 0 || total_nodes < 0 || vocab <= 0 || path_cap < 1 || max_nodes < 1 || max_nodes > kMaxNodes)
     return SPEC_ERR_ARG;
@@ -153,6 +167,19 @@ static int check_accept(int mode, const int32_t* parent, const int32_t* draft_to
   if (!parent || !draft_tokens || !target_logits || !qo_indptr || !accept_len || !path || !out_tokens)
     return SPEC_ERR_ARG;
   if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
+  return SPEC_OK;
+}
+
+// Host checks of spec_accept's arguments (SPEC_OK when they pass).
+static int check_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                        const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                        const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                        const int32_t* accept_len, const int32_t* path, const int32_t* out_tokens, const void* ws,
+                        size_t ws_bytes) {
+  const int rc = check_accept_args(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature,
+                                   vocab, qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path,
+                                   out_tokens);
+  if (rc != SPEC_OK || batch == 0) return rc;
   const size_t need = spec_workspace_size(SPEC_OP_ACCEPT, batch, total_nodes, max_nodes, 0, 0, 0, 0, vocab);
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return SPEC_ERR_WORKSPACE;
   return SPEC_OK;
@@ -188,6 +215,23 @@ int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, co
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
                        dev_status, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
+                        const float* draft_logits, const float* uniforms, float temperature, int vocab,
+                        const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
+                        int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+                        int32_t* dev_status, void* stream) {
+  int rc = check_accept_args(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                             qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens);
+  if (rc != SPEC_OK || batch == 0) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  rc = accept_noalloc_scratch(batch, total_nodes, vocab, st, &ws);
+  if (rc != SPEC_OK) return rc;
+  return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                       qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
+                       dev_status, st, nullptr);
 }
 
 int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
@@ -248,7 +292,7 @@ int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_
       num_pages < 0 || max_pages < 0)
     return SPEC_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
-  if (!attn_tc_supported(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (!attn_tc_shape(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
   if (!q || !k_tree || !v_tree || !mask || !qo_indptr || !prefix_len || !out || !kv_scale) return SPEC_ERR_ARG;
   if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
@@ -260,6 +304,7 @@ int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_
   const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
   if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
+  if (!attn_tc_ready()) return SPEC_ERR_CUDA;
   return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                         k_tree, v_tree, mask, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale, out,
                         lse, ws, dev_status, static_cast<cudaStream_t>(stream), kv_scale, nullptr);
@@ -276,7 +321,7 @@ int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void*
       num_pages < 0 || max_pages < 0)
     return SPEC_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
-  if (!attn_tc_supported(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (!attn_tc_shape(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
   if (!q || !k_tree || !v_tree || !parent || !qo_indptr || !prefix_len || !out) return SPEC_ERR_ARG;
   if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
@@ -288,6 +333,7 @@ int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void*
   const size_t need = spec_workspace_size(SPEC_OP_ATTN, batch, total_nodes, max_nodes, hq, hkv, d, max_prefix, 0);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return SPEC_ERR_WORKSPACE;
   if (sm_scale <= 0.f) sm_scale = 1.0f / sqrtf((float)d);
+  if (!attn_tc_ready()) return SPEC_ERR_CUDA;
   return launch_attn_tc(q, k_pool, v_pool, num_pages, page_size, page_table, max_pages, prefix_len, max_prefix,
                         k_tree, v_tree, nullptr, qo_indptr, batch, total_nodes, max_nodes, hq, hkv, d, sm_scale, out,
                         lse, ws, dev_status, static_cast<cudaStream_t>(stream), nullptr, parent);

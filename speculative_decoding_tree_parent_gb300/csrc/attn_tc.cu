@@ -66,7 +66,7 @@ constexpr int kTcThreads = 64 + kTiles * 128 + 32;  // + one more MMA-issuing wa
 constexpr int kMma1Warp = kTcThreads / 32 - 1;     // the MMA issuer of tile 1
 constexpr int kCvtWarps = 4;                       // FP8 cache: code -> bf16 converters
 constexpr int kF8Stages = 3;
-constexpr int kParMax = 1024;                      // nodes per tree (parent array staged in smem)
+constexpr int kParMax = kMaxTreeNodes;             // nodes per tree (parent array staged in smem)
 constexpr float kRescaleThr = 8.0f;            // log2 units: P entries stay <= 2^8
 constexpr long long kWaitLimit = 4000000000LL;  // cycles (about 2 s) before a wait gives up
 
@@ -804,16 +804,18 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tc_merge_kernel(const TcMe
 
 // ------------------------------------------------------------------------------ host
 
+// The driver's tensor-map encoder, looked up once per process (a thread-safe static; the
+// entry point is the same for every device). nullptr when there is no driver.
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -833,24 +835,25 @@ static bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint6
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
 }
 
-bool attn_tc_supported(int dtype, int hq, int hkv, int d, int page_size, int max_nodes) {
+// The shapes the tensor-core kernel serves (every bf16 call with d = 128 must be one of
+// them: such a call never runs on the CUDA-core kernel instead).
+bool attn_tc_shape(int dtype, int hq, int hkv, int d, int page_size, int max_nodes) {
   if (dtype != SPEC_BF16 || d != kTcD || page_size != 16 || hkv <= 0 || hq % hkv) return false;
   const int G = hq / hkv;
-  return G >= 1 && G <= kTcRows && kTcRows % G == 0 && max_nodes >= 1 && max_nodes <= 1024 &&
-         tensor_map_encoder() != nullptr;
+  return G >= 1 && G <= kTcRows && kTcRows % G == 0 && max_nodes >= 1 && max_nodes <= kMaxTreeNodes;
 }
 
+// The driver entry point that encodes tensor maps was found (false on a host without a
+// CUDA driver): a tensor-core call without it fails with SPEC_ERR_CUDA.
+bool attn_tc_ready() { return tensor_map_encoder() != nullptr; }
+
 static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-                                                   cudaSuccess && v > 0)
-      n = v;
-    else
-      return 152;  // no device visible (sizing on a build machine): the GB300 count
-  }
-  return n;
+  static PerDevice cache;
+  const int n = per_device(cache, [](int dev) {
+    int v = 0;
+    return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
+  });
+  return n > 0 ? n : 152;  // no device visible (sizing on a build machine): the GB300 count
 }
 
 static int tc_mtiles(int max_nodes, int G) { return ceil_div(max_nodes * G, kTcRows); }
@@ -953,8 +956,8 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   }
   const bool par = mask == nullptr && parent != nullptr;
   const int variant = fp8 ? 1 : par ? 2 : 0;
-  static bool attr_set[3] = {false, false, false};
-  if (!attr_set[variant]) {
+  static PerDevice attr_set[3];  // the raised shared-memory limit, set once per device
+  const int attr_ok = per_device(attr_set[variant], [variant](int) {
     const cudaError_t e =
         variant == 1   ? cudaFuncSetAttribute(attn_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               TcCfg<true>::kSmem)
@@ -962,9 +965,9 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
                                               TcCfg<false, true>::kSmem)
                        : cudaFuncSetAttribute(attn_tc_kernel<false, false>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<false>::kSmem);
-    if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    attr_set[variant] = true;
-  }
+    return e == cudaSuccess ? 1 : 0;
+  });
+  if (attr_ok == 0) return SPEC_ERR_CUDA;
   const int splits = attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix);
   const int mtiles = tc_mtiles(max_nodes, G);
   TcParams prm;

@@ -5,9 +5,14 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "spec_verify.h"
 
 namespace specv {
+
+// Most nodes one draft tree may have (every entry point refuses larger max_nodes).
+constexpr int kMaxTreeNodes = 1024;
 
 // First-error-wins report into the caller's status word (nullable).
 __device__ __forceinline__ void report(int32_t* status, int code) {
@@ -93,6 +98,26 @@ __device__ __forceinline__ F2 d_to_f2(double x) {
 }
 // a > b for normalised double-float values (|lo| at most half an ulp of hi).
 __device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+
+// Host-side values that belong to one device: a kernel's raised shared-memory limit
+// (cudaFuncSetAttribute applies to the current device only), its occupancy, the SM count.
+// Kept per device index and read and written under one mutex, so several devices and
+// several host threads each see their own device's value.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+  std::mutex mu;
+  int val[kMaxDevices] = {};  // 0: not known yet
+};
+// The current device's entry, computed by f() (> 0 on success, 0 on failure: asked again on
+// the next call) the first time. Returns 0 when no device is current or f() failed.
+template <typename F>
+inline int per_device(PerDevice& c, F f) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(c.mu);
+  if (c.val[dev] == 0) c.val[dev] = f(dev);
+  return c.val[dev];
+}
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }

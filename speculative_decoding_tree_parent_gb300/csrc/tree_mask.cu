@@ -31,13 +31,13 @@ __global__ void __launch_bounds__(128) tree_mask_kernel(const int32_t* __restric
 #pragma unroll
   for (int w = 0; w < W; ++w) row[w] = 0;
   int dep = 0;
-  bool ok = n <= max_nodes;
-  if (!ok) {
-    report(status, SPEC_ERR_CAPACITY);
-    return;
-  }
+  bool ok = true;
   int cur = i;
-  while (true) {
+  // a sequence longer than max_nodes: its rows are written all-zero with depth -1 (no
+  // stale bits from an earlier call survive for a later attention to read)
+  const bool fits = n <= max_nodes;
+  if (!fits) report(status, SPEC_ERR_CAPACITY);
+  while (fits) {
 #pragma unroll
     for (int w = 0; w < W; ++w)
       if ((cur >> 6) == w) row[w] |= 1ull << (cur & 63);
@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(128) tree_mask_kernel(const int32_t* __restric
     cur = p;
     ++dep;
   }
-  if (!ok) {
-    report(status, SPEC_ERR_PARENT);
+  if (!fits || !ok) {
+    if (fits) report(status, SPEC_ERR_PARENT);
 #pragma unroll
     for (int w = 0; w < W; ++w) row[w] = 0;
     dep = -1;

@@ -93,3 +93,36 @@ def test_host_argument_checks_of_the_newer_entry_points(lib):
     assert lib.spec_tree_verify_attn_parents(*c) in (0, -6)   # no work, or no tensor-core path on this host
     kv8 = (fake, fake, fake, fake) + common(30, 8)[3:]
     assert lib.spec_tree_verify_attn_kv8(*kv8) == -1
+
+
+def test_bf16_head128_runs_on_tensor_cores_only(lib):
+    """A bf16 call with head dim 128 never falls back to the CUDA-core kernel: the plan says
+    tensor cores (even on a host with no driver), shapes the tensor-core kernel does not
+    serve are refused, and so are unaligned tensors. The pointers passed are never
+    dereferenced (each call returns at its host check)."""
+    splits, tc = binding.spec_attn_plan(binding.SPEC_BF16, 1, 64, 32, 8, 128, 16, 4096)
+    assert tc == 1 and splits >= 1
+    for hq, hkv, ps in [(24, 8, 16), (32, 8, 8), (32, 8, 32)]:   # group of 3; pages of 8 and 32
+        with pytest.raises(binding.SpecError) as ei:
+            binding.spec_attn_plan(binding.SPEC_BF16, 1, 64, hq, hkv, 128, ps, 4096)
+        assert ei.value.status == -6
+    # fp32 and head dim 64 stay on the CUDA cores, page size 8 included
+    assert binding.spec_attn_plan(binding.SPEC_F32, 1, 64, 32, 8, 128, 8, 4096)[1] == 0
+    assert binding.spec_attn_plan(binding.SPEC_BF16, 1, 64, 24, 8, 64, 8, 4096)[1] == 0
+
+    fake, odd = ctypes.c_void_p(4096), ctypes.c_void_p(4098)   # 16-byte aligned / not
+
+    def call(q=fake, hq=32, hkv=8, ps=16):
+        return lib.spec_tree_verify_attn(binding.SPEC_BF16, q, fake, fake, 300, ps, fake, 300, fake, 4096, fake,
+                                         fake, fake, fake, 1, 64, 64, hq, hkv, 128, 0.0, fake, None, fake, 1 << 30,
+                                         None, None)
+    assert call(hq=24) == -6          # group of 3
+    assert call(ps=8) == -6           # 8-token pages
+    assert call(q=odd) == -1          # q not 16-byte aligned
+    try:
+        import torch
+        gpu = torch.cuda.is_available()
+    except Exception:
+        gpu = False
+    if not gpu:   # no driver here: the tensor-map encoder is missing, which is an error
+        assert call() == -7
