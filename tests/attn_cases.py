@@ -22,10 +22,11 @@ def sample_rows(inp, n, seed):
     return sorted(rows)
 
 
-def sensitive(dtype, hq, hkv, d, prefixes, sizes, seed, scale=1.0, tree="random", q_scale=1):
+def sensitive(dtype, hq, hkv, d, prefixes, sizes, seed, scale=1.0, tree="random", q_scale=1, v_scale=1):
     """Small batch with peaked softmax (unscaled N(0,1) Q/K) and short prefixes, so the
-    tree keys carry real weight and any wrong mask bit moves the output. q_scale (a power
-    of two, exact in bf16) sharpens the softmax further for long prefixes."""
+    tree keys carry real weight and any wrong mask bit moves the output. q_scale and v_scale
+    (powers of two, exact in bf16) scale Q and V: a sharper softmax for long prefixes, and
+    outputs small enough that bf16's own rounding of them stays well inside 2e-2."""
     sp = W.spec(1, dtype=dtype, batch=len(prefixes), hq=hq, hkv=hkv, d=d, vocab=64, prefix=(0, 0),
                 nodes=(1, 1), qkv_scale=scale, page_layout="shuffled", extra_pages=3)
     inp = W.generate(sp, seed)
@@ -53,13 +54,13 @@ def sensitive(dtype, hq, hkv, d, prefixes, sizes, seed, scale=1.0, tree="random"
     g = lambda *s: f((rng.standard_normal(s) * scale).astype(np.float32))
     return replace(inp, qo_indptr=np.array(qo, np.int32), parent=np.concatenate(parents).astype(np.int32),
                    draft_tokens=np.zeros(T, np.int32), q=g(T, hq, d) * np.float32(q_scale), k_tree=g(T, hkv, d),
-                   v_tree=g(T, hkv, d),
-                   k_pool=g(total, hkv, ps, d), v_pool=g(total, hkv, ps, d), page_table=pt,
+                   v_tree=g(T, hkv, d) * np.float32(v_scale),
+                   k_pool=g(total, hkv, ps, d), v_pool=g(total, hkv, ps, d) * np.float32(v_scale), page_table=pt,
                    prefix_len=np.array(prefixes, np.int32), target_logits=np.zeros((T, 64), np.float32),
                    draft_logits=None, uniforms=None, max_depth=int(max(sizes)))
 
 
-# Long prefixes with peaked softmax (N(0,1) K and V, Q scaled by 4): the key split into
+# Long prefixes with peaked softmax (N(0,1) K, Q scaled by 4, V by 1/4): the key split into
 # many pieces with its merge (19 splits over a 4096-token prefix, group 4), and the
 # wave-model split of a batch that fills the GPU several times over (eight 32768-token
 # prefixes, 128-node trees, group 8: 4 splits), checked against the per-element bound.
@@ -71,5 +72,6 @@ LONG = {
 
 def long_inputs(name):
     hq, hkv, prefixes, sizes, nrows = LONG[name]
-    inp = sensitive("bf16", hq, hkv, 128, prefixes, sizes, seed=300 + len(prefixes), q_scale=4)
+    inp = sensitive("bf16", hq, hkv, 128, prefixes, sizes, seed=300 + len(prefixes), q_scale=4,
+                    v_scale=0.25)
     return inp, (None if nrows is None else sample_rows(inp, nrows, 5))
