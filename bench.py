@@ -221,6 +221,129 @@ def recorded_traffic(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
+# ----------------------------------------------------------------------------- helpers
+
+def sweep_batch(batch, n, seed, dev, vocab=128256, prefix=2048):
+    """A DeviceBatch of the tree-size sweep's shape: the Llama-3-8B heads, `batch` sequences
+    with `prefix`-token prefixes in shuffled 16-token pages and EAGLE-2 trees of n nodes, a
+    `vocab`-token vocabulary. The trees come from the seeded generator (over a small
+    vocabulary, which only shapes them); the K/V pool and the logits are drawn on the device
+    (torch.randn), since their values do not change the kernels' work."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    from speculative_decoding_tree_parent_gb300 import binding as BIND
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
+
+    small = W.generate(W.spec(3, batch=batch, nodes=(n, n), vocab=256, prefix=(0, 0)), seed)
+    ps, hkv, d = small.page_size, small.hkv, small.d
+    per = -(-(prefix + n) // ps)
+    pages = batch * per + 3
+    rng = np.random.default_rng(seed)
+    pt = rng.permutation(pages)[: batch * per].reshape(batch, per).astype(np.int32)
+    inp = dataclasses.replace(small, prefix_len=np.full(batch, prefix, np.int32), page_table=pt,
+                              k_pool=np.zeros((1, hkv, ps, d), np.float32), v_pool=np.zeros((1, hkv, ps, d), np.float32))
+    db = DeviceBatch(inp, device=dev, mode="greedy")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    db.k_pool = torch.randn((pages, hkv, ps, d), generator=gen, device=dev).to(torch.bfloat16)
+    db.v_pool = torch.randn((pages, hkv, ps, d), generator=gen, device=dev).to(torch.bfloat16)
+    db.target_logits = torch.randn((inp.total_nodes, vocab), generator=gen, device=dev)
+    acc_ws = BIND.spec_workspace_size(BIND.SPEC_OP_ACCEPT, inp.batch, inp.total_nodes, inp.max_nodes, 0, 0, 0, 0,
+                                      vocab)
+    db.acc_ws = torch.zeros(max(acc_ws, 256), dtype=torch.uint8, device=dev)
+    return db
+
+
+def time_graph(fn, stream, flush_l2, warmup, n):
+    """Median µs of one replay of a CUDA graph of fn(), each replay after an L2 flush."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    ts = []
+    for r in range(warmup + n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush_l2()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        if r >= warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    del g
+    return statistics.median(ts)
+
+
+def workload_calls(idx, dev, stream, flush_l2, warmup, n):
+    """Per-call times of workload idx at full size (one replica; its inputs exceed the L2):
+    attention (bf16 cache and FP8 cache) with its % of roofline, and the fused acceptance +
+    commit in the workload's own mode. The kernels at scale, beside the headline workload."""
+    import torch
+
+    from speculative_decoding_tree_parent_gb300 import workloads as W
+    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
+
+    inp = W.generate_index(idx)
+    mode = W.SPECS[idx].modes[0]
+    hbm, tfl, _, _ = _peaks()
+    wc = work_counts(inp, mode=mode)
+    out = {"workload": WORKLOADS[idx].split(":")[0], "mode": mode}
+    db = DeviceBatch(inp, device=dev, mode=mode)
+    db.build_mask()
+    splits, _ = db.attn_plan()
+    for name, dbx, nbytes in (("attn", db, wc["attn_bytes"]), ("attn_fp8kv", None, wc["attn_bytes_fp8kv"])):
+        if dbx is None:
+            dbx = DeviceBatch(inp, device=dev, mode=mode, kv_fp8=True)
+            dbx.build_mask()
+        us = time_graph(dbx.attention, stream, flush_l2, warmup, n)
+        t = us * 1e-6
+        tensor_bound = wc["attn_flops"] / (tfl * 1e12) > nbytes / (hbm * 1e9)
+        out[name] = {"us": us, "tflops": wc["attn_flops"] / t / 1e12, "gbs": nbytes / t / 1e9,
+                     "bound": "tensor" if tensor_bound else "hbm",
+                     "roofline_frac": max(wc["attn_flops"] / (tfl * 1e12), nbytes / (hbm * 1e9)) / t}
+        assert dbx.device_status() == 0
+        if dbx is not db:
+            del dbx
+    out["attn"]["splits"] = splits
+    us = time_graph(lambda: db.accept_commit(mode), stream, flush_l2, warmup, n)
+    wc = work_counts(inp, db.accept_len.cpu().numpy(), mode)
+    nb = wc["accept_bytes"] + wc["commit_bytes"]
+    out["accept_commit"] = {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "hbm_frac": nb / (us * 1e-6) / (hbm * 1e9)}
+    assert db.device_status() == 0
+    del db
+    torch.cuda.empty_cache()
+    return out
+
+
+def tree_sweep_table(dev, stream, flush_l2, warmup, n, batches=(1, 8, 32, 64, 128), sizes=(64, 32, 16)):
+    """µs of one verification step (mask, attention, greedy accept + commit) by batch and
+    draft-tree size ("EAGLE-2 deep dive", production section: shrink the tree 64 -> 32 -> 16
+    as concurrency grows). The cost side only: the benefit (tokens accepted per step) needs
+    the draft model, outside this path."""
+    import torch
+
+    rows = []
+    for batch in batches:
+        for nodes in sizes:
+            db = sweep_batch(batch, nodes, 3000 + batch * 100 + nodes, dev)
+            us = time_graph(lambda: db.step("greedy"), stream, flush_l2, warmup, n)
+            assert db.device_status() == 0
+            rows.append({"batch": batch, "tree_nodes": nodes, "step_us": us, "us_per_sequence": us / batch,
+                         "tree_tokens_per_s": db.T / (us * 1e-6), "splits": db.attn_plan()[0]})
+            del db
+            torch.cuda.empty_cache()
+    return rows
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -432,6 +555,16 @@ def run_ours(args):
                 "topk": 10, "max_depth": 8, "vocab": inp.vocab,
                 "gbs": inp.batch * inp.vocab * 4 * (n_tree - 1) / (t_us * 1e-6) / 1e9}
 
+    # ---- the kernels at scale: per-call times of the batched and the tensor-bound workloads,
+    # and the verification step by batch and tree size (headline run on one GPU only)
+    extras = {}
+    if idx == CONFIG_INDEX and ws == 1 and not args.no_extras:
+        nrep = max(3, min(args.steps, 10))
+        extras["workloads"] = {str(i): workload_calls(i, dev, stream, flush_l2, 3, nrep) for i in (3, 4)}
+        extras["tree_sweep"] = {"config": "Llama-3-8B heads, prefix 2048 (shuffled pages), EAGLE-2 trees, vocab "
+                                          "128256, mask + attention + greedy accept + commit, median step µs",
+                                "table": tree_sweep_table(dev, stream, flush_l2, 3, nrep, batches=(1, 32, 64, 128))}
+
     # ---- figures ------------------------------------------------------------------------
     wc = work_counts(inp, db.accept_len.cpu().numpy(), mode)
     hbm, tfl, tfl_sus, peak_kind = _peaks()
@@ -500,6 +633,7 @@ def run_ours(args):
         "gpu_launches": (launches + call_launches) * args.steps,
         "clocks": clk.summary(),
     }
+    line.update(extras)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds, mode)
     if ws > 1:
@@ -512,61 +646,14 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- tree-size sweep
 
 def run_tree_sweep(args):
-    """Verification step cost by batch and draft-tree size ("EAGLE-2 deep dive", production
-    section: past about 32 concurrent requests verification turns compute-bound, so the tree
-    should shrink 64 -> 32 -> 16 as the batch grows, and speculation stop above 64). Each
-    case: the Llama-3-8B head shape, 2048-token prefixes, EAGLE-2 trees of N nodes, a
-    128256-token vocabulary (device-generated N(0,1) logits; the acceptance reads every row
-    once, whatever its values), one step = mask + attention + greedy accept + commit, timed
-    as CUDA-graph replays after an L2 flush. Reports the cost side only: the benefit side
-    (tokens accepted per step) needs the draft model, which is outside this path."""
+    """The tree-size sweep alone (batches 1-128 x trees of 64 / 32 / 16 nodes), one JSON line."""
     import torch
-
-    from speculative_decoding_tree_parent_gb300 import binding as BIND
-    from speculative_decoding_tree_parent_gb300 import workloads as W
-    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_BYTES, dtype=torch.uint8, device=dev)
-    vocab = 128256
-    rows = []
-    for batch in (1, 8, 32, 64, 128):
-        for n in (64, 32, 16):
-            inp = W.generate(W.spec(3, batch=batch, nodes=(n, n), vocab=256, prefix=(2048, 2048)),
-                             3000 + batch * 100 + n)
-            db = DeviceBatch(inp, device=dev, mode="greedy")
-            gen = torch.Generator(device=dev)
-            gen.manual_seed(batch * 1000 + n)
-            db.target_logits = torch.randn((inp.total_nodes, vocab), generator=gen, device=dev)
-            acc_ws = BIND.spec_workspace_size(BIND.SPEC_OP_ACCEPT, inp.batch, inp.total_nodes, inp.max_nodes,
-                                              0, 0, 0, 0, vocab)
-            db.acc_ws = torch.zeros(max(acc_ws, 256), dtype=torch.uint8, device=dev)
-            with torch.cuda.stream(stream):
-                db.step("greedy")
-            torch.cuda.synchronize()
-            assert db.device_status() == 0
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                db.step("greedy")
-            ts = []
-            for r in range(args.warmup + args.steps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(stream):
-                    flush.zero_()
-                    a.record(stream)
-                    g.replay()
-                    b.record(stream)
-                b.synchronize()
-                if r >= args.warmup:
-                    ts.append(a.elapsed_time(b) * 1e3)
-            us = statistics.median(ts)
-            rows.append({"batch": batch, "tree_nodes": n, "step_us": us, "us_per_sequence": us / batch,
-                         "tree_tokens_per_s": inp.total_nodes / (us * 1e-6),
-                         "mean_prefix": float(inp.prefix_len.mean())})
-            del db, g
-            torch.cuda.empty_cache()
+    rows = tree_sweep_table(dev, stream, lambda: flush.zero_(), args.warmup, args.steps)
     print(json.dumps({"metric": "verification step us by batch and draft-tree size (cost side)",
                       "unit": "us", "higher_is_better": False, "data": "synthetic",
                       "config": {"workload": "Llama-3-8B head shape, prefix 2048, EAGLE-2 trees, vocab 128256, "
@@ -661,6 +748,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="leave out the per-call times of workloads 3 and 4 and the tree-size sweep")
     ap.add_argument("--tree-sweep", action="store_true",
                     help="print the verification step cost by batch and draft-tree size (64 / 32 / 16) instead")
     ap.add_argument("--workload", type=int, default=CONFIG_INDEX, choices=sorted(WORKLOADS),

@@ -867,7 +867,10 @@ static int tc_mtiles(int max_nodes, int G) { return ceil_div(max_nodes * G, kTcR
 //   ceil(items * S / SMs) * (ceil(blocks / S) + 4), where blocks = the longest sequence's
 //   key blocks and 4 blocks stand for a CTA's fixed cost (prologue, partials, merge share).
 //   A batch of long sequences of equal length then stops losing its last, partly filled
-//   wave.
+//   wave. The keys are split only when that modelled cost falls at least 8% below the
+//   unsplit one: the merge kernel is not in the model, and a split that gains less loses
+//   to it (batch 64, 2048-token prefixes, 64-node trees: 2 splits modelled 1% better,
+//   measured 6% slower).
 // At least two key blocks per split, at most 32 splits. The split merge waits for the
 // whole attention grid (programmatic launch releases it only once every attention CTA
 // has started), so any number of waves is safe.
@@ -889,6 +892,8 @@ int attn_splits_tc(int batch, int max_nodes, int hq, int hkv, int max_prefix) {
         s = c;
       }
     }
+    const long unsplit = ((items + sms - 1) / sms) * (blocks + 4);
+    if (s > 1 && best * 100 > unsplit * 92) s = 1;  // less than an 8% modelled gain
   }
   if (s > blocks / 2) s = blocks / 2;
   if (s > kMaxSplits) s = kMaxSplits;

@@ -605,6 +605,31 @@ def test_accept_workspace_shared_across_sizes(inputs):
     assert int(ws[:256].sum()) == 0
 
 
+# ------------------------------------------------------------ tree-size sweep shapes
+
+@pytest.mark.parametrize("nodes", [16, 32])
+def test_tree_sweep_shapes(nodes):
+    """The shapes of the tree-size sweep ("EAGLE-2 deep dive", production section: smaller
+    trees as the batch grows): 64 sequences, 2048-token prefixes, EAGLE-2 trees of 16 or 32
+    nodes. Mask and greedy accept + commit against the oracle exactly, attention on sampled
+    rows against the per-element bound (with its negative controls)."""
+    inp = W.generate(W.spec(3, batch=64, nodes=(nodes, nodes), vocab=4096, prefix=(2048, 2048)), 77 + nodes)
+    db = DeviceBatch(inp)
+    db.step("greedy")
+    torch.cuda.synchronize()
+    assert _status(db) == 0
+    mask, depth, words = _oracle_mask(inp)
+    assert np.array_equal(_mask_np(db), words)
+    _attn_check(inp, db.out, rows=_sample_rows(inp, 64, nodes), splits=db.attn_plan()[0])
+    ref = _oracle_accept(inp, "greedy")
+    assert _accept_compare(db, ref) == 0
+    k2, v2, seq = oracle.kv_commit(inp.k_pool, inp.v_pool, inp.page_table, inp.prefix_len, inp.k_tree, inp.v_tree,
+                                   ref.path, ref.accept_len, inp.qo_indptr, inp.page_size)
+    assert np.array_equal(db.k_pool.float().cpu().numpy(), k2)
+    assert np.array_equal(db.v_pool.float().cpu().numpy(), v2)
+    assert np.array_equal(db.seq_len.cpu().numpy(), seq)
+
+
 # ------------------------------------------------------------------- 256-node trees
 
 def _large_tree_inputs(kind):

@@ -4,7 +4,7 @@ Greedy: hand-worked golden cases; brute force over every root-to-node path on
 tiny trees (a path is accepted iff each edge's token is its parent's target
 argmax); the linear-draft special case; emitted count <= depth + 1.
 
-Stochastic: hand-worked golden cases; Monte-Carlo on a vocabulary of 8 showing
+Stochastic: hand-worked golden cases; Monte-Carlo (10^6 trials each) on a vocabulary of 8 showing
 the method is lossless when draft tokens are drawn i.i.d. from the draft
 distribution — the first emitted token follows p_root, the first two follow
 p_root(x1) * p_x1(x2) — and the single-draft acceptance rate equals the closed
@@ -21,6 +21,8 @@ from scipy import stats
 from scipy.special import softmax
 
 import oracle
+
+import mc_accept
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -141,10 +143,6 @@ def test_stochastic_golden():
         assert res.flags[0] == 0
 
 
-def _dist(rng, V, sharp):
-    return softmax(sharp * rng.standard_normal(V))
-
-
 def _chisq_ok(counts, probs, alpha=1e-3):
     exp = probs * counts.sum()
     keep = exp > 0
@@ -152,91 +150,61 @@ def _chisq_ok(counts, probs, alpha=1e-3):
     return stats.chisquare(counts[keep], exp[keep]).pvalue > alpha
 
 
+# Monte-Carlo pins: 10^6 trials each, in chunks run by a pool of spawned worker processes
+# (the oracle is a plain per-sequence loop; the chunks only split the trials)
+MC_TRIALS = 1_000_000
+MC_CHUNKS = 16
+
+
+def _mc_run(fn, args):
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    workers = max(1, min(len(args), os.cpu_count() or 1))
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        return list(ex.map(fn, args))
+
+
 @pytest.mark.parametrize("k", [1, 2, 3])
 def test_stochastic_first_token_follows_target(k):
-    """Root with k children whose tokens are drawn i.i.d. from q_root: the first emitted
-    token (accepted child's token, or the residual bonus) is distributed as p_root."""
-    rng = np.random.default_rng(10 + k)
-    V, trials = 8, 60000
-    p = _dist(rng, V, 1.0)
-    q = _dist(rng, V, 1.5)
-    n = k + 1
-    parent = np.tile(np.array([-1] + [0] * k), trials)
-    toks = np.zeros((trials, n), np.int64)
-    toks[:, 1:] = rng.choice(V, size=(trials, k), p=q)
-    tl = np.tile(np.log(p), (trials * n, 1))
-    dl = np.tile(np.log(q), (trials * n, 1))
-    u = rng.random((trials * n, 2)).astype(np.float32)
-    qo = np.arange(trials + 1) * n
-    res = oracle.stochastic_accept(parent, toks.ravel(), tl, dl, u, 1.0, qo, path_cap=n)
-    first = res.out_tokens[:, 0]
-    assert _chisq_ok(np.bincount(first, minlength=V), p)
+    """Root with k children whose tokens are drawn i.i.d. from q_root: over 10^6 trials the
+    first emitted token (accepted child's token, or the residual bonus) is distributed as
+    p_root (chi-square p > 1e-3)."""
+    per = MC_TRIALS // MC_CHUNKS
+    out = _mc_run(mc_accept.first_token_chunk, [(k, per, 1000 * k + c) for c in range(MC_CHUNKS)])
+    counts = sum(o[0] for o in out)
+    accepted = sum(o[1] for o in out)
+    p, q = mc_accept.first_token_dists(k)
+    assert counts.sum() == MC_TRIALS
+    assert _chisq_ok(counts, p)
     if k == 1:
         # single draft: acceptance probability sum_x min(p(x), q(x))
-        rate = (res.accept_len == 1).mean()
+        rate = accepted / MC_TRIALS
         want = np.minimum(p, q).sum()
-        assert abs(rate - want) < 4.5 * np.sqrt(want * (1 - want) / trials)
+        assert abs(rate - want) < 4.5 * np.sqrt(want * (1 - want) / MC_TRIALS)
 
 
 def test_stochastic_first_token_fails_without_residual():
     """Power check of the Monte-Carlo pin: a sampler that draws the bonus from p instead
-    of the residual is detected by the same statistic."""
+    of the residual is detected by the same statistic at the same number of trials."""
     rng = np.random.default_rng(11)
-    V, trials = 8, 60000
-    p = _dist(rng, V, 1.0)
-    q = _dist(rng, V, 1.5)
-    x = rng.choice(V, size=trials, p=q)
-    u = rng.random(trials)
+    p, q = mc_accept.first_token_dists(1)
+    V = p.shape[0]
+    x = rng.choice(V, size=MC_TRIALS, p=q)
+    u = rng.random(MC_TRIALS)
     acc = u < p[x] / q[x]
-    wrong = np.where(acc, x, rng.choice(V, size=trials, p=p))
+    wrong = np.where(acc, x, rng.choice(V, size=MC_TRIALS, p=p))
     assert not _chisq_ok(np.bincount(wrong, minlength=V), p)
 
 
 def test_stochastic_two_tokens_joint():
-    """Depth-2 trees (2 children per node, tokens i.i.d. from the node's draft
-    distribution; target/draft logits of a node depend only on its token path):
-    the first two emitted tokens follow p_root(x1) * p_x1(x2). When a step emits only
-    one token, the second comes from the next step, a tree that is just its root."""
-    rng = np.random.default_rng(21)
-    V, trials, k = 6, 60000, 2
-    p_root, q_root = _dist(rng, V, 1.0), _dist(rng, V, 1.0)
-    p_x = np.stack([_dist(rng, V, 1.0) for _ in range(V)])
-    q_x = np.stack([_dist(rng, V, 1.0) for _ in range(V)])
-    # node layout: 0 root; 1..k children; then k grandchildren per child
-    parent = [-1] + [0] * k
-    for c in range(1, k + 1):
-        parent += [c] * k
-    parent = np.array(parent)
-    n = len(parent)
-    toks = np.zeros((trials, n), np.int64)
-    toks[:, 1 : k + 1] = rng.choice(V, size=(trials, k), p=q_root)
-    tl = np.zeros((trials, n, V))
-    dl = np.zeros((trials, n, V))
-    tl[:, 0], dl[:, 0] = np.log(p_root), np.log(q_root)
-    for c in range(1, k + 1):
-        x = toks[:, c]
-        tl[:, c], dl[:, c] = np.log(p_x[x]), np.log(q_x[x])
-        for j in range(k):
-            gc = k + 1 + (c - 1) * k + j
-            u = rng.random(trials)
-            cdf = np.cumsum(q_x[x], axis=1)
-            toks[:, gc] = np.minimum((cdf < u[:, None]).sum(1), V - 1)
-            tl[:, gc] = dl[:, gc] = 0.0
-    u = rng.random((trials * n, 2)).astype(np.float32)
-    qo = np.arange(trials + 1) * n
-    res = oracle.stochastic_accept(np.tile(parent, trials), toks.ravel(), tl.reshape(-1, V),
-                                   dl.reshape(-1, V), u, 1.0, qo, path_cap=n)
-    x1 = res.out_tokens[:, 0].copy()
-    x2 = res.out_tokens[:, 1].copy()
-    short = res.accept_len == 0
-    m = int(short.sum())
-    nxt = oracle.stochastic_accept(np.full(m, -1), np.zeros(m, np.int64), np.log(p_x[x1[short]]),
-                                   np.log(p_x[x1[short]]), rng.random((m, 2)).astype(np.float32),
-                                   1.0, np.arange(m + 1), path_cap=1)
-    x2[short] = nxt.out_tokens[:, 0]
-    joint = np.bincount(x1 * V + x2, minlength=V * V)
-    want = (p_root[:, None] * p_x).ravel()
-    assert _chisq_ok(joint, want)
+    """Depth-2 trees: over 10^6 trials the first two emitted tokens follow
+    p_root(x1) * p_x1(x2) (chi-square p > 1e-3); see mc_accept.joint_chunk."""
+    per = MC_TRIALS // MC_CHUNKS
+    joint = sum(_mc_run(mc_accept.joint_chunk, [(per, 5000 + c) for c in range(MC_CHUNKS)]))
+    p_root, _, p_x, _ = mc_accept.joint_dists()
+    assert joint.sum() == MC_TRIALS
+    assert _chisq_ok(joint, (p_root[:, None] * p_x).ravel())
 
 
 def test_stochastic_equal_distributions_accept_first_child():
