@@ -165,6 +165,30 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t& lo, uint3
   hi = e4m3x2_lanes_to_bf16x2(b);
 }
 
+// Two fp32 lanes per instruction (packed f32x2 on this architecture); each lane is the
+// scalar operation, rounded to nearest.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mov.b64 rc, {%6, %7};"
+      " fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; add.rn.f32x2 rd, ra, rb;"
+      " mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -604,14 +628,17 @@ __global__ void __launch_bounds__(TcCfg<kFp8, kPar>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c] = ((bits >> c) & 1ull) ? sv[c] : -INFINITY;
         }
-        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+        // row max in four chains of three-input maxima (exact, any order)
+        float mxc[4];
 #pragma unroll
-        for (int c = 4; c < kTcKeys; c += 4) {
-          mx0 = fmaxf(mx0, sv[c]);
-          mx1 = fmaxf(mx1, sv[c + 1]);
-          mx2 = fmaxf(mx2, sv[c + 2]);
-          mx3 = fmaxf(mx3, sv[c + 3]);
+        for (int q = 0; q < 4; ++q) {
+          const float* v = sv + 16 * q;
+          float m = fmax3(v[0], v[1], v[2]);
+#pragma unroll
+          for (int c = 3; c < 15; c += 2) m = fmax3(m, v[c], v[c + 1]);
+          mxc[q] = fmaxf(m, v[15]);
         }
+        const float mx0 = mxc[0], mx1 = mxc[1], mx2 = mxc[2], mx3 = mxc[3];
         const bool pre8 = kFp8 && j < npb;
         const float sc = pre8 ? sl2_pre : sl2;
         const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sc;  // sm_scale, scales > 0
@@ -625,21 +652,22 @@ __global__ void __launch_bounds__(TcCfg<kFp8, kPar>::kThreads, 1)
         float negm = m_run == -INFINITY ? 0.f : -m_run;  // all scores are -inf then
         if (pre8) negm += lvs_pre;
         uint32_t packed[kTcKeys / 2];
-        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+        // exponent arguments and row sums two lanes at a time (packed f32x2); per lane the
+        // same roundings, in the same order, as the scalar form
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(negm, negm);
+        float2 r01 = make_float2(0.f, 0.f), r23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kTcKeys; c += 4) {
-          const float p0 = ex2_approx(fmaf(sv[c], sc, negm));
-          const float p1 = ex2_approx(fmaf(sv[c + 1], sc, negm));
-          const float p2 = ex2_approx(fmaf(sv[c + 2], sc, negm));
-          const float p3 = ex2_approx(fmaf(sv[c + 3], sc, negm));
-          r0 += p0;
-          r1 += p1;
-          r2 += p2;
-          r3 += p3;
-          packed[c >> 1] = pack_bf16x2(p0, p1);
-          packed[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+          const float2 x01 = ffma2(make_float2(sv[c], sv[c + 1]), sc2, nm2);
+          const float2 x23 = ffma2(make_float2(sv[c + 2], sv[c + 3]), sc2, nm2);
+          const float2 p01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+          const float2 p23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+          r01 = fadd2(r01, p01);
+          r23 = fadd2(r23, p23);
+          packed[c >> 1] = pack_bf16x2(p01.x, p01.y);
+          packed[(c >> 1) + 1] = pack_bf16x2(p23.x, p23.y);
         }
-        float rsum = (r0 + r1) + (r2 + r3);
+        float rsum = (r01.x + r01.y) + (r23.x + r23.y);
         if (pre8) rsum *= ivs_pre;
         l = l * alpha + rsum;
         if (j >= 1) {  // PV of the previous block done: O is stable
