@@ -490,8 +490,9 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
     // this CTA has streamed its tasks: the next kernel may be scheduled -- unless this
     // launch also commits K/V, which a next kernel may read before it waits
     if (ca.k_tree == nullptr) pdl_trigger();
-    __threadfence();
-    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    unsigned prev;  // one release-acquire RMW: this CTA's slot updates are visible before its count
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(prev) : "l"(done) : "memory");
+    s_last = prev == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
@@ -1172,9 +1173,11 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
       return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
     });
     if (occ == 0 || sms == 0) return SPEC_ERR_CUDA;
-    // one wave, every CTA with the same number of tasks
-    const int per_cta = ceil_div(tasks, occ * sms);
-    const int grid_n = ceil_div(tasks, per_cta);
+    // one wave with the same number of CTAs on every SM: tasks go round-robin to the CTAs, so
+    // each SM's share differs from another's by at most one task per CTA it holds (a grid that
+    // is not a multiple of the SM count leaves some SMs with one CTA -- and its tasks -- more)
+    const int ctas_sm = occ < ceil_div(tasks, sms) ? occ : ceil_div(tasks, sms);
+    const int grid_n = ctas_sm * sms;
     if (launch_pdl(kern, dim3((unsigned)grid_n), dim3(kAcceptThreads), 0, stream, tl, vocab, gch, tasks, qo, batch,
                    total_nodes, parent, tokens, path_cap, accept_len, path, out_tokens, flags, counter,
                    total_nodes <= kArgSlots ? reinterpret_cast<unsigned long long*>(wb + w.slots) : nullptr, part, am,
