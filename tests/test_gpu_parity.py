@@ -218,6 +218,41 @@ def test_attention_long_prefix_peaked(name):
     _attn_check(inp, db.out, rows=rows, splits=splits)
 
 
+def _lpt_inputs():
+    """40 sequences of unequal length with repeated lengths (rank ties broken by sequence id),
+    empty prefixes and one-node trees: an unsplit launch of 80 work items, which takes the
+    longest-first instance."""
+    prefixes = [0, 16, 33, 64, 200, 200, 200, 500, 0, 47] * 4
+    sizes = [1, 5, 12, 3, 30, 30, 7, 64, 2, 17] * 4
+    return _sensitive("bf16", 8, 2, 128, prefixes, sizes, seed=404)
+
+
+def test_attention_longest_first_dispatch():
+    """The longest-first instances (bf16 cache, FP8 cache, parent array) against the oracle
+    in full, and bit-identical to each other where they must be (mask + attention against the
+    attention that builds the mask)."""
+    inp = _lpt_inputs()
+    db = DeviceBatch(inp)
+    assert db.attn_plan() == (1, 1)   # unsplit, tensor cores: the longest-first instance
+    db.build_mask()
+    db.attention()
+    fused = DeviceBatch(inp)
+    fused.attention_parents()
+    torch.cuda.synchronize()
+    assert _status(db) == 0 and _status(fused) == 0
+    _attn_check(inp, db.out, splits=1)
+    assert torch.equal(db.out, fused.out)
+    f8 = DeviceBatch(inp, kv_fp8=True)
+    f8.build_mask()
+    f8.attention()
+    torch.cuda.synchronize()
+    assert f8.device_status() == 0
+    kc, vc, sc = f8.kv_codes
+    mask, _, _ = _oracle_mask(inp)
+    ref, _, A = AT.reference(inp, mask, pools=(kc, vc), kv_scale=sc)
+    AT.check(f8.out.float().cpu().numpy(), ref, A, "longest-first, FP8 cache")
+
+
 def test_attention_chain_equals_causal():
     """Chain trees: the GPU result against causal attention over prefix + chain
     (oracle already pinned to torch SDPA; here the GPU is checked on the same inputs)."""
