@@ -70,10 +70,15 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(
     const bool is_tree = blk >= sr.n_prefix_blocks;
     const int key0 = is_tree ? (blk - sr.n_prefix_blocks) * KB : blk * KB;
     const int nvalid = is_tree ? min(KB, N - key0) : min(KB, P - key0);
-    __syncthreads();  // previous tile fully consumed
-    for (int idx = tid; idx < KB * D; idx += blockDim.x) {
+    // the tile's K/V into registers (every load of the tile in flight at once), then shared memory
+    constexpr int kPer = KB * D / (kSimtWarps * 32);
+    float kr[kPer], vr[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = tid + u * kSimtWarps * 32;
       const int j = idx / D, d = idx - (idx / D) * D;
-      float kv = 0.f, vv = 0.f;
+      kr[u] = 0.f;
+      vr[u] = 0.f;
       if (j < nvalid) {
         size_t off;
         bool ok = true;
@@ -89,12 +94,18 @@ __global__ void __launch_bounds__(kSimtWarps * 32) attn_simt_kernel(
           off = ((size_t)(base + key0 + j) * hkv + g) * D + d;
         }
         if (ok) {
-          kv = to_f32(is_tree ? k_tree[off] : k_pool[off]);
-          vv = to_f32(is_tree ? v_tree[off] : v_pool[off]);
+          kr[u] = to_f32(is_tree ? k_tree[off] : k_pool[off]);
+          vr[u] = to_f32(is_tree ? v_tree[off] : v_pool[off]);
         }
       }
-      sk[j][d] = kv;
-      sv[j][d] = vv;
+    }
+    __syncthreads();  // previous tile fully consumed
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = tid + u * kSimtWarps * 32;
+      const int j = idx / D, d = idx - (idx / D) * D;
+      sk[j][d] = kr[u];
+      sv[j][d] = vr[u];
     }
     if (is_tree && tid < R) {
       const int row = row0 + tid;
@@ -193,7 +204,10 @@ int attn_splits_simt(int batch, int max_nodes, int hq, int hkv, int max_prefix) 
   const long base = (long)batch * hkv * row_blocks;
   const int blocks = ceil_div(max_prefix, kSimtKeys) + ceil_div(max_nodes, kSimtKeys);
   int s = (int)((2L * 152 + base - 1) / (base > 0 ? base : 1));
-  const int cap = blocks / 4 > 1 ? blocks / 4 : 1;
+  // at least four 32-key tiles per split, except for grids far too small to fill the GPU
+  // (a handful of row blocks): there one tile per split, as the tiles are the only parallelism
+  const int per = base * 4 <= 152 ? 1 : 4;
+  const int cap = blocks / per > 1 ? blocks / per : 1;
   if (s > cap) s = cap;
   if (s > 64) s = 64;
   return s < 1 ? 1 : s;
