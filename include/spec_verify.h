@@ -14,7 +14,8 @@
  * boundary fewer). spec_tree_verify_attn_parents runs the first two as one call (the mask
  * built inside the attention from the parent array). spec_tree_verify_attn_kv8 and
  * spec_kv_commit_kv8 are the attention and the commit over an FP8 (E4M3) paged cache;
- * spec_tree_init / spec_tree_expand build the draft tree on the device;
+ * spec_tree_init / spec_tree_expand (/ spec_tree_expand_multi) build the draft tree on
+ * the device;
  * spec_accept_noalloc is spec_accept without a workspace argument.
  *
  * Sources of the operations (page title, then section):
@@ -334,6 +335,46 @@ int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride,
                      int batch, int max_nodes, int topk, int max_depth, double threshold, void* state,
                      size_t state_bytes, int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out,
                      int32_t* next_node, uint8_t* flags, int32_t* dev_status, void* stream);
+
+/*
+ * spec_tree_expand_multi -- the same construction, several draft rows per call.
+ *   ("EAGLE-2 deep dive", section on the dynamic draft-tree algorithm, as above; the batching
+ *   is this library's and leaves the tree unchanged.)
+ *   A queued candidate's expansion (its draft row's top-k and probabilities) depends only on
+ *   the candidate -- its parent node and its token -- not on when it is popped. So each call
+ *   lists up to `width` requests per sequence for the next call: request 0 is the node
+ *   awaiting its expansion (the last node created), requests 1.. are the best queued
+ *   candidates (largest score first, earlier push on ties) that have no row yet and sit
+ *   below the depth limit. The caller's draft model writes one row per request (for a
+ *   candidate: the row of the node it would become, given its parent and token). The next
+ *   call reduces every row, keeps each candidate's result, expands the awaiting node and
+ *   pops exactly as spec_tree_expand would, expanding at once every popped node whose result
+ *   it holds; it stops at the first popped node that needs a row it has not got, or when the
+ *   tree is complete. The tree (parent_out, tokens_out, n_nodes_out, flags) is therefore
+ *   spec_tree_expand's, node for node, for every width; width 1 is spec_tree_expand.
+ *
+ *   After spec_tree_init the request list is the root alone (row 0).
+ *   draft_logits  float; row j of sequence b starts at draft_logits + b * row_stride +
+ *                 j * req_stride (elements); rows j >= req_n[b] are not read.
+ *   width         in [1, 8]: the same for every call on one state (a state listing more
+ *                 requests than the call's width is refused: SPEC_ERR_ARG in *dev_status,
+ *                 nothing changes). topk, max_depth and threshold as for spec_tree_expand,
+ *                 also the same for every call on one state.
+ *   state         as for spec_tree_expand (spec_tree_init's), driven by this call only.
+ *   req_parent, req_token  int32 [batch][width] (out): the parent node id (-1 for the root)
+ *                 and token of each request; -1 past req_n[b].
+ *   req_n         int32 [batch] (out): requests listed; 0 once the tree is complete.
+ *   next_node     int32 [batch] (out): the awaiting node (request 0), -1 once complete.
+ *   A sequence whose tree is complete is skipped: its outputs keep their last values.
+ *   Device errors: SPEC_ERR_ARG as above; SPEC_ERR_CAPACITY if the state's result entries
+ *   ran out (they cannot: max_nodes * 8 entries, and each call takes at most width while
+ *   creating at least one node), the tree then ends.
+ */
+int spec_tree_expand_multi(const float* draft_logits, int vocab, long long row_stride, long long req_stride,
+                           int batch, int max_nodes, int width, int topk, int max_depth, double threshold,
+                           void* state, size_t state_bytes, int32_t* parent_out, int32_t* tokens_out,
+                           int32_t* n_nodes_out, int32_t* next_node, int32_t* req_parent, int32_t* req_token,
+                           int32_t* req_n, uint8_t* flags, int32_t* dev_status, void* stream);
 
 /*
  * spec_accept_noalloc — spec_accept for callers that cannot allocate device memory.

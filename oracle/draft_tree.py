@@ -12,7 +12,8 @@ Readings: node ids are given in the order nodes leave the queue (so parent[i] < 
 convention the mask and verification calls use); ties in confidence go to the candidate
 queued first; ties among a row's logits go to the lower token id; the probabilities are
 softmax(logits) in fp64. `row_of(u)` returns the draft logits row of node u (the draft model
-is outside the path).
+is outside the path); with row_key="edge" it is called as row_of(parent, token) instead, the
+node's parent id (-1 for the root) and its token -- what a draft model conditions on.
 """
 
 import numpy as np
@@ -28,17 +29,19 @@ def topk_softmax(row, k):
     return idx, p[idx]
 
 
-def best_first_tree(row_of, root_token, n_nodes, topk, max_depth, threshold=0.0, tie_rel=1e-6):
+def best_first_tree(row_of, root_token, n_nodes, topk, max_depth, threshold=0.0, tie_rel=1e-6, row_key="node"):
     """Returns (parent int32 [n], token int32 [n], score float64 [n], tight bool) where n <=
     n_nodes (fewer when the queue runs dry); `tight`: some pop had its best two confidences
     within a relative `tie_rel` (a kernel computing in lower precision may order it either
-    way)."""
+    way). row_key: "node" (row_of(u)) or "edge" (row_of(parent[u], token[u]))."""
+    assert row_key in ("node", "edge")
     parent, token, score, depth = [-1], [int(root_token)], [1.0], [0]
     queue = []          # [confidence, parent, token, alive] in push order
     tight = False
 
     def expand(u):
-        toks, probs = topk_softmax(row_of(u), topk)
+        row = row_of(u) if row_key == "node" else row_of(parent[u], token[u])
+        toks, probs = topk_softmax(row, topk)
         for t, p in zip(toks.tolist(), probs.tolist()):
             c = score[u] * p
             if threshold > 0 and not c > threshold:

@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
            "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
            "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8",
-           "spec_tree_verify_attn_parents")
+           "spec_tree_verify_attn_parents", "spec_tree_expand_multi")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -46,6 +46,8 @@ _SIGS = {
     "spec_tree_init": (_I, [_P, _I, _I, _P, _Z, _P, _P, _P, _P, _P, _P]),
     "spec_tree_expand": (_I, [_P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _I, _I, _I, ctypes.c_double, _P, _Z,
                               _P, _P, _P, _P, _P, _P, _P]),
+    "spec_tree_expand_multi": (_I, [_P, _I, ctypes.c_longlong, ctypes.c_longlong, _I, _I, _I, _I, _I, ctypes.c_double,
+                                    _P, _Z, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "spec_tree_verify_attn_kv8": (_I, [_P, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                        _I, _F, _P, _P, _P, _Z, _P, _P]),
     "spec_tree_verify_attn_parents": (_I, [_P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -230,6 +232,25 @@ def spec_tree_expand(draft_logits, max_nodes, topk, max_depth, state, parent_out
                                  state.numel() * state.element_size(), _ptr(parent_out), _ptr(tokens_out),
                                  _ptr(n_nodes_out), _ptr(next_node), _ptr(flags), _ptr(dev_status), _stream(stream))
     return _check(st, "spec_tree_expand")
+
+
+def spec_tree_expand_multi(draft_rows, max_nodes, topk, max_depth, state, parent_out, tokens_out, n_nodes_out,
+                           next_node, req_parent, req_token, req_n, threshold=0.0, flags=None, dev_status=None,
+                           stream=None):
+    """One multi-row expansion of every sequence's draft tree. draft_rows float32
+    [batch][width][vocab]: row j of sequence b is the draft logits of the request listed in
+    req_parent[b][j] / req_token[b][j] by the previous call (after spec_tree_init: the root
+    alone, in row 0). req_parent / req_token int32 [batch][width], req_n int32 [batch] are
+    written with the next call's requests."""
+    Bn, W, V = draft_rows.shape
+    if draft_rows.dtype != torch.float32 or draft_rows.stride(2) != 1:
+        raise ValueError("draft_rows must be float32 with contiguous rows")
+    st = load().spec_tree_expand_multi(_ptr(draft_rows), V, int(draft_rows.stride(0)), int(draft_rows.stride(1)), Bn,
+                                       int(max_nodes), W, int(topk), int(max_depth), float(threshold), _ptr(state),
+                                       state.numel() * state.element_size(), _ptr(parent_out), _ptr(tokens_out),
+                                       _ptr(n_nodes_out), _ptr(next_node), _ptr(req_parent), _ptr(req_token),
+                                       _ptr(req_n), _ptr(flags), _ptr(dev_status), _stream(stream))
+    return _check(st, "spec_tree_expand_multi")
 
 
 

@@ -364,7 +364,7 @@ int spec_tree_init(const int32_t* root_tokens, int batch, int max_nodes, void* s
   if (!root_tokens || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
   if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
   TreeArgs a{static_cast<uint8_t*>(state), max_nodes, 1, 1, 0.0, parent_out, tokens_out, n_nodes_out, next_node,
-             flags, nullptr};
+             flags, nullptr, 1, nullptr, nullptr, nullptr};
   return launch_tree_init(root_tokens, batch, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -379,9 +379,28 @@ int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride,
   if (!draft_logits || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
   if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
   TreeArgs a{static_cast<uint8_t*>(state), max_nodes, topk, max_depth, threshold, parent_out, tokens_out,
-             n_nodes_out, next_node, flags, dev_status};
+             n_nodes_out, next_node, flags, dev_status, 1, nullptr, nullptr, nullptr};
   return launch_tree_expand(draft_logits, vocab, (long)row_stride, (long)node_stride, batch, a,
                             static_cast<cudaStream_t>(stream));
+}
+
+int spec_tree_expand_multi(const float* draft_logits, int vocab, long long row_stride, long long req_stride,
+                           int batch, int max_nodes, int width, int topk, int max_depth, double threshold,
+                           void* state, size_t state_bytes, int32_t* parent_out, int32_t* tokens_out,
+                           int32_t* n_nodes_out, int32_t* next_node, int32_t* req_parent, int32_t* req_token,
+                           int32_t* req_n, uint8_t* flags, int32_t* dev_status, void* stream) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes || vocab < 1 || topk < 1 || topk > 16 ||
+      max_depth < 1 || width < 1 || width > kTreeMaxW || row_stride < 0 || req_stride < 0)
+    return SPEC_ERR_ARG;
+  if (batch == 0) return SPEC_OK;
+  if (!draft_logits || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node || !req_parent ||
+      !req_token || !req_n)
+    return SPEC_ERR_ARG;
+  if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
+  TreeArgs a{static_cast<uint8_t*>(state), max_nodes, topk, max_depth, threshold, parent_out, tokens_out,
+             n_nodes_out, next_node, flags, dev_status, width, req_parent, req_token, req_n};
+  return launch_tree_expand_multi(draft_logits, vocab, (long)row_stride, (long)req_stride, batch, a,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

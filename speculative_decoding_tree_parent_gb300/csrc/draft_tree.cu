@@ -37,22 +37,32 @@ constexpr int kTreeCand = 2048;  // candidate buffer of a row scan (shared memor
 constexpr double kTreeTieRel = 1e-6;
 
 // Per-sequence state: a header, then node scores and depths [N], then the candidate
-// arrays [N * kTreeMaxK] (scores; parents; tokens). A candidate score < 0 marks a slot
-// already popped (scores are probabilities products: >= 0).
+// arrays [N * kTreeMaxK] (scores; parents; tokens; result index), then the expansion
+// results of the multi-row call [N * kTreeMaxW][kTreeMaxK] (tokens; probabilities). A
+// candidate score < 0 marks a slot already popped (scores are probabilities products: >= 0).
 struct TreeHeader {
   int n_nodes, n_cand, cur, flags;
+  // multi-row call: the current request list is result entries [req_base, req_base + nreq);
+  // n_res entries are assigned; arrive counts the request clusters of the running call
+  int nreq, req_base, n_res, arrive;
 };
 struct TreeLayout {
-  size_t score, depth, cscore, cparent, ctoken, per_seq;
+  size_t score, depth, cscore, cparent, ctoken, cres, rtok, rp, per_seq;
+  int n_res_max;
   __host__ __device__ static TreeLayout make(int max_nodes) {
     TreeLayout l;
     const size_t C = (size_t)max_nodes * kTreeMaxK;
+    const size_t R = (size_t)max_nodes * kTreeMaxW;
+    l.n_res_max = (int)R;
     size_t off = align_up(sizeof(TreeHeader), 16);
     l.score = off;   off = align_up(off + sizeof(double) * max_nodes, 16);
     l.depth = off;   off = align_up(off + sizeof(int) * max_nodes, 16);
     l.cscore = off;  off = align_up(off + sizeof(double) * C, 16);
     l.cparent = off; off = align_up(off + sizeof(int) * C, 16);
     l.ctoken = off;  off = align_up(off + sizeof(int) * C, 16);
+    l.cres = off;    off = align_up(off + sizeof(int) * C, 16);
+    l.rtok = off;    off = align_up(off + sizeof(int) * R * kTreeMaxK, 16);
+    l.rp = off;      off = align_up(off + sizeof(double) * R * kTreeMaxK, 16);
     l.per_seq = align_up(off, 256);
     return l;
   }
@@ -75,6 +85,10 @@ __global__ void tree_init_kernel(const int32_t* __restrict__ root_tokens, int ba
     h->n_cand = 0;
     h->cur = a.max_nodes > 1 ? 0 : -1;  // the root awaits its expansion
     h->flags = 0;
+    h->nreq = a.max_nodes > 1 ? 1 : 0;  // the multi-row call's first request: the root (entry 0)
+    h->req_base = 0;
+    h->n_res = 1;
+    h->arrive = 0;
     reinterpret_cast<double*>(st + l.score)[0] = 1.0;
     reinterpret_cast<int*>(st + l.depth)[0] = 0;
     a.n_nodes_out[b] = 1;
@@ -94,23 +108,26 @@ __device__ __forceinline__ bool key_better(long long s, int i, long long s2, int
   return s > s2 || (s == s2 && i < i2);
 }
 
+// The softmax statistics and the top-k tokens of one draft row (row_base: its first logit),
+// by the 8 CTAs of the calling cluster, each on an eighth of the vocabulary (the passes and the
+// cluster exchange described at the top of this file). Every rank must call it. Returns false
+// in ranks 1-7, which are then done with the row; true in rank 0, with out.gv / out.gi the
+// row's top-k in shared memory (largest logit first, lower token id on ties; INT_MAX when the
+// row has fewer than k tokens), out.M the row max and out.inv_z the normaliser's reciprocal.
+struct RowTopk {
+  const float* gv;
+  const int* gi;
+  float M;
+  double inv_z;
+};
+
 template <int KMAX, bool kVec>
-__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThreads, 1)
-    tree_expand_kernel(const float* __restrict__ logits, int vocab, long row_stride, long node_stride, TreeArgs a) {
+__device__ __forceinline__ bool tree_row_topk(const float* __restrict__ row_base, int vocab, int k, RowTopk& out) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
-  const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kTreeThreads / 32;
-  const TreeLayout l = TreeLayout::make(a.max_nodes);
-  uint8_t* st = a.state + (size_t)b * l.per_seq;
-  TreeHeader* h = reinterpret_cast<TreeHeader*>(st);
-  double* score = reinterpret_cast<double*>(st + l.score);
-  int* depth = reinterpret_cast<int*>(st + l.depth);
-  double* cscore = reinterpret_cast<double*>(st + l.cscore);
-  int* cparent = reinterpret_cast<int*>(st + l.cparent);
-  int* ctoken = reinterpret_cast<int*>(st + l.ctoken);
   __shared__ float s_m[kWarps], s_th[kWarps], s_hi[kWarps], s_lo[kWarps];
   __shared__ float s_cv[kTreeCand];  // the row's elements >= theta (the top-k is among them)
   __shared__ int s_ci[kTreeCand];
@@ -119,30 +136,21 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
   __shared__ int s_wi[kWarps];
   __shared__ float s_topv[KMAX];
   __shared__ int s_topi[KMAX];
-  __shared__ long long s_k1[kWarps], s_k2[kWarps];
-  __shared__ int s_i1[kWarps];
   __shared__ double s_inv_z;
-  __shared__ int s_u, s_stop;
   __shared__ float s_gv[KMAX];                 // rank 0: the merged top-k
   __shared__ int s_gi[KMAX];
   __shared__ float s_allv[kTreeCluster * KMAX];  // rank 0: every slice's list, pushed to it
   __shared__ int s_alli[kTreeCluster * KMAX];
   __shared__ float s_allz[2 * kTreeCluster];
   __shared__ float s_allM[kTreeCluster], s_allT[kTreeCluster];  // every slice's max, threshold
-  pdl_wait();  // the logits row (the draft model) and the state (the previous call)
-  if (threadIdx.x == 0) s_u = h->cur;
-  __syncthreads();
-  const int u = s_u;
-  if (u < 0) return;  // this sequence's tree is complete (the same answer in every rank)
   // every rank of the cluster is running before any writes into another's shared memory:
   // arrive now, wait just before the first such write (after pass 1)
   cl.barrier_arrive();
-  const int k = a.topk;
   // this CTA's slice of the row: tokens [c_lo, c_lo + n_sl) (a multiple of 4 long, but the last)
   const int per = ((vocab + kTreeCluster - 1) / kTreeCluster + 3) & ~3;
   const int c_lo = rank * per;
   const int n_sl = max(0, min(vocab, c_lo + per) - c_lo);
-  const float* row = logits + (long)b * row_stride + (long)u * node_stride + c_lo;
+  const float* row = row_base + c_lo;
 
   // Every element of the row goes through `visit(x, t)`, eight loads per thread in flight.
   constexpr int kU = 8;
@@ -353,7 +361,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
     }
   }
   cl.sync();  // (B) every slice's list and partial are in rank 0; the other CTAs are done
-  if (rank != 0) return;
+  if (rank != 0) return false;
   if (warp == 0) {  // the slices' k best each (up to 8 x 16 entries): k rounds over the warp
     constexpr int kPer = (kTreeCluster * KMAX + 31) / 32;
     float ev[kPer];
@@ -402,15 +410,122 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
     }
   }
   __syncthreads();
+  out.gv = s_gv;
+  out.gi = s_gi;
+  out.M = M;
+  out.inv_z = s_inv_z;
+  return true;
+}
+
+// The best candidate (largest key, then lowest slot) among the slots c < nc with a
+// non-negative key that ok(c) admits, and the second-best key, reduced over the CTA: the
+// answer is in every lane of warp 0 (k1 = -1 / i1 = INT_MAX: none). Every thread must call it;
+// the caller synchronises before calling it again.
+template <class Ok>
+__device__ __forceinline__ void cand_best(const double* cscore, int nc, Ok ok, long long& k1, int& i1,
+                                          long long& k2) {
+  constexpr int kWarps = kTreeThreads / 32;
+  __shared__ long long s_k1[kWarps], s_k2[kWarps];
+  __shared__ int s_i1[kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  k1 = -1;
+  k2 = -1;
+  i1 = INT_MAX;
+  for (int c = threadIdx.x; c < nc; c += kTreeThreads) {
+    const long long key = score_key(cscore[c]);
+    if (key < 0 || !ok(c)) continue;  // popped, or not admitted
+    if (key_better(key, c, k1, i1)) {
+      k2 = k1;
+      k1 = key;
+      i1 = c;
+    } else if (key > k2) {
+      k2 = key;
+    }
+  }
+  auto merge = [&](long long ok1, int oi1, long long ok2) {
+    if (key_better(ok1, oi1, k1, i1)) {
+      k2 = k1 > ok2 ? k1 : ok2;
+      k1 = ok1;
+      i1 = oi1;
+    } else if (ok1 > k2) {
+      k2 = ok1;
+    }
+  };
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    merge(__shfl_xor_sync(0xffffffffu, k1, o), __shfl_xor_sync(0xffffffffu, i1, o),
+          __shfl_xor_sync(0xffffffffu, k2, o));
+  if (lane == 0) {
+    s_k1[warp] = k1;
+    s_k2[warp] = k2;
+    s_i1[warp] = i1;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    k1 = lane < kWarps ? s_k1[lane] : -1;
+    k2 = lane < kWarps ? s_k2[lane] : -1;
+    i1 = lane < kWarps ? s_i1[lane] : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      merge(__shfl_xor_sync(0xffffffffu, k1, o), __shfl_xor_sync(0xffffffffu, i1, o),
+            __shfl_xor_sync(0xffffffffu, k2, o));
+  }
+}
+
+// Pops the best candidate as node n_nodes (by lane 0 of warp 0, with k1 / i1 / k2 from
+// cand_best): writes its parent, token, score and depth and marks the slot popped. Returns the
+// new node id, or -1 when no candidate is left. Sets flags bit 0 on a near tie.
+__device__ __forceinline__ int pop_node(TreeHeader* h, double* score, int* depth, double* cscore, const int* cparent,
+                                        const int* ctoken, const TreeArgs& a, int b, long long k1, int i1, long long k2) {
+  if (i1 == INT_MAX || k1 < 0) return -1;
+  const double b1 = __longlong_as_double(k1);
+  if (k2 >= 0) {  // near tie: the gap relative to the best, in fp32 (ample for 1e-6)
+    const float f1 = (float)b1, f2 = (float)__longlong_as_double(k2);
+    if (f1 - f2 <= (float)kTreeTieRel * f1) h->flags |= 1;
+  }
+  const int nid = h->n_nodes;
+  const int par = cparent[i1];
+  cscore[i1] = -1.0;  // popped
+  a.parent_out[(size_t)b * a.max_nodes + nid] = par;
+  a.tokens_out[(size_t)b * a.max_nodes + nid] = ctoken[i1];
+  score[nid] = b1;
+  depth[nid] = depth[par] + 1;
+  h->n_nodes = nid + 1;
+  return nid;
+}
+
+template <int KMAX, bool kVec>
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThreads, 1)
+    tree_expand_kernel(const float* __restrict__ logits, int vocab, long row_stride, long node_stride, TreeArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const TreeLayout l = TreeLayout::make(a.max_nodes);
+  uint8_t* st = a.state + (size_t)b * l.per_seq;
+  TreeHeader* h = reinterpret_cast<TreeHeader*>(st);
+  double* score = reinterpret_cast<double*>(st + l.score);
+  int* depth = reinterpret_cast<int*>(st + l.depth);
+  double* cscore = reinterpret_cast<double*>(st + l.cscore);
+  int* cparent = reinterpret_cast<int*>(st + l.cparent);
+  int* ctoken = reinterpret_cast<int*>(st + l.ctoken);
+  __shared__ int s_u, s_stop;
+  pdl_wait();  // the logits row (the draft model) and the state (the previous call)
+  if (threadIdx.x == 0) s_u = h->cur;
+  __syncthreads();
+  const int u = s_u;
+  if (u < 0) return;  // this sequence's tree is complete (the same answer in every rank)
+  const int k = a.topk;
+  RowTopk rt;
+  if (!tree_row_topk<KMAX, kVec>(logits + (long)b * row_stride + (long)u * node_stride, vocab, k, rt)) return;
+  const float M = rt.M;
   if (warp == 0) {
     // ---- push the k children of u: lane r scores candidate r; a ballot keeps the order
     const int nc0 = h->n_cand;
     double c = 0.0;
     bool keep = false;
     if (lane < k) {
-      const int tok = s_gi[lane];
+      const int tok = rt.gi[lane];
       if (tok != INT_MAX && tok < vocab) {
-        c = score[u] * ((double)expf(s_gv[lane] - M) * s_inv_z);
+        c = score[u] * ((double)expf(rt.gv[lane] - M) * rt.inv_z);
         keep = !(a.threshold > 0.0) || c > a.threshold;
       }
     }
@@ -419,7 +534,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
       const int at = nc0 + __popc(kb & ((1u << lane) - 1u));
       cscore[at] = c;
       cparent[at] = u;
-      ctoken[at] = s_gi[lane];
+      ctoken[at] = rt.gi[lane];
     }
     if (lane == 0) {
       h->n_cand = nc0 + __popc(kb);
@@ -431,79 +546,223 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
   // ---- pops: the best candidate becomes the next node, until one needs its expansion
   const int nc = h->n_cand;
   while (true) {
-    long long k1 = -1, k2 = -1;
-    int i1 = INT_MAX;
-    for (int c = threadIdx.x; c < nc; c += kTreeThreads) {
-      const long long key = score_key(cscore[c]);
-      if (key < 0) continue;  // popped
-      if (key_better(key, c, k1, i1)) {
-        k2 = k1;
-        k1 = key;
-        i1 = c;
-      } else if (key > k2) {
-        k2 = key;
+    long long k1, k2;
+    int i1;
+    cand_best(cscore, nc, [](int) { return true; }, k1, i1, k2);
+    if (threadIdx.x == 0) {
+      int stop = 1;
+      const int nid = pop_node(h, score, depth, cscore, cparent, ctoken, a, b, k1, i1, k2);
+      if (nid < 0) {
+        h->cur = -1;  // no candidate left
+      } else if (depth[nid] < a.max_depth && nid + 1 < a.max_nodes) {
+        h->cur = nid;  // its logits come next
+      } else if (nid + 1 < a.max_nodes) {
+        stop = 0;  // at the depth limit: the next candidate
+      } else {
+        h->cur = -1;  // budget met
       }
-    }
-    auto merge = [&](long long ok1, int oi1, long long ok2) {
-      if (key_better(ok1, oi1, k1, i1)) {
-        k2 = k1 > ok2 ? k1 : ok2;
-        k1 = ok1;
-        i1 = oi1;
-      } else if (ok1 > k2) {
-        k2 = ok1;
-      }
-    };
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      merge(__shfl_xor_sync(0xffffffffu, k1, o), __shfl_xor_sync(0xffffffffu, i1, o),
-            __shfl_xor_sync(0xffffffffu, k2, o));
-    if (lane == 0) {
-      s_k1[warp] = k1;
-      s_k2[warp] = k2;
-      s_i1[warp] = i1;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      k1 = lane < kWarps ? s_k1[lane] : -1;
-      k2 = lane < kWarps ? s_k2[lane] : -1;
-      i1 = lane < kWarps ? s_i1[lane] : INT_MAX;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-        merge(__shfl_xor_sync(0xffffffffu, k1, o), __shfl_xor_sync(0xffffffffu, i1, o),
-              __shfl_xor_sync(0xffffffffu, k2, o));
-      if (lane == 0) {
-        int stop = 1;
-        if (i1 != INT_MAX && k1 >= 0) {
-          const double b1 = __longlong_as_double(k1);
-          if (k2 >= 0) {  // near tie: the gap relative to the best, in fp32 (ample for 1e-6)
-            const float f1 = (float)b1, f2 = (float)__longlong_as_double(k2);
-            if (f1 - f2 <= (float)kTreeTieRel * f1) h->flags |= 1;
-          }
-          const int nid = h->n_nodes;
-          const int par = cparent[i1];
-          cscore[i1] = -1.0;  // popped
-          a.parent_out[(size_t)b * a.max_nodes + nid] = par;
-          a.tokens_out[(size_t)b * a.max_nodes + nid] = ctoken[i1];
-          score[nid] = b1;
-          depth[nid] = depth[par] + 1;
-          h->n_nodes = nid + 1;
-          if (depth[nid] < a.max_depth && nid + 1 < a.max_nodes) {
-            h->cur = nid;  // its logits come next
-          } else if (nid + 1 < a.max_nodes) {
-            stop = 0;  // at the depth limit: the next candidate
-          } else {
-            h->cur = -1;  // budget met
-          }
-        } else {
-          h->cur = -1;  // no candidate left
-        }
-        s_stop = stop;
-      }
+      s_stop = stop;
     }
     __syncthreads();
     if (s_stop) break;
   }
   if (threadIdx.x == 0) {
+    a.n_nodes_out[b] = h->n_nodes;
+    a.next_node[b] = h->cur;
+    if (a.flags != nullptr) a.flags[b] = (uint8_t)h->flags;
+  }
+}
+
+// ------------------------------------------------------------------ the multi-row call
+// Exact batching of the construction above. A queued candidate's expansion (its draft row's
+// top-k tokens and probabilities) depends on the candidate alone -- its parent and token --
+// not on when it leaves the queue. So one call takes the rows of the node awaiting its
+// expansion and of up to width - 1 of the best queued candidates (the requests the previous
+// call listed), keeps each row's result with its candidate, and then pops exactly as the
+// one-row call would: a popped node whose result is at hand has its children pushed at once
+// and the pops go on; the first popped node that needs a row it has not got ends the call.
+// The tree is the one-row call's, node for node; only the number of calls falls.
+//
+// Grid: one 8-CTA cluster per (request slot, sequence), width slots. A cluster with a request
+// reduces its row (as above) and rank 0 stores the result in the state's entry for that
+// request; every cluster's rank 0 then counts itself in with one acq_rel atomic (a cluster
+// without a request only after all its ranks have read the header), and the one that counts
+// in last runs the pops and lists the next requests. So the header is rewritten only after
+// every CTA has read it, and nothing waits: the other clusters are done when they count in.
+template <int KMAX, bool kVec>
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThreads, 1)
+    tree_expand_multi_kernel(const float* __restrict__ logits, int vocab, long row_stride, long req_stride,
+                             TreeArgs a) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const TreeLayout l = TreeLayout::make(a.max_nodes);
+  uint8_t* st = a.state + (size_t)b * l.per_seq;
+  TreeHeader* h = reinterpret_cast<TreeHeader*>(st);
+  double* score = reinterpret_cast<double*>(st + l.score);
+  int* depth = reinterpret_cast<int*>(st + l.depth);
+  double* cscore = reinterpret_cast<double*>(st + l.cscore);
+  int* cparent = reinterpret_cast<int*>(st + l.cparent);
+  int* ctoken = reinterpret_cast<int*>(st + l.ctoken);
+  int* cres = reinterpret_cast<int*>(st + l.cres);
+  int* rtok = reinterpret_cast<int*>(st + l.rtok);
+  double* rp = reinterpret_cast<double*>(st + l.rp);
+  __shared__ int s_nreq, s_base, s_last, s_stop, s_node, s_res, s_nr;
+  pdl_wait();  // the rows (the draft model) and the state (the previous call)
+  if (threadIdx.x == 0) {
+    s_nreq = h->nreq;
+    s_base = h->req_base;
+  }
+  __syncthreads();
+  const int nreq = s_nreq;
+  if (nreq == 0) return;  // the tree is complete: no CTA counts in, nothing changes
+  if (nreq > (int)gridDim.y) {  // listed by a call of a larger width: refused, nothing changes
+    if (j == 0 && cl.block_rank() == 0 && threadIdx.x == 0) report(a.status, SPEC_ERR_ARG);
+    return;
+  }
+  const int k = a.topk;
+  if (j < nreq) {
+    RowTopk rt;
+    if (!tree_row_topk<KMAX, kVec>(logits + (long)b * row_stride + (long)j * req_stride, vocab, k, rt)) return;
+    // rank 0: the row's result into entry req_base + j
+    const int e = s_base + j;
+    if (warp == 0 && lane < k) {
+      const int tok = rt.gi[lane];
+      const bool ok = tok != INT_MAX && tok < vocab;
+      rtok[(size_t)e * kTreeMaxK + lane] = ok ? tok : -1;
+      rp[(size_t)e * kTreeMaxK + lane] = ok ? (double)expf(rt.gv[lane] - rt.M) * rt.inv_z : 0.0;
+    }
+    __syncthreads();  // the entry is written before thread 0's release
+  } else {
+    cl.sync();  // every rank has read the header before rank 0 counts in
+    if (cl.block_rank() != 0) return;
+  }
+  if (threadIdx.x == 0) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(&h->arrive) : "memory");
+    s_last = old == (int)gridDim.y - 1;
+    if (s_last) h->arrive = 0;  // every slot has counted in: ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  // ---- the last cluster: expand the awaiting node from entry req_base, then pop
+  // (the other clusters' entries are read from L2: they were written on other SMs)
+  auto push_children = [&](int u, int r) {  // warp 0: the children of node u from entry r
+    const int nc0 = h->n_cand;
+    double c = 0.0;
+    bool keep = false;
+    int tok = -1;
+    if (lane < k) {
+      tok = __ldcg(rtok + (size_t)r * kTreeMaxK + lane);
+      if (tok >= 0) {
+        c = score[u] * __ldcg(rp + (size_t)r * kTreeMaxK + lane);
+        keep = !(a.threshold > 0.0) || c > a.threshold;
+      }
+    }
+    const unsigned kb = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int at = nc0 + __popc(kb & ((1u << lane) - 1u));
+      cscore[at] = c;
+      cparent[at] = u;
+      ctoken[at] = tok;
+      cres[at] = -1;  // no row yet
+    }
+    if (lane == 0) h->n_cand = nc0 + __popc(kb);
+  };
+  if (threadIdx.x == 0) {
+    s_node = h->cur;
+    s_res = s_base;
+  }
+  __syncthreads();
+  while (true) {
+    if (warp == 0) push_children(s_node, s_res);
+    __syncthreads();
+    const int nc = h->n_cand;
+    int stop;
+    while (true) {  // pops until one needs a row (stop 1) or has its result (stop 0)
+      long long k1, k2;
+      int i1;
+      cand_best(cscore, nc, [](int) { return true; }, k1, i1, k2);
+      if (threadIdx.x == 0) {
+        int sp = 1;
+        const int r = i1 != INT_MAX ? cres[i1] : -1;
+        const int nid = pop_node(h, score, depth, cscore, cparent, ctoken, a, b, k1, i1, k2);
+        if (nid < 0) {
+          h->cur = -1;  // no candidate left
+        } else if (depth[nid] < a.max_depth && nid + 1 < a.max_nodes) {
+          if (r >= 0) {  // its row came with an earlier request: expand it now
+            s_node = nid;
+            s_res = r;
+            sp = 0;
+          } else {
+            h->cur = nid;  // its row is the next call's first request
+          }
+        } else if (nid + 1 < a.max_nodes) {
+          sp = 2;  // at the depth limit: the next candidate
+        } else {
+          h->cur = -1;  // budget met
+        }
+        s_stop = sp;
+      }
+      __syncthreads();
+      stop = s_stop;
+      if (stop != 2) break;
+    }
+    if (stop == 1) break;
+  }
+
+  // ---- the next requests: the awaiting node, then the best queued candidates that have no
+  // row yet and would be expanded (below the depth limit), best first
+  const int cur = h->cur;
+  const int nc = h->n_cand;
+  if (threadIdx.x == 0) s_nr = 0;
+  if (cur >= 0) {
+    const int n_res = h->n_res;
+    // Entries suffice: a call with requests consumes one awaiting node and the next awaiting
+    // node is a new node, so at most max_nodes - 1 such calls follow the root's, each taking
+    // at most width <= kTreeMaxW entries. Checked all the same: short, it reports and stops.
+    const int room = min(a.width, l.n_res_max - n_res);
+    if (threadIdx.x == 0 && room <= 0) {
+      report(a.status, SPEC_ERR_CAPACITY);
+      h->cur = -1;
+    }
+    if (threadIdx.x == 0 && room > 0) {
+      a.req_parent[(size_t)b * a.width] = a.parent_out[(size_t)b * a.max_nodes + cur];
+      a.req_token[(size_t)b * a.width] = a.tokens_out[(size_t)b * a.max_nodes + cur];
+      s_nr = 1;
+    }
+    __syncthreads();
+    for (int q = 1; q < room; ++q) {
+      long long k1, k2;
+      int i1;
+      cand_best(
+          cscore, nc, [&](int c) { return cres[c] < 0 && depth[cparent[c]] + 1 < a.max_depth; }, k1, i1, k2);
+      if (threadIdx.x == 0) {
+        if (i1 != INT_MAX && k1 >= 0) {
+          cres[i1] = n_res + q;
+          a.req_parent[(size_t)b * a.width + q] = cparent[i1];
+          a.req_token[(size_t)b * a.width + q] = ctoken[i1];
+          s_nr = q + 1;
+        }
+      }
+      __syncthreads();
+      if (s_nr != q + 1) break;
+    }
+    if (threadIdx.x == 0) {
+      h->req_base = n_res;
+      h->n_res = n_res + s_nr;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    h->nreq = s_nr;
+    for (int q = s_nr; q < a.width; ++q) {
+      a.req_parent[(size_t)b * a.width + q] = -1;
+      a.req_token[(size_t)b * a.width + q] = -1;
+    }
+    a.req_n[b] = s_nr;
     a.n_nodes_out[b] = h->n_nodes;
     a.next_node[b] = h->cur;
     if (a.flags != nullptr) a.flags[b] = (uint8_t)h->flags;
@@ -526,6 +785,28 @@ int launch_tree_expand(const float* logits, int vocab, long row_stride, long nod
                        logits, vocab, row_stride, node_stride, a)                                          \
           : launch_pdl(tree_expand_kernel<K, false>, dim3(kTreeCluster, batch), dim3(kTreeThreads), 0, stream, \
                        logits, vocab, row_stride, node_stride, a)
+  if (a.topk <= 4)
+    SPECV_TREE_LAUNCH(4);
+  else if (a.topk <= 10)
+    SPECV_TREE_LAUNCH(10);
+  else
+    SPECV_TREE_LAUNCH(kTreeMaxK);
+#undef SPECV_TREE_LAUNCH
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+int launch_tree_expand_multi(const float* logits, int vocab, long row_stride, long req_stride, int batch,
+                             const TreeArgs& a, cudaStream_t stream) {
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 && vocab % 4 == 0 && row_stride % 4 == 0 &&
+                   req_stride % 4 == 0;
+  const dim3 grid(kTreeCluster, a.width, batch);
+  cudaError_t e;
+#define SPECV_TREE_LAUNCH(K)                                                                               \
+  e = vec ? launch_pdl(tree_expand_multi_kernel<K, true>, grid, dim3(kTreeThreads), 0, stream, logits, vocab,  \
+                       row_stride, req_stride, a)                                                          \
+          : launch_pdl(tree_expand_multi_kernel<K, false>, grid, dim3(kTreeThreads), 0, stream, logits, vocab, \
+                       row_stride, req_stride, a)
   if (a.topk <= 4)
     SPECV_TREE_LAUNCH(4);
   else if (a.topk <= 10)

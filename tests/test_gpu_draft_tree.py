@@ -124,3 +124,147 @@ def test_tree_refuses_bad_arguments():
     with pytest.raises(B.SpecError) as ei:
         B.spec_tree_expand(logits, 4, 17, 2, big, z, z, one, one, row_stride=32, node_stride=8)  # topk > 16
     assert ei.value.status == -1
+
+
+# ---------------------------------------------------------------- the multi-row call
+from draft_protocol import EdgeRows, multi_row_tree  # noqa: E402
+
+
+def _build_multi(er, roots, n, k, depth, width, threshold=0.0):
+    """Drive spec_tree_expand_multi to completion, the host standing in for the draft model:
+    after each call it writes the rows of the listed requests (EdgeRows, keyed by parent and
+    token). Returns the device outputs and, per call, every sequence's request list."""
+    Bn, V = len(roots), er.vocab
+    dev = "cuda"
+    state = torch.zeros(B.spec_workspace_size(B.SPEC_OP_TREE, Bn, 0, n, 0, 0, 0, 0, 0), dtype=torch.uint8,
+                        device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    parent, tokens = torch.empty((Bn, n), **i32), torch.empty((Bn, n), **i32)
+    nn, nxt, req_n = torch.empty(Bn, **i32), torch.empty(Bn, **i32), torch.empty(Bn, **i32)
+    req_p, req_t = torch.empty((Bn, width), **i32), torch.empty((Bn, width), **i32)
+    flags = torch.empty(Bn, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, **i32)
+    B.spec_tree_init(torch.from_numpy(roots).cuda(), n, state, parent, tokens, nn, nxt, flags)
+    rows = torch.zeros((Bn, width, V), dtype=torch.float32, device=dev)
+    host = np.zeros((Bn, width, V), np.float32)
+    reqs = [[(-1, int(roots[b]))] if n > 1 else [] for b in range(Bn)]
+    calls = []
+    while any(reqs):
+        host[:] = 0
+        for b in range(Bn):
+            for j, (p, t) in enumerate(reqs[b]):
+                host[b, j] = er.row(b, p, t)
+        rows.copy_(torch.from_numpy(host))
+        B.spec_tree_expand_multi(rows, n, k, depth, state, parent, tokens, nn, nxt, req_p, req_t, req_n,
+                                 threshold=threshold, flags=flags, dev_status=status)
+        calls.append(reqs)
+        rn, rp, rt = req_n.cpu().numpy(), req_p.cpu().numpy(), req_t.cpu().numpy()
+        reqs = [[(int(rp[b, j]), int(rt[b, j])) for j in range(rn[b])] for b in range(Bn)]
+        for b in range(Bn):
+            assert (rp[b, rn[b]:] == -1).all() and (rt[b, rn[b]:] == -1).all()
+        assert len(calls) <= n + 1
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return (parent.cpu().numpy(), tokens.cpu().numpy(), nn.cpu().numpy(), nxt.cpu().numpy(), flags.cpu().numpy(),
+            calls)
+
+
+def _compare_multi(er, roots, n, k, depth, width, threshold=0.0, strict=False):
+    parent, tokens, nn, nxt, flags, calls = _build_multi(er, roots, n, k, depth, width, threshold)
+    assert (nxt == -1).all()
+    tight = 0
+    for b in range(len(roots)):
+        p, t, s, is_tight = oracle.best_first_tree(er.of(b), int(roots[b]), n, k, depth, threshold, row_key="edge")
+        if is_tight and not strict:
+            tight += 1
+            continue
+        assert nn[b] == len(p), b
+        assert np.array_equal(parent[b, : len(p)], p), b
+        assert np.array_equal(tokens[b, : len(p)], t), b
+        assert (parent[b, len(p):] == -1).all() and (tokens[b, len(p):] == -1).all()
+        # the requests, call by call, are the protocol's (the host model in fp64)
+        model = multi_row_tree(er.of(b), int(roots[b]), n, k, depth, width, threshold)
+        got = [c[b] for c in calls if c[b]]
+        assert got == model.requests, b
+    return tight, len(calls)
+
+
+@pytest.mark.parametrize("width", [1, 4, 8])
+def test_multi_tree_llama3_vocab(width):
+    """128256-token vocabulary, top-10, depth 8, 64 nodes, draft logits ~ N(0, 2^2): the
+    one-row construction's tree, the protocol's requests, and (width 8) 9 calls instead of 63."""
+    er = EdgeRows(21, 128256, scale=2.0)
+    tight, ncalls = _compare_multi(er, np.array([17], np.int32), 64, 10, 8, width)
+    assert tight == 0
+    assert ncalls == {1: 63, 4: 17, 8: 9}[width]
+
+
+@pytest.mark.parametrize("seed,V,k,depth,n,width,bump", [
+    (1, 4096, 10, 8, 64, 8, 0.0), (2, 4096, 4, 6, 48, 3, 0.0), (3, 4096, 16, 3, 128, 8, 0.0),
+    (4, 4096, 1, 8, 9, 8, 0.0), (5, 1001, 10, 8, 64, 8, 12.0), (6, 4096, 10, 8, 64, 8, 14.0)])
+def test_multi_tree_batch(seed, V, k, depth, n, width, bump):
+    """Three sequences per call; odd vocabulary (scalar loads); confident draft heads
+    (bump: deep chains, where fewer candidates are popped per call)."""
+    rng = np.random.default_rng(seed)
+    roots = rng.integers(0, V, 3).astype(np.int32)
+    er = EdgeRows(100 + seed, V, scale=2.0, bump=bump)
+    tight, _ = _compare_multi(er, roots, n, k, depth, width)
+    assert tight <= 1
+
+
+def test_multi_tree_threshold_and_ties():
+    """A threshold that empties the queue before the budget; quantised logits (exact ties in
+    the top-k and equal confidences at depth 1)."""
+    er = EdgeRows(7, 100, scale=1.5)
+    _compare_multi(er, np.arange(4, dtype=np.int32), 32, 3, 5, 8, threshold=0.05)
+
+    class Quantised(EdgeRows):
+        def row(self, b, parent, token):
+            r = super().row(b, parent, token)
+            return np.floor(np.abs(r)).astype(np.float32)
+
+    _compare_multi(Quantised(8, 64, scale=1.2), np.zeros(5, np.int32), 9, 8, 1, 8, strict=True)
+
+
+def test_multi_tree_edges():
+    """max_nodes 1 (nothing to request, a call changes nothing); a width above 8 is refused on
+    the host; a call narrower than the pending request list is refused on the device and
+    leaves the tree as it was."""
+    dev = "cuda"
+    i32 = dict(dtype=torch.int32, device=dev)
+    st1 = torch.zeros(B.spec_workspace_size(B.SPEC_OP_TREE, 1, 0, 1, 0, 0, 0, 0, 0), dtype=torch.uint8, device=dev)
+    par, tok = torch.empty((1, 1), **i32), torch.empty((1, 1), **i32)
+    nn, nxt, rn = torch.full((1,), 7, **i32), torch.empty(1, **i32), torch.full((1,), 5, **i32)
+    rp, rt = torch.full((1, 2), 9, **i32), torch.full((1, 2), 9, **i32)
+    B.spec_tree_init(torch.tensor([3], **i32), 1, st1, par, tok, nn, nxt)
+    rows = torch.zeros((1, 2, 64), dtype=torch.float32, device=dev)
+    B.spec_tree_expand_multi(rows, 1, 4, 4, st1, par, tok, nn, nxt, rp, rt, rn)
+    torch.cuda.synchronize()
+    assert int(nn.item()) == 1 and int(nxt.item()) == -1 and int(rn.item()) == 5   # skipped: untouched
+
+    with pytest.raises(B.SpecError) as ei:
+        B.spec_tree_expand_multi(torch.zeros((1, 9, 64), dtype=torch.float32, device=dev), 1, 4, 4, st1, par, tok,
+                                 nn, nxt, torch.empty((1, 9), **i32), torch.empty((1, 9), **i32), rn)
+    assert ei.value.status == -1
+
+    er = EdgeRows(9, 256, scale=2.0)
+    n = 16
+    st = torch.zeros(B.spec_workspace_size(B.SPEC_OP_TREE, 1, 0, n, 0, 0, 0, 0, 0), dtype=torch.uint8, device=dev)
+    par, tok = torch.empty((1, n), **i32), torch.empty((1, n), **i32)
+    rp8, rt8 = torch.empty((1, 8), **i32), torch.empty((1, 8), **i32)
+    status = torch.zeros(1, **i32)
+    B.spec_tree_init(torch.tensor([1], **i32), n, st, par, tok, nn, nxt)
+    rows8 = torch.zeros((1, 8, 256), dtype=torch.float32, device=dev)
+    rows8[0, 0] = torch.from_numpy(er.row(0, -1, 1))
+    B.spec_tree_expand_multi(rows8, n, 4, 4, st, par, tok, nn, nxt, rp8, rt8, rn, dev_status=status)
+    torch.cuda.synchronize()
+    listed = int(rn.item())
+    assert listed > 2 and int(status.item()) == 0
+    before = (par.clone(), tok.clone(), int(nn.item()))
+    rp2, rt2 = torch.empty((1, 2), **i32), torch.empty((1, 2), **i32)
+    B.spec_tree_expand_multi(torch.zeros((1, 2, 256), dtype=torch.float32, device=dev), n, 4, 4, st, par, tok, nn,
+                             nxt, rp2, rt2, rn, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -1
+    assert torch.equal(par, before[0]) and torch.equal(tok, before[1]) and int(nn.item()) == before[2]
+    assert int(rn.item()) == listed

@@ -108,3 +108,42 @@ def test_ties_go_to_the_earlier_candidate():
     parent, token, score, tight = DT.best_first_tree(lambda u: rows[u], 0, 4, 2, 1)
     assert token.tolist() == [0, 0, 1] and parent.tolist() == [-1, 0, 0]
     assert tight
+
+
+def test_edge_keyed_rows_reach_the_node_they_define():
+    """row_key="edge" hands row_of the node's own parent and token: the same tree comes out
+    when the rows are looked up by node id from the finished tree."""
+    from draft_protocol import EdgeRows
+    er = EdgeRows(3, 50, scale=1.5)
+    parent, token, score, _ = DT.best_first_tree(er.of(0), 5, 24, 4, 4, row_key="edge")
+    by_node = [er.row(0, parent[u], token[u]) for u in range(len(parent))]
+    parent2, token2, score2, _ = DT.best_first_tree(lambda u: by_node[u], 5, 24, 4, 4)
+    assert np.array_equal(parent, parent2) and np.array_equal(token, token2)
+    np.testing.assert_array_equal(score, score2)
+
+
+@pytest.mark.parametrize("seed,V,k,depth,n,thr,bump", [
+    (1, 64, 10, 8, 64, 0.0, 0.0), (2, 40, 4, 6, 48, 0.0, 0.0), (3, 30, 16, 3, 100, 0.0, 0.0),
+    (4, 25, 1, 8, 9, 0.0, 0.0), (5, 100, 3, 5, 32, 0.05, 0.0), (6, 64, 10, 8, 64, 0.0, 6.0),
+    (7, 16, 2, 12, 80, 0.0, 3.0)])
+def test_multi_row_protocol_builds_the_pages_tree(seed, V, k, depth, n, thr, bump):
+    """The batched protocol (several rows per call, results kept per candidate, pops replayed)
+    gives the one-pop-at-a-time tree for every width; width 1 takes one call per expanded
+    node; a wider call never needs more calls; every request is a distinct (parent, token)."""
+    from draft_protocol import EdgeRows, multi_row_tree
+    er = EdgeRows(seed, V, scale=2.0, bump=bump)
+    want_p, want_t, _, _ = DT.best_first_tree(er.of(0), 1, n, k, depth, threshold=thr, row_key="edge")
+    calls = {}
+    for w in (1, 2, 3, 8):
+        run = multi_row_tree(er.of(0), 1, n, k, depth, w, threshold=thr)
+        assert np.array_equal(run.parent, want_p) and np.array_equal(run.token, want_t), w
+        seen = [rq for call in run.requests for rq in call]
+        assert len(seen) == len(set(seen)), "a row was requested twice"
+        assert all(len(call) <= w for call in run.requests)
+        calls[w] = run.calls
+    d = [0] * len(want_p)
+    for u in range(1, len(want_p)):
+        d[u] = d[want_p[u]] + 1
+    expanded = sum(1 for u in range(len(want_p)) if d[u] < depth and u < n - 1)   # nodes that needed a row
+    assert calls[1] == expanded
+    assert calls[8] <= calls[3] <= calls[1] and calls[2] <= calls[1]
