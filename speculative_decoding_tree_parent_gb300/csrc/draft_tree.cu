@@ -35,6 +35,9 @@ constexpr int kTreeCluster = 8;  // CTAs per sequence, each on an eighth of the 
 constexpr int kTreeMaxK = 16;
 constexpr int kTreeCand = 2048;  // candidate buffer of a row scan (shared memory)
 constexpr double kTreeTieRel = 1e-6;
+// the multi-row call's queue goes to shared memory up to this size (with the row scan's ~19 KB
+// static shared memory it stays under the default 48 KB dynamic limit)
+constexpr size_t kTreeFastSmemMax = 28 * 1024;
 
 // Per-sequence state: a header, then node scores and depths [N], then the candidate
 // arrays [N * kTreeMaxK] (scores; parents; tokens; result index), then the expansion
@@ -198,16 +201,17 @@ __device__ __forceinline__ bool tree_row_topk(const float* __restrict__ row_base
   float tmax = -INFINITY;
   scan_row([&](float x, int) { tmax = fmaxf(tmax, x); }, false);
   {
-    float mine = tmax, th = -INFINITY, wmax = -INFINITY;
-    for (int r = 0; r < k; ++r) {
-      float v = mine;
+    // each lane's place among the warp's 32 maxima (larger first, ties by lane: all distinct),
+    // from 32 independent shuffles; theta is the value in place k - 1 (k <= 16)
+    const float mine = tmax;
+    int ahead = 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-      if (r == 0) wmax = v;
-      th = v;
-      const unsigned who = __ballot_sync(0xffffffffu, mine == v);
-      if (lane == __ffs(who) - 1) mine = -INFINITY;
+    for (int j = 0; j < 32; ++j) {
+      const float o = __shfl_sync(0xffffffffu, mine, j);
+      ahead += (o > mine || (o == mine && j < lane)) ? 1 : 0;
     }
+    const float th = __shfl_sync(0xffffffffu, mine, __ffs(__ballot_sync(0xffffffffu, ahead == k - 1)) - 1);
+    const float wmax = __shfl_sync(0xffffffffu, mine, __ffs(__ballot_sync(0xffffffffu, ahead == 0)) - 1);
     if (lane == 0) {
       s_m[warp] = wmax;
       s_th[warp] = th;
@@ -256,48 +260,41 @@ __device__ __forceinline__ bool tree_row_topk(const float* __restrict__ row_base
     s_lo[warp] = zs.lo;
   }
   __syncthreads();
-  // ---- top-k of this slice: k rounds, round r taking the best element strictly after round
-  // r-1's winner in the (value, lower id) order. Up to 256 candidates: warp 0 alone, from
-  // registers; more (many ties at theta): the whole CTA, from the buffer or, past its
-  // capacity, from the slice.
+  // ---- top-k of this slice. The buffer (up to kTreeCand elements, usually a few dozen): every
+  // element counts the elements ahead of it in the (value, lower id) order -- a strict order,
+  // the ids being distinct -- and one whose count is below k is the count-th best. More
+  // elements than the buffer holds (many ties at theta): k rounds over the slice, round r
+  // taking the best element strictly after round r-1's winner.
   const int cnt = s_cnt;
-  constexpr int kLane = 8;
-  if (cnt <= 32 * kLane) {
-    if (warp == 0) {
-      float cv[kLane];
-      int ci[kLane];
+  const int cnt8 = (min(cnt, kTreeCand) + 7) & ~7;
+  for (int r = threadIdx.x; r < k; r += kTreeThreads) {  // (slots no element reaches: none)
+    s_topv[r] = -INFINITY;
+    s_topi[r] = INT_MAX;
+  }
+  for (int c = cnt + threadIdx.x; c < cnt8; c += kTreeThreads) {  // padding: never ahead of anything
+    s_cv[c] = -INFINITY;
+    s_ci[c] = INT_MAX;
+  }
+  __syncthreads();
+  if (cnt <= kTreeCand) {
+    for (int c = threadIdx.x; c < cnt; c += kTreeThreads) {
+      const float v = s_cv[c];
+      const int i = s_ci[c];
+      int ahead = 0;
+      for (int e0 = 0; e0 < cnt8; e0 += 8) {  // eight loads in flight, then eight tests
+        float vv[8];
+        int ii[8];
 #pragma unroll
-      for (int q = 0; q < kLane; ++q) {
-        const int c = lane + 32 * q;
-        cv[q] = c < cnt ? s_cv[c] : -INFINITY;
-        ci[q] = c < cnt ? s_ci[c] : INT_MAX;
+        for (int q = 0; q < 8; ++q) {
+          vv[q] = s_cv[e0 + q];
+          ii[q] = s_ci[e0 + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ahead += tk_better(vv[q], ii[q], v, i) ? 1 : 0;
       }
-      float prev_v = INFINITY;
-      int prev_i = -1;
-      for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int q = 0; q < kLane; ++q)
-          if (ci[q] != INT_MAX && tk_better(prev_v, prev_i, cv[q], ci[q]) && tk_better(cv[q], ci[q], bv, bi)) {
-            bv = cv[q];
-            bi = ci[q];
-          }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (tk_better(v2, i2, bv, bi)) {
-            bv = v2;
-            bi = i2;
-          }
-        }
-        if (lane == 0) {
-          s_topv[r] = bv;
-          s_topi[r] = bi;
-        }
-        prev_v = bv;
-        prev_i = bi;
+      if (ahead < k) {
+        s_topv[ahead] = v;
+        s_topi[ahead] = i;
       }
     }
   } else {
@@ -306,17 +303,14 @@ __device__ __forceinline__ bool tree_row_topk(const float* __restrict__ row_base
     for (int r = 0; r < k; ++r) {
       float bv = -INFINITY;
       int bi = INT_MAX;
-      auto offer = [&](float x, int t) {
-        if (x >= theta && tk_better(prev_v, prev_i, x, t) && tk_better(x, t, bv, bi)) {
-          bv = x;
-          bi = t;
-        }
-      };
-      if (cnt <= kTreeCand) {
-        for (int c = threadIdx.x; c < cnt; c += kTreeThreads) offer(s_cv[c], s_ci[c]);
-      } else {
-        scan_row(offer, false);
-      }
+      scan_row(
+          [&](float x, int t) {
+            if (x >= theta && tk_better(prev_v, prev_i, x, t) && tk_better(x, t, bv, bi)) {
+              bv = x;
+              bi = t;
+            }
+          },
+          false);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -362,43 +356,36 @@ __device__ __forceinline__ bool tree_row_topk(const float* __restrict__ row_base
   }
   cl.sync();  // (B) every slice's list and partial are in rank 0; the other CTAs are done
   if (rank != 0) return false;
-  if (warp == 0) {  // the slices' k best each (up to 8 x 16 entries): k rounds over the warp
-    constexpr int kPer = (kTreeCluster * KMAX + 31) / 32;
-    float ev[kPer];
-    int ei[kPer];
+  // the slices' k best each (up to 8 x 16 entries, ids distinct across slices): ranked as
+  // above; entries a short slice left empty (-inf, INT_MAX) tie among themselves, but rank
+  // behind every real one and write only what the slots already hold
+  if (threadIdx.x < k) {
+    s_gv[threadIdx.x] = -INFINITY;
+    s_gi[threadIdx.x] = INT_MAX;
+  }
+  __syncthreads();
+  if (threadIdx.x < kTreeCluster * k) {
+    const int ne = kTreeCluster * k;
+    const float v = s_allv[threadIdx.x];
+    const int i = s_alli[threadIdx.x];
+    int ahead = 0;
+    for (int e0 = 0; e0 < ne; e0 += 8) {  // (ne = 8 k)
+      float vv[8];
+      int ii[8];
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = lane + 32 * q;
-      ev[q] = e < kTreeCluster * k ? s_allv[e] : -INFINITY;
-      ei[q] = e < kTreeCluster * k ? s_alli[e] : INT_MAX;
-    }
-    float prev_v = INFINITY;
-    int prev_i = -1;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int q = 0; q < kPer; ++q)
-        if (ei[q] != INT_MAX && tk_better(prev_v, prev_i, ev[q], ei[q]) && tk_better(ev[q], ei[q], bv, bi)) {
-          bv = ev[q];
-          bi = ei[q];
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (tk_better(v2, i2, bv, bi)) {
-          bv = v2;
-          bi = i2;
-        }
+      for (int q = 0; q < 8; ++q) {
+        vv[q] = s_allv[e0 + q];
+        ii[q] = s_alli[e0 + q];
       }
-      if (lane == 0) {
-        s_gv[r] = bv;
-        s_gi[r] = bi;
-      }
-      prev_v = bv;
-      prev_i = bi;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ahead += tk_better(vv[q], ii[q], v, i) ? 1 : 0;
     }
+    if (ahead < k) {
+      s_gv[ahead] = v;
+      s_gi[ahead] = i;
+    }
+  }
+  if (warp == 0) {
     if (lane == 0) {
       F2 z{0.f, 0.f};
       for (int r = 0; r < kTreeCluster; ++r) z = f2_add(z, F2{s_allz[r], s_allz[kTreeCluster + r]});
@@ -573,6 +560,295 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
   }
 }
 
+// The pops and the next requests of the multi-row call with the tree's queue staged in shared
+// memory and walked by one warp: no CTA barrier and no L2 round trip per pop (the CTA-wide form
+// in the kernel below pays both, about 1.7 us a pop). Every thread stages the candidates
+// (key = score bits, parent, token, result entry), the node depths and this call's result
+// entries; warp 0 pops, pushes and selects exactly as the CTA-wide form; every thread writes
+// the candidates back. Shared memory: cap * 20 + max_nodes * 4 + width * kTreeMaxK * 12 bytes,
+// cap = max_nodes * topk (the most candidates one tree can hold) + 256 slots of padding, so
+// that a lane's eight-slot loads never need a bounds test (padding keys are -1: popped).
+constexpr int kTreePad = 256;
+struct FastReplay {
+  long long* key;
+  int *par, *tok, *res, *dep, *rtk;
+  double* rpp;
+};
+
+__device__ __forceinline__ FastReplay fast_replay_carve(uint8_t* smem, int cap, int max_nodes) {
+  FastReplay f;
+  f.key = reinterpret_cast<long long*>(smem);
+  f.rpp = reinterpret_cast<double*>(smem + (size_t)cap * 8);
+  f.par = reinterpret_cast<int*>(smem + (size_t)cap * 8 + (size_t)kTreeMaxW * kTreeMaxK * 8);
+  f.tok = f.par + cap;
+  f.res = f.tok + cap;
+  f.dep = f.res + cap;
+  f.rtk = f.dep + max_nodes;
+  return f;
+}
+
+size_t tree_fast_smem_bytes(int max_nodes, int topk) {
+  const size_t cap = (size_t)max_nodes * topk + kTreePad;
+  return cap * 20 + (size_t)max_nodes * 4 + (size_t)kTreeMaxW * kTreeMaxK * 12;
+}
+
+__device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int* depth, double* cscore, int* cparent,
+                                              int* ctoken, int* cres, const int* rtok, const double* rp,
+                                              const TreeArgs& a, int b, int base, int nreq, int n_res_max, int cap) {
+  extern __shared__ __align__(16) uint8_t tree_dsmem[];
+  const FastReplay f = fast_replay_carve(tree_dsmem, cap, a.max_nodes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = a.topk;
+  const int nc0 = h->n_cand, nn0 = h->n_nodes;
+  for (int c = threadIdx.x; c < cap; c += blockDim.x) {  // (slots past the queue: padding)
+    const bool in = c < nc0;
+    f.key[c] = in ? score_key(cscore[c]) : -1;
+    f.par[c] = in ? cparent[c] : 0;
+    f.tok[c] = in ? ctoken[c] : -1;
+    f.res[c] = in ? cres[c] : -1;
+  }
+  for (int u = threadIdx.x; u < nn0; u += blockDim.x) f.dep[u] = depth[u];
+  for (int i = threadIdx.x; i < nreq * kTreeMaxK; i += blockDim.x) {  // this call's entries (other SMs wrote them)
+    f.rtk[i] = __ldcg(rtok + (size_t)base * kTreeMaxK + i);
+    f.rpp[i] = __ldcg(rp + (size_t)base * kTreeMaxK + i);
+  }
+  __shared__ int s_nc;
+  __syncthreads();
+  if (warp == 0) {
+    int nc = nc0, nn = nn0, flags = h->flags, cur = h->cur;
+    int node = cur, r = base;
+    double node_score = score[cur];
+    // Each lane keeps the best two of its own slots (c = lane mod 32): (ck1, ci1) the best
+    // alive one, ck2 the second-best key. A pop reduces the 32 over the warp, and the warp
+    // rescans the winning lane's slots together (lane j takes the j-th of them): every step
+    // has 32 independent loads or shuffles behind it, not a chain of one lane's.
+    long long ck1 = -1, ck2 = -1;
+    int ci1 = INT_MAX;
+    auto offer = [](long long key, int c, long long& k1, int& i1, long long& k2) {
+      if (key < 0) return;  // popped (or not admitted)
+      if (key_better(key, c, k1, i1)) {
+        k2 = k1;
+        k1 = key;
+        i1 = c;
+      } else if (key > k2) {
+        k2 = key;
+      }
+    };
+    // (key, slot) of the best and the second-best key over the warp's 32 values: every lane
+    auto wreduce = [](long long& k1, int& i1, long long& k2) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const long long ok1 = __shfl_xor_sync(0xffffffffu, k1, o), ok2 = __shfl_xor_sync(0xffffffffu, k2, o);
+        const int oi1 = __shfl_xor_sync(0xffffffffu, i1, o);
+        if (key_better(ok1, oi1, k1, i1)) {
+          k2 = k1 > ok2 ? k1 : ok2;
+          k1 = ok1;
+          i1 = oi1;
+        } else if (ok1 > k2) {
+          k2 = ok1;
+        }
+      }
+    };
+    // lane w's slots, scanned by the warp; sel: only the slots the selection admits
+    auto scan_lane = [&](int w, bool sel, long long& k1, int& i1, long long& k2) {
+      k1 = -1;
+      k2 = -1;
+      i1 = INT_MAX;
+      for (int c = w + 32 * lane; c < nc; c += 32 * 32) {
+        const long long key = f.key[c];
+        const bool ok = !sel || (f.res[c] < 0 && f.dep[f.par[c]] + 1 < a.max_depth);
+        offer(ok ? key : -1, c, k1, i1, k2);
+      }
+      wreduce(k1, i1, k2);
+    };
+    // this lane's own slots, eight loads in flight at a time (no bounds test: the slots past
+    // the queue hold padding keys)
+    auto scan_own = [&](bool sel, long long& k1, int& i1, long long& k2) {
+      k1 = -1;
+      k2 = -1;
+      i1 = INT_MAX;
+      for (int c0 = lane; c0 < nc; c0 += 32 * 8) {
+        long long kk[8];
+        int rs[8], ps[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          kk[q] = f.key[c0 + 32 * q];
+          rs[q] = f.res[c0 + 32 * q];
+          ps[q] = f.par[c0 + 32 * q];
+        }
+        if (sel) {
+          int dd[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dd[q] = f.dep[ps[q]];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (!(rs[q] < 0 && dd[q] + 1 < a.max_depth)) kk[q] = -1;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) offer(kk[q], c0 + 32 * q, k1, i1, k2);
+      }
+    };
+    scan_own(false, ck1, ci1, ck2);
+    while (true) {
+      // push the children of `node` from result entry r (lane q: child q)
+      {
+        const bool local = r >= base && r < base + nreq;
+        double c = 0.0;
+        bool keep = false;
+        int tok = -1;
+        if (lane < k) {
+          const size_t at = (size_t)(local ? r - base : r) * kTreeMaxK + lane;
+          tok = local ? f.rtk[at] : __ldcg(rtok + at);
+          if (tok >= 0) {
+            c = node_score * (local ? f.rpp[at] : __ldcg(rp + at));
+            keep = !(a.threshold > 0.0) || c > a.threshold;
+          }
+        }
+        const unsigned kb = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int at = nc + __popc(kb & ((1u << lane) - 1u));
+          f.key[at] = score_key(c);
+          f.par[at] = node;
+          f.tok[at] = tok;
+          f.res[at] = -1;
+        }
+        __syncwarp();
+        const int nc_new = nc + __popc(kb);
+        for (int c2 = nc + ((lane - nc) & 31); c2 < nc_new; c2 += 32) offer(f.key[c2], c2, ck1, ci1, ck2);
+        nc = nc_new;
+      }
+      int stop = 2;
+      while (stop == 2) {  // pops until one needs a row (1) or has its result (0)
+        long long k1 = ck1, k2 = ck2;
+        int i1 = ci1;
+        wreduce(k1, i1, k2);
+        if (i1 == INT_MAX || k1 < 0) {
+          cur = -1;  // no candidate left
+          stop = 1;
+          break;
+        }
+        const double b1 = __longlong_as_double(k1);
+        if (k2 >= 0) {
+          const float f1 = (float)b1, f2 = (float)__longlong_as_double(k2);
+          if (f1 - f2 <= (float)kTreeTieRel * f1) flags |= 1;
+        }
+        const int nid = nn, par = f.par[i1], tk = f.tok[i1], rr = f.res[i1];
+        const int d = f.dep[par] + 1;
+        __syncwarp();
+        if (lane == 0) {
+          f.key[i1] = -1;  // popped
+          f.dep[nid] = d;
+          a.parent_out[(size_t)b * a.max_nodes + nid] = par;
+          a.tokens_out[(size_t)b * a.max_nodes + nid] = tk;
+          score[nid] = b1;
+          depth[nid] = d;
+        }
+        __syncwarp();
+        {  // the winner's lane, rescanned
+          const int w = i1 & 31;
+          long long n1, n2;
+          int ni;
+          scan_lane(w, false, n1, ni, n2);
+          if (lane == w) {
+            ck1 = n1;
+            ci1 = ni;
+            ck2 = n2;
+          }
+        }
+        nn = nid + 1;
+        if (d < a.max_depth && nid + 1 < a.max_nodes) {
+          if (rr >= 0) {  // its row came with an earlier request: expand it now
+            node = nid;
+            node_score = b1;
+            r = rr;
+            stop = 0;
+          } else {
+            cur = nid;  // its row is the next call's first request
+            stop = 1;
+          }
+        } else if (nid + 1 >= a.max_nodes) {
+          cur = -1;  // budget met
+          stop = 1;
+        }  // else: at the depth limit, the next candidate
+      }
+      if (stop == 1) break;
+    }
+    // the next requests: per-lane caches of the best admitted slot, reduced per round
+    int nr = 0;
+    const int n_res = h->n_res;
+    if (cur >= 0) {
+      const int room = min(a.width, n_res_max - n_res);
+      if (room <= 0) {
+        if (lane == 0) report(a.status, SPEC_ERR_CAPACITY);
+        cur = -1;
+      } else {
+        if (lane == 0) {
+          a.req_parent[(size_t)b * a.width] = a.parent_out[(size_t)b * a.max_nodes + cur];
+          a.req_token[(size_t)b * a.width] = a.tokens_out[(size_t)b * a.max_nodes + cur];
+        }
+        nr = 1;
+        long long sk1, sk2;
+        int si1;
+        if (room > 1) scan_own(true, sk1, si1, sk2);
+        for (int q = 1; q < room; ++q) {
+          long long k1 = sk1, k2 = sk2;
+          int i1 = si1;
+          wreduce(k1, i1, k2);
+          if (i1 == INT_MAX || k1 < 0) break;
+          __syncwarp();
+          if (lane == 0) {
+            f.res[i1] = n_res + q;
+            a.req_parent[(size_t)b * a.width + q] = f.par[i1];
+            a.req_token[(size_t)b * a.width + q] = f.tok[i1];
+          }
+          __syncwarp();
+          nr = q + 1;
+          if (q + 1 < room) {
+            const int w = i1 & 31;
+            long long n1, n2;
+            int ni;
+            scan_lane(w, true, n1, ni, n2);
+            if (lane == w) {
+              sk1 = n1;
+              si1 = ni;
+              sk2 = n2;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      for (int q = nr; q < a.width; ++q) {
+        a.req_parent[(size_t)b * a.width + q] = -1;
+        a.req_token[(size_t)b * a.width + q] = -1;
+      }
+      h->n_nodes = nn;
+      h->n_cand = nc;
+      h->cur = cur;
+      h->flags = flags;
+      h->nreq = nr;
+      if (nr > 0) {
+        h->req_base = n_res;
+        h->n_res = n_res + nr;
+      }
+      a.req_n[b] = nr;
+      a.n_nodes_out[b] = nn;
+      a.next_node[b] = cur;
+      if (a.flags != nullptr) a.flags[b] = (uint8_t)flags;
+      s_nc = nc;
+    }
+  }
+  __syncthreads();
+  const int nc = s_nc;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {  // the queue back to the state
+    const long long key = f.key[c];
+    cscore[c] = key < 0 ? -1.0 : __longlong_as_double(key);
+    cparent[c] = f.par[c];
+    ctoken[c] = f.tok[c];
+    cres[c] = f.res[c];
+  }
+}
+
 // ------------------------------------------------------------------ the multi-row call
 // Exact batching of the construction above. A queued candidate's expansion (its draft row's
 // top-k tokens and probabilities) depends on the candidate alone -- its parent and token --
@@ -592,7 +868,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
 template <int KMAX, bool kVec>
 __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThreads, 1)
     tree_expand_multi_kernel(const float* __restrict__ logits, int vocab, long row_stride, long req_stride,
-                             TreeArgs a) {
+                             TreeArgs a, int fast_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int j = blockIdx.y, b = blockIdx.z;
@@ -646,6 +922,11 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
   }
   __syncthreads();
   if (!s_last) return;
+  if (fast_cap > 0) {  // the queue fits in shared memory: one warp pops
+    tree_replay_fast(h, score, depth, cscore, cparent, ctoken, cres, rtok, rp, a, b, s_base, nreq, l.n_res_max,
+                     fast_cap);
+    return;
+  }
 
   // ---- the last cluster: expand the awaiting node from entry req_base, then pop
   // (the other clusters' entries are read from L2: they were written on other SMs)
@@ -801,12 +1082,17 @@ int launch_tree_expand_multi(const float* logits, int vocab, long row_stride, lo
   const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 && vocab % 4 == 0 && row_stride % 4 == 0 &&
                    req_stride % 4 == 0;
   const dim3 grid(kTreeCluster, a.width, batch);
+  // the queue in shared memory when it fits beside the row scan's own (no raised limit needed)
+  const size_t fsm = tree_fast_smem_bytes(a.max_nodes, a.topk);
+  const bool fast = fsm <= kTreeFastSmemMax;
+  const size_t dsm = fast ? fsm : 0;
+  const int cap = fast ? a.max_nodes * a.topk + kTreePad : 0;
   cudaError_t e;
-#define SPECV_TREE_LAUNCH(K)                                                                               \
-  e = vec ? launch_pdl(tree_expand_multi_kernel<K, true>, grid, dim3(kTreeThreads), 0, stream, logits, vocab,  \
-                       row_stride, req_stride, a)                                                          \
-          : launch_pdl(tree_expand_multi_kernel<K, false>, grid, dim3(kTreeThreads), 0, stream, logits, vocab, \
-                       row_stride, req_stride, a)
+#define SPECV_TREE_LAUNCH(K)                                                                                 \
+  e = vec ? launch_pdl(tree_expand_multi_kernel<K, true>, grid, dim3(kTreeThreads), dsm, stream, logits, vocab,  \
+                       row_stride, req_stride, a, cap)                                                       \
+          : launch_pdl(tree_expand_multi_kernel<K, false>, grid, dim3(kTreeThreads), dsm, stream, logits, vocab, \
+                       row_stride, req_stride, a, cap)
   if (a.topk <= 4)
     SPECV_TREE_LAUNCH(4);
   else if (a.topk <= 10)
