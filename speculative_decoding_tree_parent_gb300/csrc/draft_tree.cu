@@ -459,6 +459,15 @@ __device__ __forceinline__ void cand_best(const double* cscore, int nc, Ok ok, l
   }
 }
 
+// Whether a pop's best two scores (their keys) lie within a relative 1e-6, in fp32. Keys 2^36
+// or more apart (same sign, non-negative doubles) differ by more than 2^-17 relative, which
+// no fp32 rounding brings under 1e-6: those skip the conversions (fp64 pipe, slow here).
+__device__ __forceinline__ bool near_tie(long long k1, long long k2) {
+  if (k2 < 0 || k1 - k2 >= (1ll << 36)) return false;
+  const float f1 = (float)__longlong_as_double(k1), f2 = (float)__longlong_as_double(k2);
+  return f1 - f2 <= (float)kTreeTieRel * f1;
+}
+
 // Pops the best candidate as node n_nodes (by lane 0 of warp 0, with k1 / i1 / k2 from
 // cand_best): writes its parent, token, score and depth and marks the slot popped. Returns the
 // new node id, or -1 when no candidate is left. Sets flags bit 0 on a near tie.
@@ -466,10 +475,7 @@ __device__ __forceinline__ int pop_node(TreeHeader* h, double* score, int* depth
                                         const int* ctoken, const TreeArgs& a, int b, long long k1, int i1, long long k2) {
   if (i1 == INT_MAX || k1 < 0) return -1;
   const double b1 = __longlong_as_double(k1);
-  if (k2 >= 0) {  // near tie: the gap relative to the best, in fp32 (ample for 1e-6)
-    const float f1 = (float)b1, f2 = (float)__longlong_as_double(k2);
-    if (f1 - f2 <= (float)kTreeTieRel * f1) h->flags |= 1;
-  }
+  if (near_tie(k1, k2)) h->flags |= 1;  // (the gap relative to the best, in fp32: ample for 1e-6)
   const int nid = h->n_nodes;
   const int par = cparent[i1];
   cscore[i1] = -1.0;  // popped
@@ -568,6 +574,29 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kTreeThre
 // the candidates back. Shared memory: cap * 20 + max_nodes * 4 + width * kTreeMaxK * 12 bytes,
 // cap = max_nodes * topk (the most candidates one tree can hold) + 256 slots of padding, so
 // that a lane's eight-slot loads never need a bounds test (padding keys are -1: popped).
+// The warp's best two (key, slot) pairs from every lane's own best two (keys >= -1, -1 for
+// none; slots distinct, INT_MAX for none): the larger key first, the lower slot on equal keys.
+// Each step is one redux.sync over 32-bit halves, so no lane waits on a chain of shuffles.
+__device__ __forceinline__ void warp_top2(long long& k1, int& i1, long long& k2, int& i2) {
+  auto best = [](long long k, int i, long long& km, int& im) {
+    const unsigned long long u = (unsigned long long)(k + 1);  // -1 -> 0
+    const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(u >> 32));
+    const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(u >> 32) == hi ? (unsigned)u : 0u);
+    const unsigned long long m = ((unsigned long long)hi << 32) | lo;
+    im = (int)__reduce_min_sync(0xffffffffu, u == m ? (unsigned)i : 0xffffffffu);
+    km = (long long)m - 1;
+  };
+  long long m1, m2;
+  int j1, j2;
+  best(k1, i1, m1, j1);
+  const bool won = i1 == j1;  // this lane held the winner: it offers its second
+  best(won ? k2 : k1, won ? i2 : i1, m2, j2);
+  k1 = m1;
+  i1 = j1;
+  k2 = m2;
+  i2 = j2;
+}
+
 constexpr int kTreePad = 256;
 struct FastReplay {
   long long* key;
@@ -594,8 +623,10 @@ size_t tree_fast_smem_bytes(int max_nodes, int topk) {
 
 __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int* depth, double* cscore, int* cparent,
                                               int* ctoken, int* cres, const int* rtok, const double* rp,
-                                              const TreeArgs& a, int b, int base, int nreq, int n_res_max, int cap) {
+                                              const TreeArgs& a_ref, int b, int base, int nreq, int n_res_max,
+                                              int cap) {
   extern __shared__ __align__(16) uint8_t tree_dsmem[];
+  const TreeArgs a = a_ref;  // (in registers: the stores below cannot alias it)
   const FastReplay f = fast_replay_carve(tree_dsmem, cap, a.max_nodes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = a.topk;
@@ -634,32 +665,32 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
         k2 = key;
       }
     };
-    // (key, slot) of the best and the second-best key over the warp's 32 values: every lane
-    auto wreduce = [](long long& k1, int& i1, long long& k2) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const long long ok1 = __shfl_xor_sync(0xffffffffu, k1, o), ok2 = __shfl_xor_sync(0xffffffffu, k2, o);
-        const int oi1 = __shfl_xor_sync(0xffffffffu, i1, o);
-        if (key_better(ok1, oi1, k1, i1)) {
-          k2 = k1 > ok2 ? k1 : ok2;
-          k1 = ok1;
-          i1 = oi1;
-        } else if (ok1 > k2) {
-          k2 = ok1;
-        }
+    // the best two of a lane's values (slot of the second too)
+    auto offer2 = [](long long key, int c, long long& k1, int& i1, long long& k2, int& i2) {
+      if (key < 0) return;
+      if (key_better(key, c, k1, i1)) {
+        k2 = k1;
+        i2 = i1;
+        k1 = key;
+        i1 = c;
+      } else if (key_better(key, c, k2, i2)) {
+        k2 = key;
+        i2 = c;
       }
     };
-    // lane w's slots, scanned by the warp; sel: only the slots the selection admits
-    auto scan_lane = [&](int w, bool sel, long long& k1, int& i1, long long& k2) {
+    // lane w's slots, scanned by the warp (lane j takes the j-th of them), with their best two;
+    // sel: only the slots the selection admits
+    auto scan_lane = [&](int w, bool sel, long long& k1, int& i1, long long& k2, int& i2) {
       k1 = -1;
       k2 = -1;
       i1 = INT_MAX;
+      i2 = INT_MAX;
       for (int c = w + 32 * lane; c < nc; c += 32 * 32) {
         const long long key = f.key[c];
         const bool ok = !sel || (f.res[c] < 0 && f.dep[f.par[c]] + 1 < a.max_depth);
-        offer(ok ? key : -1, c, k1, i1, k2);
+        offer2(ok ? key : -1, c, k1, i1, k2, i2);
       }
-      wreduce(k1, i1, k2);
+      warp_top2(k1, i1, k2, i2);
     };
     // this lane's own slots, eight loads in flight at a time (no bounds test: the slots past
     // the queue hold padding keys)
@@ -688,6 +719,7 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
         for (int q = 0; q < 8; ++q) offer(kk[q], c0 + 32 * q, k1, i1, k2);
       }
     };
+    const bool use_thr = a.threshold > 0.0;
     scan_own(false, ck1, ci1, ck2);
     while (true) {
       // push the children of `node` from result entry r (lane q: child q)
@@ -701,7 +733,7 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
           tok = local ? f.rtk[at] : __ldcg(rtok + at);
           if (tok >= 0) {
             c = node_score * (local ? f.rpp[at] : __ldcg(rp + at));
-            keep = !(a.threshold > 0.0) || c > a.threshold;
+            keep = !use_thr || c > a.threshold;
           }
         }
         const unsigned kb = __ballot_sync(0xffffffffu, keep);
@@ -720,18 +752,15 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
       int stop = 2;
       while (stop == 2) {  // pops until one needs a row (1) or has its result (0)
         long long k1 = ck1, k2 = ck2;
-        int i1 = ci1;
-        wreduce(k1, i1, k2);
+        int i1 = ci1, i2 = INT_MAX;  // (i2: the runner-up's slot, unused: ck2 is a key alone)
+        warp_top2(k1, i1, k2, i2);
         if (i1 == INT_MAX || k1 < 0) {
           cur = -1;  // no candidate left
           stop = 1;
           break;
         }
         const double b1 = __longlong_as_double(k1);
-        if (k2 >= 0) {
-          const float f1 = (float)b1, f2 = (float)__longlong_as_double(k2);
-          if (f1 - f2 <= (float)kTreeTieRel * f1) flags |= 1;
-        }
+        if (near_tie(k1, k2)) flags |= 1;
         const int nid = nn, par = f.par[i1], tk = f.tok[i1], rr = f.res[i1];
         const int d = f.dep[par] + 1;
         __syncwarp();
@@ -747,8 +776,8 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
         {  // the winner's lane, rescanned
           const int w = i1 & 31;
           long long n1, n2;
-          int ni;
-          scan_lane(w, false, n1, ni, n2);
+          int ni, ni2;
+          scan_lane(w, false, n1, ni, n2, ni2);
           if (lane == w) {
             ck1 = n1;
             ci1 = ni;
@@ -787,13 +816,33 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
           a.req_token[(size_t)b * a.width] = a.tokens_out[(size_t)b * a.max_nodes + cur];
         }
         nr = 1;
-        long long sk1, sk2;
-        int si1;
-        if (room > 1) scan_own(true, sk1, si1, sk2);
+        // Each lane keeps its best two admitted slots with their indices; a round reduces the
+        // bests, the winning lane promotes its second, and only a lane that wins without a
+        // known second rescans (with the warp).
+        long long sk1 = -1, sk2 = -1;
+        int si1 = INT_MAX, si2 = INT_MAX;
+        bool sec = true;  // (sk2, si2) is this lane's true second
+        if (room > 1) {
+          for (int c0 = lane; c0 < nc; c0 += 32 * 8) {
+            long long kk[8];
+            int rs[8], ps[8], dd[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              kk[q] = f.key[c0 + 32 * q];
+              rs[q] = f.res[c0 + 32 * q];
+              ps[q] = f.par[c0 + 32 * q];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dd[q] = f.dep[ps[q]];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              offer2(rs[q] < 0 && dd[q] + 1 < a.max_depth ? kk[q] : -1, c0 + 32 * q, sk1, si1, sk2, si2);
+          }
+        }
         for (int q = 1; q < room; ++q) {
           long long k1 = sk1, k2 = sk2;
-          int i1 = si1;
-          wreduce(k1, i1, k2);
+          int i1 = si1, i2 = si2;
+          warp_top2(k1, i1, k2, i2);
           if (i1 == INT_MAX || k1 < 0) break;
           __syncwarp();
           if (lane == 0) {
@@ -803,15 +852,25 @@ __device__ __noinline__ void tree_replay_fast(TreeHeader* h, double* score, int*
           }
           __syncwarp();
           nr = q + 1;
-          if (q + 1 < room) {
-            const int w = i1 & 31;
+          const int w = i1 & 31;
+          const bool resc = __shfl_sync(0xffffffffu, sec ? 0 : 1, w) != 0;
+          if (lane == w && !resc) {  // promote the known second
+            sk1 = sk2;
+            si1 = si2;
+            sk2 = -1;
+            si2 = INT_MAX;
+            sec = false;
+          }
+          if (resc && q + 1 < room) {  // lane w's slots, by the warp: its best two
             long long n1, n2;
-            int ni;
-            scan_lane(w, true, n1, ni, n2);
+            int ni1, ni2;
+            scan_lane(w, true, n1, ni1, n2, ni2);
             if (lane == w) {
               sk1 = n1;
-              si1 = ni;
+              si1 = ni1;
               sk2 = n2;
+              si2 = ni2;
+              sec = true;
             }
           }
         }
