@@ -22,7 +22,7 @@
 //   accept_stats_kernel    grid = chunks x nodes. Per chunk of a row of target and
 //                          draft logits: max and sum of exp((x - max) / T) (fp32
 //                          elements from ex2.approx, Kahan compensated per thread,
-//                          double-float across threads, stored in fp64). The walk
+//                          double-float across threads and stored so). The walk
 //                          merges a node's chunk partials when it visits the node.
 //   accept_walk_kernel     one 8-CTA cluster per sequence. The decisions at a node
 //                          need sums over the vocabulary of the residual
@@ -60,13 +60,13 @@ struct alignas(8) ArgPartial {
   float v;
   int i;
 };
-struct StatPartial {
+struct StatPartial {  // a chunk's max and sum of exp((x - max) / T), the sums as double-float
   float m_p, m_q;
-  double s_p, s_q;
+  float sp_hi, sp_lo, sq_hi, sq_lo;
 };
-struct NodeStats {
+struct NodeStats {  // a row's max and the reciprocal of its softmax normaliser (fp32)
   float m_p, m_q;
-  double z_p, z_q;
+  float inv_zp, inv_zq;
 };
 
 // Workspace layout for spec_accept (offsets in bytes, each 256-aligned). The greedy
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
   const float Mp = block_max(ep.m, redf);
   const float Mq = block_max(eq.m, redf);
   // each thread's compensated sum rescaled to the block max as a double-float, then summed
-  // across the block in double-float (fp64 only for the stored result)
+  // across the block in double-float
   auto rescaled = [&](const OnlineExp& e, float M) {
     if (e.m == -INFINITY) return F2{0.f, 0.f};
     const float f = expf((e.m - M) * invT);
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
       tp = f2_add(tp, F2{red_hi[0][w], red_lo[0][w]});
       tq = f2_add(tq, F2{red_hi[1][w], red_lo[1][w]});
     }
-    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, f2_to_d(tp), f2_to_d(tq)};
+    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, tp.hi, tp.lo, tq.hi, tq.lo};
     pdl_trigger();
   }
 }
@@ -772,33 +772,35 @@ __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float 
     mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
     mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
   }
-  double zp = 0.0, zq = 0.0;
+  F2 zp{0.f, 0.f}, zq{0.f, 0.f};  // double-float throughout: fp64 is slow on this part
   for (int k = lane; k < chunks; k += 32) {
-    const float m_p = __ldcg(&part[k].m_p), m_q = __ldcg(&part[k].m_q);
-    if (m_p != -INFINITY) zp += __ldcg(&part[k].s_p) * (double)expf((m_p - mp) * invT);
-    if (m_q != -INFINITY) zq += __ldcg(&part[k].s_q) * (double)expf((m_q - mq) * invT);
+    const StatPartial& sp = part[k];
+    const float m_p = __ldcg(&sp.m_p), m_q = __ldcg(&sp.m_q);
+    if (m_p != -INFINITY) zp = f2_add(zp, f2_mul_f(F2{__ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo)}, expf((m_p - mp) * invT)));
+    if (m_q != -INFINITY) zq = f2_add(zq, f2_mul_f(F2{__ldcg(&sp.sq_hi), __ldcg(&sp.sq_lo)}, expf((m_q - mq) * invT)));
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    zp += __shfl_xor_sync(0xffffffffu, zp, o);
-    zq += __shfl_xor_sync(0xffffffffu, zq, o);
-  }
-  return NodeStats{mp, mq, zp, zq};
+  zp = f2_warp_sum(zp);
+  zq = f2_warp_sum(zq);
+  return NodeStats{mp, mq, f2_rcp(zp), f2_rcp(zq)};
 }
 
 // ---------------------------------------------------------------- stochastic: walk
 
 // The CTA's slice [c_lo, c_hi) of the vocabulary (a multiple of 4 tokens long, so rows
 // with 16-byte alignment stage with float4 loads) is cut into kWalkWarps contiguous
-// segments, one per warp (a multiple of 32 tokens each); lane l of a warp takes the
+// segments, one per warp (a multiple of 256 tokens each); lane l of a warp takes the
 // segment's tokens l, l + 32, ... At a node's first pass p and q of the slice are staged
-// in shared memory as fp32 values (dynamic shared memory: kWalkStage of each at most,
-// i.e. vocabularies up to 8 x kWalkStage tokens; larger ones are evaluated from global
-// memory on every pass, with the same arithmetic). Sums: fp32 Kahan per lane, then
+// in shared memory as fp32 values, zero past the slice up to kWalkWarps whole segments
+// (a zero p and q add nothing), so the passes load eight tokens at a time without a
+// bounds test (dynamic shared memory: kWalkStage of each at most, i.e. vocabularies up to
+// about 8 x kWalkStage tokens; larger ones are evaluated from global memory on every pass,
+// with the same arithmetic). Sums: fp32 Kahan per lane, then
 // double-float (an fp32 pair, error-free adds, about 48 significant bits) across lanes,
-// warps and the CTAs of the cluster. fp64 is kept to a few operations per decision: on
-// this part a dependent fp64 operation costs hundreds of cycles.
+// warps and the CTAs of the cluster. The decisions are taken in double-float as well, with no
+// fp64: on this part a dependent fp64 operation costs hundreds of cycles.
 constexpr int kWalkWarps = kWalkThreads / 32;
+constexpr int kWalkKids = 32;  // children listed per batch
+static_assert(kMaxTreeNodes == 32 * 32, "the children bitmap is one word per lane of a warp");
 constexpr int kWalkStage = 24576;
 
 struct WalkShared {
@@ -807,6 +809,11 @@ struct WalkShared {
   float pre_hi[kWalkWarps], pre_lo[kWalkWarps];    // their exclusive prefix (bonus draw)
   float cta_hi[2], cta_lo[2];         // this CTA's pass total (double-buffered by pass parity)
   unsigned kids[kMaxTreeNodes / 32];  // children bitmap of the current node
+  // the next children to test (ascending id) with what their tests read: loaded together,
+  // so the tests do not each wait on a token load and then on its logits
+  int kid_c[kWalkKids], kid_x[kWalkKids];
+  float kid_p[kWalkKids], kid_q[kWalkKids], kid_u[kWalkKids];
+  int nkids;
   int found;                          // bonus token found by this CTA (-1 = none)
   int found_flag;
 };
@@ -835,15 +842,28 @@ struct WalkSlice {
   }
 };
 
+// A CTA's slice length, its segment length, and the floats staged per row (p, and q after
+// it): the kernel's layout and the launch's dynamic shared memory both come from here.
+__host__ __device__ __forceinline__ int walk_per_cta(int vocab) {
+  return ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
+}
+__host__ __device__ __forceinline__ int walk_seg(int vocab) {
+  return ((walk_per_cta(vocab) + kWalkWarps - 1) / kWalkWarps + 255) & ~255;
+}
+__host__ __device__ __forceinline__ int walk_stage_floats(int vocab) {  // 0: not staged
+  const int padded = kWalkWarps * walk_seg(vocab);
+  return padded <= kWalkStage ? padded : 0;
+}
+
 __device__ __forceinline__ WalkSlice walk_slice(int vocab, int rank, float* smem) {
-  const int per_cta = ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
+  const int per_cta = walk_per_cta(vocab);
   WalkSlice s;
   s.c_lo = rank * per_cta;
   s.n = max(0, min(vocab, s.c_lo + per_cta) - s.c_lo);
-  s.seg = (((s.n + kWalkWarps - 1) / kWalkWarps) + 31) & ~31;
-  const bool staged = per_cta <= kWalkStage;
-  s.sp = staged ? smem : nullptr;
-  s.sq = staged ? smem + per_cta : nullptr;
+  s.seg = walk_seg(vocab);  // (the same in every CTA)
+  const int staged = walk_stage_floats(vocab);
+  s.sp = staged > 0 ? smem : nullptr;
+  s.sq = staged > 0 ? smem + staged : nullptr;
   return s;
 }
 
@@ -881,6 +901,10 @@ __device__ void walk_stage(const WalkSlice& sl, const RowEval& ev, bool vec) {
       sl.sq[i] = ev.q(sl.c_lo + i);
     }
   }
+  for (int i = sl.n + threadIdx.x; i < kWalkWarps * sl.seg; i += kWalkThreads) {  // padding
+    sl.sp[i] = 0.f;
+    sl.sq[i] = 0.f;
+  }
   __syncthreads();
 }
 
@@ -893,11 +917,25 @@ __device__ F2 walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
   float s = 0.f, comp = 0.f;
-  for (int i = s_lo + lane; i < s_hi; i += 32) {
-    const float y = sl.resid(ev, i, c) - comp;
+  auto add = [&](float x) {  // fp32 Kahan step
+    const float y = x - comp;
     const float z = s + y;
     comp = (z - s) - y;
     s = z;
+  };
+  if (sl.sp != nullptr) {  // staged and padded: whole segments, eight tokens in flight
+    for (int i0 = s_lo + lane; i0 < s_lo + sl.seg; i0 += 32 * 8) {
+      float pv[8], qv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        pv[u] = sl.sp[i0 + 32 * u];
+        qv[u] = sl.sq[i0 + 32 * u];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) add(c == 0.f ? pv[u] : fmaxf(pv[u] - c * qv[u], 0.f));
+    }
+  } else {
+    for (int i = s_lo + lane; i < s_hi; i += 32) add(sl.resid(ev, i, c));
   }
   const F2 w = f2_warp_sum(F2{s, -comp});
   if (lane == 0) {
@@ -919,11 +957,17 @@ __device__ F2 walk_pass(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& 
   }
   cl.sync();
   const int rank = (int)cl.block_rank();
-  F2 all{0.f, 0.f}, pre{0.f, 0.f};
+  float xh[kWalkCluster], xl[kWalkCluster];  // every CTA's total: all sixteen loads first
+#pragma unroll
   for (int r = 0; r < kWalkCluster; ++r) {
-    const F2 x{*cl.map_shared_rank(&sh.cta_hi[parity], r), *cl.map_shared_rank(&sh.cta_lo[parity], r)};
+    xh[r] = *cl.map_shared_rank(&sh.cta_hi[parity], r);
+    xl[r] = *cl.map_shared_rank(&sh.cta_lo[parity], r);
+  }
+  F2 all{0.f, 0.f}, pre{0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < kWalkCluster; ++r) {
     if (r == rank) pre = all;
-    all = f2_add(all, x);
+    all = f2_add(all, F2{xh[r], xl[r]});
   }
   if (cta_pre != nullptr) *cta_pre = pre;
   return all;
@@ -967,7 +1011,7 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     __syncthreads();
     const NodeStats st = sh.st;
     const RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
-                     (float)(1.0 / st.z_p), (float)(1.0 / st.z_q)};
+                     st.inv_zp, st.inv_zq};
     bool staged = false;  // p and q of v's slice in shared memory (done before v's first pass)
     auto stage = [&]() {
       if (!staged && sl.sp != nullptr) walk_stage(sl, ev, vec);
@@ -976,45 +1020,83 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     for (int c = v + 1 + threadIdx.x; c < n; c += blockDim.x)
       if (__ldg(parent + base + c) == v) atomicOr(&sh.kids[c >> 5], 1u << (c & 31));
     __syncthreads();
-    double cc = 0.0, ss = 1.0;  // residual r = max(p - cc q, 0) / ss
+    F2 cc{0.f, 0.f}, ss{1.f, 0.f};  // residual r = max(p - cc q, 0) / ss (double-float)
     int accepted = -1;
-    for (int w = (v + 1) >> 5; w < kMaxTreeNodes / 32 && accepted < 0; ++w) {
-      unsigned bits = sh.kids[w];
-      while (bits) {
-        const int c = (w << 5) + __ffs(bits) - 1;
-        bits &= bits - 1;
+    int next_c = v + 1;  // children with ids >= next_c are not listed yet
+    while (accepted < 0) {
+      // list the next children (ascending id): warp 0, one bitmap word per lane
+      if (warp == 0) {
+        unsigned bits = sh.kids[lane];
+        const int w0 = next_c >> 5;
+        if (lane < w0) bits = 0u;
+        if (lane == w0) bits &= ~((1u << (next_c & 31)) - 1u);
+        const int cnt = __popc(bits);
+        int incl = cnt;  // inclusive prefix of the counts over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int at = incl - cnt;
+        while (bits && at < kWalkKids) {
+          sh.kid_c[at++] = (lane << 5) + __ffs(bits) - 1;
+          bits &= bits - 1;
+        }
+        if (lane == 31) sh.nkids = min(incl, kWalkKids);
+      }
+      __syncthreads();
+      const int nk = sh.nkids;
+      if (nk == 0) break;
+      // their tokens, then p(x), q(x) (the fp32 values the passes use) and u: one round trip each
+      for (int j = threadIdx.x; j < nk; j += blockDim.x) {
+        const int c = sh.kid_c[j];
         const int x = __ldg(tokens + base + c);
+        sh.kid_x[j] = x;
+        const bool okx = x >= 0 && x < vocab;
+        sh.kid_p[j] = okx ? ev.p(x) : 0.f;
+        sh.kid_q[j] = okx ? ev.q(x) : 0.f;
+        sh.kid_u[j] = __ldg(uniforms + 2 * (size_t)(base + c));
+      }
+      __syncthreads();
+      for (int j = 0; j < nk; ++j) {
+        const int c = sh.kid_c[j];
+        const int x = sh.kid_x[j];
         if (x < 0 || x >= vocab) {
           if (writer) report(status, SPEC_ERR_INDEX);
           continue;
         }
-        // p(x), q(x): the fp32 values the passes use; the test u < max(p - cc q, 0) / (ss q)
-        // as u ss q < max(p - cc q, 0) in fp64, with no exponential or division there
-        const double px = (double)ev.p(x), qx = (double)ev.q(x);
-        const double u = (double)__ldg(uniforms + 2 * (size_t)(base + c));
-        const double num = fmax(fma(-cc, qx, px), 0.0);
+        // the test u < max(p - cc q, 0) / (ss q) as u ss q < max(p - cc q, 0) in double-float
+        // (about 48 bits: a decision it could take otherwise than fp64 lies far inside the
+        // flagged band), with no exponential or division there
+        const float px = sh.kid_p[j], qx = sh.kid_q[j], u = sh.kid_u[j];
+        const F2 cq = f2_mul_f(cc, qx);
+        F2 num = f2_add(F2{px, 0.f}, F2{-cq.hi, -cq.lo});
+        if (!f2_gt(num, F2{0.f, 0.f})) num = F2{0.f, 0.f};
         bool ok;
-        if (qx > 0.0) {
-          const double den = ss * qx;
-          const double lhs = u * den;
-          if (fabs(lhs - num) <= kTieEps * den) flag |= 1;
-          ok = lhs < num;
+        if (qx > 0.f) {
+          const F2 den = f2_mul_f(ss, qx);
+          const F2 lhs = f2_mul_f(den, u);
+          const F2 gap = f2_add(lhs, F2{-num.hi, -num.lo});
+          if (fabsf(gap.hi + gap.lo) <= (float)kTieEps * (den.hi + den.lo)) flag |= 1;
+          ok = f2_gt(num, lhs);
         } else {
-          ok = num > 0.0;
+          ok = f2_gt(num, F2{0.f, 0.f});
         }
         if (ok) {
           accepted = c;
           break;
         }
         stage();
-        const double cn = cc + ss;
-        const double sn = f2_to_d(walk_pass(cl, sh, sl, ev, (float)cn, parity, false, nullptr));
+        const F2 cn = f2_add(cc, ss);
+        const F2 sn = walk_pass(cl, sh, sl, ev, cn.hi + cn.lo, parity, false, nullptr);
         parity ^= 1;
-        if (sn > 0.0) {
+        if (f2_gt(sn, F2{0.f, 0.f})) {
           cc = cn;
           ss = sn;
         }
       }
+      next_c = sh.kid_c[nk - 1] + 1;
+      __syncthreads();  // (the list is rewritten next round)
     }
     __syncthreads();  // everyone done with sh.kids before the next node rebuilds it
     if (accepted >= 0) {
@@ -1036,10 +1118,9 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     // segment holding the threshold; its warp scans it 32 tokens at a time.
     {
       stage();
-      const float cf = (float)cc;
+      const float cf = cc.hi + cc.lo;
       F2 cta_pre{0.f, 0.f};
       const F2 total2 = walk_pass(cl, sh, sl, ev, cf, parity, true, &cta_pre);
-      const double total = f2_to_d(total2);
       parity ^= 1;
       if (threadIdx.x == 0) {
         sh.found = -1;
@@ -1047,42 +1128,67 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
       }
       __syncthreads();
       // threshold and segment bounds in double-float: the segment intervals tile the line
-      const F2 thr = d_to_f2((double)__ldg(uniforms + 2 * (size_t)(base + v) + 1) * total);
+      const F2 thr = f2_mul_f(total2, __ldg(uniforms + 2 * (size_t)(base + v) + 1));
       const int s_lo = warp * sl.seg, s_hi = min(sl.n, s_lo + sl.seg);
       const F2 seg_start = f2_add(cta_pre, F2{sh.pre_hi[warp], sh.pre_lo[warp]});
       const F2 seg_end = f2_add(seg_start, F2{sh.part_hi[warp], sh.part_lo[warp]});
       if (s_hi > s_lo && !f2_gt(seg_start, thr) && f2_gt(seg_end, thr)) {  // (warp-uniform)
+        // The segment holds the threshold. Lane l sums its own contiguous run of sub = seg / 32
+        // tokens (read in a rotated order, so the lanes hit distinct banks), a double-float scan
+        // over the lanes finds the run where the cumulative residual crosses, and that run's
+        // lane walks it in order for the token.
         const F2 loc = f2_add(thr, F2{-seg_start.hi, -seg_start.lo});
-        const float band = (float)(kBonusEps * total);
-        F2 carry{0.f, 0.f};
-        int tok = -1, last_pos = -1, fl = 0;
-        for (int i0 = s_lo; i0 < s_hi && tok < 0; i0 += 32) {
-          const int i = i0 + lane;
-          const float rv = i < s_hi ? sl.resid(ev, i, cf) : 0.f;
-          F2 inc{rv, 0.f};  // inclusive scan of the round (double-float), then the carry
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const F2 y{__shfl_up_sync(0xffffffffu, inc.hi, o), __shfl_up_sync(0xffffffffu, inc.lo, o)};
-            if (lane >= o) inc = f2_add(y, inc);
-          }
-          const F2 cum = f2_add(carry, inc);
-          const unsigned hit = __ballot_sync(0xffffffffu, i < s_hi && f2_gt(cum, loc));
-          const unsigned pos = __ballot_sync(0xffffffffu, i < s_hi && rv > 0.f);
-          if (pos) last_pos = i0 + 31 - __clz(pos);
-          if (hit) {
-            const int l = __ffs(hit) - 1;
-            tok = sl.c_lo + i0 + l;
-            // distances of the crossing token's two CDF edges from the threshold
-            const F2 da = f2_add(cum, F2{-loc.hi, -loc.lo});
-            const F2 db = f2_add(da, F2{-rv, 0.f});
-            const float d_after = __shfl_sync(0xffffffffu, da.hi + da.lo, l);
-            const float d_before = __shfl_sync(0xffffffffu, db.hi + db.lo, l);
-            if (fabsf(d_after) <= band || fabsf(d_before) <= band) fl = 2;
-          }
-          carry = F2{__shfl_sync(0xffffffffu, cum.hi, 31), __shfl_sync(0xffffffffu, cum.lo, 31)};
+        const float band = (float)kBonusEps * (total2.hi + total2.lo);
+        const int sub = sl.seg >> 5;
+        const int r_lo = s_lo + lane * sub, r_hi = min(s_hi, r_lo + sub);
+        float rs = 0.f, rc = 0.f;
+        int lp = -1;  // the run's last token with positive residual
+        const int rot = lane % sub;
+        for (int t = 0; t < sub; ++t) {
+          const int i = r_lo + (t + rot < sub ? t + rot : t + rot - sub);
+          const float rv = i < r_hi ? sl.resid(ev, i, cf) : 0.f;
+          const float y = rv - rc, z = rs + y;
+          rc = (z - rs) - y;
+          rs = z;
+          if (rv > 0.f && i > lp) lp = i;
         }
-        if (tok < 0) {  // rounding put the crossing just past this segment's last mass
-          tok = sl.c_lo + (last_pos >= 0 ? last_pos : s_lo);
+        F2 inc{rs, -rc};  // inclusive scan of the runs' sums over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const F2 y{__shfl_up_sync(0xffffffffu, inc.hi, o), __shfl_up_sync(0xffffffffu, inc.lo, o)};
+          if (lane >= o) inc = f2_add(y, inc);
+        }
+        F2 exc{__shfl_up_sync(0xffffffffu, inc.hi, 1), __shfl_up_sync(0xffffffffu, inc.lo, 1)};
+        if (lane == 0) exc = F2{0.f, 0.f};
+        const unsigned hit = __ballot_sync(0xffffffffu, r_hi > r_lo && f2_gt(inc, loc));
+        int tok = -1, fl = 0;
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          if (lane == l) {
+            F2 cum = exc;
+            for (int i = r_lo; i < r_hi; ++i) {
+              const float rv = sl.resid(ev, i, cf);
+              const F2 nxt = f2_add(cum, F2{rv, 0.f});
+              if (f2_gt(nxt, loc)) {
+                tok = sl.c_lo + i;
+                // distances of the crossing token's two CDF edges from the threshold
+                const F2 da = f2_add(nxt, F2{-loc.hi, -loc.lo});
+                const F2 db = f2_add(cum, F2{-loc.hi, -loc.lo});
+                if (fabsf(da.hi + da.lo) <= band || fabsf(db.hi + db.lo) <= band) fl = 2;
+                break;
+              }
+              cum = nxt;
+            }
+            if (tok < 0) {  // the in-order sum fell short of the run's total: at its last mass
+              tok = sl.c_lo + (lp >= 0 ? lp : r_lo);
+              fl = 2;
+            }
+          }
+          tok = __shfl_sync(0xffffffffu, tok, l);
+          fl = __shfl_sync(0xffffffffu, fl, l);
+        } else {  // rounding put the crossing just past this segment's last mass
+          const int last = __reduce_max_sync(0xffffffffu, (unsigned)(lp + 1)) - 1;
+          tok = sl.c_lo + (last >= 0 ? last : s_lo);
           fl = 2;
         }
         if (lane == 0) {
@@ -1092,14 +1198,19 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
       }
       cl.sync();
       if (rank == 0 && threadIdx.x == 0) {
-        int tok = -1;
-        for (int r = 0; r < kWalkCluster && tok < 0; ++r) {
-          const int f = *cl.map_shared_rank(&sh.found, r);
-          if (f >= 0) {
-            tok = f;
-            flag |= *cl.map_shared_rank(&sh.found_flag, r);
-          }
+        int fs[kWalkCluster], ffl[kWalkCluster];  // all sixteen loads first
+#pragma unroll
+        for (int r = 0; r < kWalkCluster; ++r) {
+          fs[r] = *cl.map_shared_rank(&sh.found, r);
+          ffl[r] = *cl.map_shared_rank(&sh.found_flag, r);
         }
+        int tok = -1;
+#pragma unroll
+        for (int r = 0; r < kWalkCluster; ++r)
+          if (tok < 0 && fs[r] >= 0) {
+            tok = fs[r];
+            flag |= ffl[r];
+          }
         if (tok < 0) flag |= 2;  // (no segment held the threshold: an fp64 rounding gap, flagged)
         bonus = tok < 0 ? 0 : tok;
       }
@@ -1193,8 +1304,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   // dynamic shared memory of the walk: each CTA's slice of p and q (when it fits)
-  const int per_cta = ((vocab + kWalkCluster - 1) / kWalkCluster + 3) & ~3;
-  const size_t walk_smem = per_cta <= kWalkStage ? 2 * sizeof(float) * (size_t)per_cta : 0;
+  const size_t walk_smem = 2 * sizeof(float) * (size_t)walk_stage_floats(vocab);  // (p, then q)
   static PerDevice walk_attr;  // the raised shared-memory limit, set once per device
   if (per_device(walk_attr, [](int) {
         return cudaFuncSetAttribute(accept_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -98,6 +98,22 @@ __device__ __forceinline__ F2 d_to_f2(double x) {
 }
 // a > b for normalised double-float values (|lo| at most half an ulp of hi).
 __device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+// a * b for a double-float a and an fp32 b: the product of the high parts exactly (fma), the
+// low part's product added, renormalised.
+__device__ __forceinline__ F2 f2_mul_f(F2 a, float b) {
+  const float p = a.hi * b;
+  const float e = fmaf(a.lo, b, fmaf(a.hi, b, -p));
+  const float hi = p + e;
+  return F2{hi, e - (hi - p)};
+}
+// 1 / (hi + lo) in fp32: the fp32 reciprocal of hi refined once with the residual of both
+// parts (Newton's step r + r (1 - x r)); 0 for a zero or negative input.
+__device__ __forceinline__ float f2_rcp(F2 x) {
+  if (!(x.hi > 0.f)) return 0.f;
+  const float r = 1.0f / x.hi;
+  const float e = fmaf(-x.hi, r, 1.0f) - x.lo * r;
+  return fmaf(r, e, r);
+}
 
 // Host-side values that belong to one device: a kernel's raised shared-memory limit
 // (cudaFuncSetAttribute applies to the current device only), its occupancy, the SM count.
