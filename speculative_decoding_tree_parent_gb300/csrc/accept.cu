@@ -762,10 +762,21 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
 // gets bitwise the same result.
 __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float invT) {
   const int lane = threadIdx.x & 31;
-  float mp = -INFINITY, mq = -INFINITY;
-  for (int k = lane; k < chunks; k += 32) {
-    mp = fmaxf(mp, __ldcg(&part[k].m_p));
-    mq = fmaxf(mq, __ldcg(&part[k].m_q));
+  // up to 32 chunks (vocabularies to 128K tokens): every field of the lane's chunk loaded at
+  // once and kept, one round trip to L2; more: the sum pass reloads them
+  const bool kept = chunks <= 32;
+  StatPartial mine{-INFINITY, -INFINITY, 0.f, 0.f, 0.f, 0.f};
+  if (kept && lane < chunks) {
+    const StatPartial& sp = part[lane];
+    mine = StatPartial{__ldcg(&sp.m_p), __ldcg(&sp.m_q), __ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo),
+                       __ldcg(&sp.sq_hi), __ldcg(&sp.sq_lo)};
+  }
+  float mp = mine.m_p, mq = mine.m_q;
+  if (!kept) {
+    for (int k = lane; k < chunks; k += 32) {
+      mp = fmaxf(mp, __ldcg(&part[k].m_p));
+      mq = fmaxf(mq, __ldcg(&part[k].m_q));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -773,11 +784,18 @@ __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float 
     mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
   }
   F2 zp{0.f, 0.f}, zq{0.f, 0.f};  // double-float throughout: fp64 is slow on this part
-  for (int k = lane; k < chunks; k += 32) {
-    const StatPartial& sp = part[k];
-    const float m_p = __ldcg(&sp.m_p), m_q = __ldcg(&sp.m_q);
-    if (m_p != -INFINITY) zp = f2_add(zp, f2_mul_f(F2{__ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo)}, expf((m_p - mp) * invT)));
-    if (m_q != -INFINITY) zq = f2_add(zq, f2_mul_f(F2{__ldcg(&sp.sq_hi), __ldcg(&sp.sq_lo)}, expf((m_q - mq) * invT)));
+  auto add = [&](const StatPartial& x) {
+    if (x.m_p != -INFINITY) zp = f2_add(zp, f2_mul_f(F2{x.sp_hi, x.sp_lo}, expf((x.m_p - mp) * invT)));
+    if (x.m_q != -INFINITY) zq = f2_add(zq, f2_mul_f(F2{x.sq_hi, x.sq_lo}, expf((x.m_q - mq) * invT)));
+  };
+  if (kept) {
+    add(mine);
+  } else {
+    for (int k = lane; k < chunks; k += 32) {
+      const StatPartial& sp = part[k];
+      add(StatPartial{__ldcg(&sp.m_p), __ldcg(&sp.m_q), __ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo), __ldcg(&sp.sq_hi),
+                      __ldcg(&sp.sq_lo)});
+    }
   }
   zp = f2_warp_sum(zp);
   zq = f2_warp_sum(zq);
@@ -1144,13 +1162,32 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
         float rs = 0.f, rc = 0.f;
         int lp = -1;  // the run's last token with positive residual
         const int rot = lane % sub;
-        for (int t = 0; t < sub; ++t) {
-          const int i = r_lo + (t + rot < sub ? t + rot : t + rot - sub);
-          const float rv = i < r_hi ? sl.resid(ev, i, cf) : 0.f;
+        auto take = [&](int i, float rv) {  // fp32 Kahan step; the last positive token
           const float y = rv - rc, z = rs + y;
           rc = (z - rs) - y;
           rs = z;
           if (rv > 0.f && i > lp) lp = i;
+        };
+        if (sl.sp != nullptr) {  // staged: padded with zeros, eight tokens in flight (sub % 8 == 0)
+          for (int t0 = 0; t0 < sub; t0 += 8) {
+            float pv[8], qv[8];
+            int ix[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int o = t0 + u + rot;
+              ix[u] = r_lo + (o < sub ? o : o - sub);
+              pv[u] = sl.sp[ix[u]];
+              qv[u] = sl.sq[ix[u]];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) take(ix[u], cf == 0.f ? pv[u] : fmaxf(pv[u] - cf * qv[u], 0.f));
+          }
+        } else {
+          for (int t = 0; t < sub; ++t) {
+            const int o = t + rot;
+            const int i = r_lo + (o < sub ? o : o - sub);
+            take(i, i < r_hi ? sl.resid(ev, i, cf) : 0.f);
+          }
         }
         F2 inc{rs, -rc};  // inclusive scan of the runs' sums over the lanes
 #pragma unroll
@@ -1163,29 +1200,39 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
         const unsigned hit = __ballot_sync(0xffffffffu, r_hi > r_lo && f2_gt(inc, loc));
         int tok = -1, fl = 0;
         if (hit) {
+          // the crossing run, in order, 32 tokens a round: lane j takes the round's j-th token,
+          // an inclusive double-float scan over the lanes, the first lane past the threshold
           const int l = __ffs(hit) - 1;
-          if (lane == l) {
-            F2 cum = exc;
-            for (int i = r_lo; i < r_hi; ++i) {
-              const float rv = sl.resid(ev, i, cf);
-              const F2 nxt = f2_add(cum, F2{rv, 0.f});
-              if (f2_gt(nxt, loc)) {
-                tok = sl.c_lo + i;
-                // distances of the crossing token's two CDF edges from the threshold
-                const F2 da = f2_add(nxt, F2{-loc.hi, -loc.lo});
-                const F2 db = f2_add(cum, F2{-loc.hi, -loc.lo});
-                if (fabsf(da.hi + da.lo) <= band || fabsf(db.hi + db.lo) <= band) fl = 2;
-                break;
-              }
-              cum = nxt;
+          const int c_lo = s_lo + l * sub, c_hi = min(s_hi, c_lo + sub);
+          F2 carry{__shfl_sync(0xffffffffu, exc.hi, l), __shfl_sync(0xffffffffu, exc.lo, l)};
+          for (int i0 = c_lo; i0 < c_hi && tok < 0; i0 += 32) {
+            const int i = i0 + lane;
+            const float rv = i < c_hi ? sl.resid(ev, i, cf) : 0.f;
+            F2 in2{rv, 0.f};
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const F2 y{__shfl_up_sync(0xffffffffu, in2.hi, o), __shfl_up_sync(0xffffffffu, in2.lo, o)};
+              if (lane >= o) in2 = f2_add(y, in2);
             }
-            if (tok < 0) {  // the in-order sum fell short of the run's total: at its last mass
-              tok = sl.c_lo + (lp >= 0 ? lp : r_lo);
-              fl = 2;
+            const F2 cum = f2_add(carry, in2);
+            const unsigned h2 = __ballot_sync(0xffffffffu, i < c_hi && f2_gt(cum, loc));
+            if (h2) {
+              const int j = __ffs(h2) - 1;
+              tok = sl.c_lo + i0 + j;
+              // distances of the crossing token's two CDF edges from the threshold
+              const F2 da = f2_add(cum, F2{-loc.hi, -loc.lo});
+              const F2 db = f2_add(da, F2{-rv, 0.f});
+              const float d_after = __shfl_sync(0xffffffffu, da.hi + da.lo, j);
+              const float d_before = __shfl_sync(0xffffffffu, db.hi + db.lo, j);
+              if (fabsf(d_after) <= band || fabsf(d_before) <= band) fl = 2;
             }
+            carry = F2{__shfl_sync(0xffffffffu, cum.hi, 31), __shfl_sync(0xffffffffu, cum.lo, 31)};
           }
-          tok = __shfl_sync(0xffffffffu, tok, l);
-          fl = __shfl_sync(0xffffffffu, fl, l);
+          if (tok < 0) {  // the in-order sum fell short of the run's total: at its last mass
+            const int lpl = __shfl_sync(0xffffffffu, lp, l);
+            tok = sl.c_lo + (lpl >= 0 ? lpl : c_lo);
+            fl = 2;
+          }
         } else {  // rounding put the crossing just past this segment's last mass
           const int last = __reduce_max_sync(0xffffffffu, (unsigned)(lp + 1)) - 1;
           tok = sl.c_lo + (last >= 0 ? last : s_lo);
