@@ -91,7 +91,10 @@ typedef enum {
   SPEC_ERR_PAGE = -3,        /* device: page table entry outside [0, num_pages)              */
   SPEC_ERR_CAPACITY = -4,    /* device: a sequence needs more nodes/pages/path slots than given */
   SPEC_ERR_WORKSPACE = -5,   /* host: ws_bytes smaller than spec_workspace_size()            */
-  SPEC_ERR_UNSUPPORTED = -6, /* host: dtype / head dim / group size not implemented          */
+  SPEC_ERR_UNSUPPORTED = -6, /* host: dtype / head dim / group size not implemented, or a
+                                batch past a launch's grid: batch x hkv > 65535 for the
+                                attention calls, batch > 65535 for stochastic acceptance
+                                and the draft-tree calls                                      */
   SPEC_ERR_CUDA = -7,        /* host: a CUDA runtime call or kernel launch failed            */
   SPEC_ERR_TIMEOUT = -8,     /* device: a bounded wait inside a kernel gave up               */
   SPEC_ERR_INDEX = -9        /* device: token id / path node id out of range                 */

@@ -46,6 +46,8 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // bf16 inputs with head dim 128 run on the tensor-core kernel and nowhere else; the
 // CUDA-core kernel serves fp32 inputs and head dim 64.
 static bool attn_wants_tc(int dtype, int d) { return dtype == SPEC_BF16 && d == 128; }
+// Grids put (sequence, KV head) pairs, or sequences, on a launch's y or z dimension.
+static bool grid_fits(long n) { return n <= kMaxGridYZ; }
 
 }  // namespace specv
 
@@ -97,6 +99,7 @@ int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, 
     return SPEC_ERR_ARG;
   if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+  if (!grid_fits((long)batch * hkv)) return SPEC_ERR_UNSUPPORTED;
   const bool tc = attn_wants_tc(dtype, d);
   if (tc && !attn_tc_shape(dtype, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   *tensor_cores = tc ? 1 : 0;
@@ -127,6 +130,7 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
   if (d != 64 && d != 128) return SPEC_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size % 8 != 0) return SPEC_ERR_UNSUPPORTED;
+  if (!grid_fits((long)batch * hkv)) return SPEC_ERR_UNSUPPORTED;
   const bool tc = attn_wants_tc(dtype, d);
   if (tc && !attn_tc_shape(dtype, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
@@ -167,6 +171,7 @@ static int check_accept_args(int mode, const int32_t* parent, const int32_t* dra
   if (!parent || !draft_tokens || !target_logits || !qo_indptr || !accept_len || !path || !out_tokens)
     return SPEC_ERR_ARG;
   if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
+  if (mode == SPEC_STOCHASTIC && !grid_fits(batch)) return SPEC_ERR_UNSUPPORTED;  // one cluster row each
   return SPEC_OK;
 }
 
@@ -293,6 +298,7 @@ int spec_tree_verify_attn_kv8(const void* q, const uint8_t* k_pool, const uint8_
     return SPEC_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
   if (!attn_tc_shape(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (!grid_fits((long)batch * hkv)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
   if (!q || !k_tree || !v_tree || !mask || !qo_indptr || !prefix_len || !out || !kv_scale) return SPEC_ERR_ARG;
   if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
@@ -322,6 +328,7 @@ int spec_tree_verify_attn_parents(const void* q, const void* k_pool, const void*
     return SPEC_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SPEC_ERR_ARG;
   if (!attn_tc_shape(SPEC_BF16, hq, hkv, d, page_size, max_nodes)) return SPEC_ERR_UNSUPPORTED;
+  if (!grid_fits((long)batch * hkv)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0 || total_nodes == 0) return SPEC_OK;
   if (!q || !k_tree || !v_tree || !parent || !qo_indptr || !prefix_len || !out) return SPEC_ERR_ARG;
   if (max_prefix > 0 && (!k_pool || !v_pool || !page_table || max_pages <= 0 || num_pages <= 0))
@@ -360,6 +367,7 @@ int spec_tree_init(const int32_t* root_tokens, int batch, int max_nodes, void* s
                    int32_t* parent_out, int32_t* tokens_out, int32_t* n_nodes_out, int32_t* next_node,
                    uint8_t* flags, void* stream) {
   if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes) return SPEC_ERR_ARG;
+  if (!grid_fits(batch)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0) return SPEC_OK;
   if (!root_tokens || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
   if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
@@ -375,6 +383,7 @@ int spec_tree_expand(const float* draft_logits, int vocab, long long row_stride,
   if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes || vocab < 1 || topk < 1 || topk > 16 ||
       max_depth < 1 || row_stride < 0 || node_stride < 0)
     return SPEC_ERR_ARG;
+  if (!grid_fits(batch)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0) return SPEC_OK;
   if (!draft_logits || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node) return SPEC_ERR_ARG;
   if (state_bytes < tree_state_bytes(batch, max_nodes)) return SPEC_ERR_WORKSPACE;
@@ -392,6 +401,7 @@ int spec_tree_expand_multi(const float* draft_logits, int vocab, long long row_s
   if (batch < 0 || max_nodes < 1 || max_nodes > kMaxNodes || vocab < 1 || topk < 1 || topk > 16 ||
       max_depth < 1 || width < 1 || width > kTreeMaxW || row_stride < 0 || req_stride < 0)
     return SPEC_ERR_ARG;
+  if (!grid_fits(batch)) return SPEC_ERR_UNSUPPORTED;
   if (batch == 0) return SPEC_OK;
   if (!draft_logits || !state || !parent_out || !tokens_out || !n_nodes_out || !next_node || !req_parent ||
       !req_token || !req_n)

@@ -13,6 +13,7 @@ namespace specv {
 
 // Most nodes one draft tree may have (every entry point refuses larger max_nodes).
 constexpr int kMaxTreeNodes = 1024;
+constexpr long kMaxGridYZ = 65535;  // a launch's y and z extents
 
 // First-error-wins report into the caller's status word (nullable).
 __device__ __forceinline__ void report(int32_t* status, int code) {

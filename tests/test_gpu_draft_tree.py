@@ -268,3 +268,13 @@ def test_multi_tree_edges():
     assert int(status.item()) == -1
     assert torch.equal(par, before[0]) and torch.equal(tok, before[1]) and int(nn.item()) == before[2]
     assert int(rn.item()) == listed
+
+
+def test_multi_tree_many_sequences():
+    """Twenty sequences at width 8: 1280 CTAs, more than one wave, so a sequence's replaying
+    cluster may start after other sequences' clusters have finished (nothing waits)."""
+    rng = np.random.default_rng(31)
+    roots = rng.integers(0, 4096, 20).astype(np.int32)
+    er = EdgeRows(131, 4096, scale=2.5)
+    tight, ncalls = _compare_multi(er, roots, 32, 4, 6, 8)
+    assert tight <= 2

@@ -126,3 +126,33 @@ def test_bf16_head128_runs_on_tensor_cores_only(lib):
         gpu = False
     if not gpu:   # no driver here: the tensor-map encoder is missing, which is an error
         assert call() == -7
+
+
+def test_batches_past_a_launch_grid_are_refused(lib):
+    """Sizes whose grid would exceed a launch's y / z extent (65535) are refused on the host
+    (SPEC_ERR_UNSUPPORTED) instead of failing at launch: the attention's batch x KV heads, the
+    stochastic acceptance's and the draft tree's sequences. Every call returns at its host
+    check; the pointers are never dereferenced."""
+    fake = ctypes.c_void_p(256)
+    with pytest.raises(binding.SpecError) as ei:
+        binding.spec_attn_plan(binding.SPEC_BF16, 8192, 64, 32, 8, 128, 16, 4096)   # 65536 (sequence, head) pairs
+    assert ei.value.status == -6
+    assert binding.spec_attn_plan(binding.SPEC_BF16, 8191, 64, 32, 8, 128, 16, 4096)[1] == 1
+    common = lambda batch: (fake, fake, fake, 4, 16, fake, 4, fake, 64, fake, fake, fake, fake, batch, batch, 4, 32,
+                            8, 128, 0.0, fake, None, None, 0, None, None)
+    assert lib.spec_tree_verify_attn_parents(*common(8192)) == -6
+    assert lib.spec_tree_verify_attn(binding.SPEC_BF16, *common(8192)) == -6
+    # stochastic acceptance: 65536 sequences; greedy has no such limit (it stops later, here at
+    # the workspace check: 0 bytes given)
+    acc = lambda mode: (mode, fake, fake, fake, fake, fake, ctypes.c_float(1.0), 1000, fake, 65536, 65536, 4, 4,
+                        fake, fake, fake, None, fake, 0, None, None)
+    assert lib.spec_accept(*acc(binding.SPEC_STOCHASTIC)) == -6
+    assert lib.spec_accept(*acc(binding.SPEC_GREEDY)) == -5
+    # draft tree
+    assert lib.spec_tree_init(fake, 65536, 64, fake, 1 << 40, fake, fake, fake, fake, None, None) == -6
+    st = lib.spec_tree_expand(fake, 1000, 1000, 1000, 65536, 64, 4, 4, 0.0, fake, 1 << 40, fake, fake, fake, fake,
+                              None, None, None)
+    assert st == -6
+    st = lib.spec_tree_expand_multi(fake, 1000, 1000, 1000, 65536, 64, 8, 4, 4, 0.0, fake, 1 << 40, fake, fake,
+                                    fake, fake, fake, fake, fake, None, None, None)
+    assert st == -6
