@@ -120,8 +120,13 @@ def work_counts(inp, accept_len=None, mode="greedy"):
                      + inp.total_nodes * inp.mask_words * 8)
     # FP8 cache: one byte per prefix K/V element (the tree K/V, Q and O stay bf16)
     attn_bytes_fp8kv = attn_bytes - int(P.sum() * inp.hkv * inp.d * (esz - 1) * 2)
-    # one pass over every node's logits (target, and draft too for stochastic acceptance)
-    accept_bytes = int(inp.total_nodes * inp.vocab * 4 * (2 if mode == "stochastic" else 1))
+    # greedy: one pass over every node's logits; stochastic: the target and draft rows of the
+    # nodes the walk visits (the root and each accepted node, accept_len + 1 per sequence),
+    # the only rows the method reads (all rows while the accepted lengths are not known yet)
+    if mode == "stochastic" and accept_len is not None:
+        accept_bytes = int((np.asarray(accept_len, np.int64) + 1).sum() * inp.vocab * 4 * 2)
+    else:
+        accept_bytes = int(inp.total_nodes * inp.vocab * 4 * (2 if mode == "stochastic" else 1))
     commit_bytes = 0
     if accept_len is not None:
         commit_bytes = int(((np.asarray(accept_len) + 1) * inp.hkv * inp.d * esz * 2 * 2).sum())

@@ -18,18 +18,17 @@
 //                          last CTA to finish (atomic counter, no waiting) reads every
 //                          row's argmax from the slots and walks every sequence, one
 //                          warp each.
-// Stochastic, two launches:
-//   accept_stats_kernel    grid = chunks x nodes. Per chunk of a row of target and
-//                          draft logits: max and sum of exp((x - max) / T) (fp32
-//                          elements from ex2.approx, Kahan compensated per thread,
-//                          double-float across threads and stored so). The walk
-//                          merges a node's chunk partials when it visits the node.
-//   accept_walk_kernel     one 8-CTA cluster per sequence. The decisions at a node
-//                          need sums over the vocabulary of the residual
-//                          max(p - c q, 0) (see below); each CTA sums its eighth of the
-//                          vocabulary and the eight partials are exchanged through
-//                          distributed shared memory. Every CTA of the cluster takes
-//                          the same decisions from bitwise-identical sums.
+// Stochastic, one launch:
+//   accept_walk_kernel     one 8-CTA cluster per sequence, each CTA on an eighth of the
+//                          vocabulary. At each node the walk visits (the root, then each
+//                          accepted child) it loads the node's target and draft rows, takes
+//                          their max and sum of exp((x - max) / T) (fp32 elements, Kahan per
+//                          thread, double-float across threads, warps and the CTAs of the
+//                          cluster, exchanged through distributed shared memory) and keeps p
+//                          and q of its slice in shared memory; the children's tests and the
+//                          residual passes then read those. Only the visited nodes' rows are
+//                          read: the method needs no other node's distributions. Every CTA of
+//                          the cluster takes the same decisions from bitwise-identical sums.
 //
 // Residual in closed form. Starting from r_1 = p, the update
 // r <- max(r - q, 0) / sum(max(r - q, 0)) keeps r of the form
@@ -60,10 +59,6 @@ struct alignas(8) ArgPartial {
   float v;
   int i;
 };
-struct StatPartial {  // a chunk's max and sum of exp((x - max) / T), the sums as double-float
-  float m_p, m_q;
-  float sp_hi, sp_lo, sq_hi, sq_lo;
-};
 struct NodeStats {  // a row's max and the reciprocal of its softmax normaliser (fp32)
   float m_p, m_q;
   float inv_zp, inv_zq;
@@ -82,21 +77,21 @@ struct AcceptWs {
     size_t off = 0;
     w.counter = off;  off = align_up(off + sizeof(unsigned), 256);
     w.slots = off;    off = align_up(off + sizeof(unsigned long long) * kArgSlots, 256);
-    w.partials = off; off = align_up(off + sizeof(StatPartial) * (size_t)total_nodes * chunks, 256);
-    w.results = off;  off = align_up(off + sizeof(NodeStats) * (size_t)total_nodes, 256);
+    w.partials = off; off = align_up(off + sizeof(ArgPartial) * (size_t)total_nodes * chunks, 256);
+    w.results = off;  off = align_up(off + sizeof(int) * (size_t)total_nodes, 256);
     w.total = off;
     return w;
   }
 };
 
-// One CTA streams kChunk logits of one row: 8 float4 per thread, all loads issued
-// before any is used, so a CTA costs one memory round trip.
-constexpr int kVecPerThread = 8;
-constexpr int kChunk = kAcceptThreads * kVecPerThread * 4;
+constexpr int kGreedyVec = 4;                                  // float4 per thread per task
+constexpr int kGreedyChunk = kAcceptThreads * kGreedyVec * 4;  // 4096 logits
+int greedy_chunks(int vocab) { return ceil_div(vocab, kGreedyChunk); }
 
+// the greedy per-task partials (past kArgSlots rows): one per 4096-logit piece of a row
 int accept_chunks(int total_nodes, int vocab) {
   (void)total_nodes;
-  return ceil_div(vocab, kChunk);
+  return greedy_chunks(vocab);
 }
 
 size_t accept_ws_bytes(int batch, int total_nodes, int vocab) {
@@ -129,12 +124,6 @@ __device__ __forceinline__ void warp_arg_reduce(float& v, int& i) {
     const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
     arg_better(v, i, v2, i2);
   }
-}
-
-// Chunk range [lo, hi) of chunk c (lo a multiple of 4).
-__device__ __forceinline__ void chunk_range(int vocab, int c, int& lo, int& hi) {
-  lo = c * kChunk;
-  hi = lo + kChunk < vocab ? lo + kChunk : vocab;
 }
 
 // Greedy walk of one sequence by one warp: from the root, move to the first child
@@ -195,13 +184,10 @@ __device__ void greedy_walk_warp(int b, int n, const int* parent, const int* tok
 // order-preserving key; beyond kArgSlots rows it leaves a partial instead). The last CTA
 // to finish (one counter, no waiting) reads every row's argmax (or merges the partials)
 // and walks every sequence, one warp per sequence, on the tree staged in shared memory.
-constexpr int kGreedyVec = 4;                                  // float4 per thread per task
-constexpr int kGreedyChunk = kAcceptThreads * kGreedyVec * 4;  // 4096 logits
-constexpr int kGreedyStage = 2048;                             // nodes the final CTA stages
+constexpr int kGreedyStage = 2048;  // nodes the final CTA stages
 constexpr int kCommitCta = 4;          // fused commit: up to this many sequences, one at a time by the CTA
 constexpr int kCommitPathStage = 128;  // path rows up to this long kept in shared memory for it
 
-int greedy_chunks(int vocab) { return ceil_div(vocab, kGreedyChunk); }
 
 // The same walk on a tree staged in shared memory, in two steps: every node c > 0 whose
 // draft token equals its parent's argmax offers itself to the parent (atomicMin keeps the
@@ -619,189 +605,6 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
   }
 }
 
-// ---------------------------------------------------------------- stochastic: statistics
-
-// 2^x by the hardware approximation (used on the statistics pass, where every value of a
-// chunk is exponentiated once)
-__device__ __forceinline__ float ex2a(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Online max / compensated sum of exp((x - m) * invT) over a stream of values.
-struct OnlineExp {
-  float m = -INFINITY, s = 0.f, comp = 0.f;
-  __device__ __forceinline__ void add(float x, float invT) {
-    if (x > m) {
-      const float f = (m == -INFINITY) ? 0.f : expf((m - x) * invT);
-      s *= f;
-      comp *= f;
-      m = x;
-      kahan(1.f);
-    } else {
-      kahan(expf((x - m) * invT));
-    }
-  }
-  __device__ __forceinline__ void kahan(float e) {
-    const float y = e - comp;
-    const float t = s + y;
-    comp = (t - s) - y;
-    s = t;
-  }
-};
-
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float r = red[0];
-  for (int w = 1; w < nw; ++w) r = fmaxf(r, red[w]);
-  return r;
-}
-
-template <bool kVec>
-__global__ void __launch_bounds__(kAcceptThreads) accept_stats_kernel(
-    const float* __restrict__ tl, const float* __restrict__ dl, int vocab, int chunks, float invT,
-    StatPartial* partials) {
-  const int t = blockIdx.x / chunks;
-  const int c = blockIdx.x - t * chunks;
-  int lo, hi;
-
-  chunk_range(vocab, c, lo, hi);
-  OnlineExp ep, eq;
-  const float* rp = tl + (size_t)t * vocab;
-  const float* rq = dl + (size_t)t * vocab;
-  if (kVec) {
-    const float4* p4 = reinterpret_cast<const float4*>(rp);
-    const float4* q4 = reinterpret_cast<const float4*>(rq);
-    const int q0 = lo >> 2, q1 = hi >> 2;
-    float4 a[kVecPerThread], d[kVecPerThread];
-    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int j = q0 + threadIdx.x + u * kAcceptThreads;
-      a[u] = j < q1 ? __ldcs(p4 + j) : none;
-      d[u] = j < q1 ? __ldcs(q4 + j) : none;
-    }
-    // every value is in registers: the max first, then one exponential per value (no
-    // running rescale, no divergent branch); values outside the chunk are -inf and add 0
-    float mp = -INFINITY, mq = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      mp = fmaxf(mp, fmaxf(fmaxf(a[u].x, a[u].y), fmaxf(a[u].z, a[u].w)));
-      mq = fmaxf(mq, fmaxf(fmaxf(d[u].x, d[u].y), fmaxf(d[u].z, d[u].w)));
-    }
-    // one ex2.approx per value of (x - m) / T in log2 units: x - m first, so the terms near
-    // the max keep their exponent exactly; a term's relative error is then that of
-    // ex2.approx (a few parts in 10^7), and the sums stay compensated
-    const float k2 = invT * 1.4426950408889634f;  // log2(e) / T
-    if (mp != -INFINITY) {
-      ep.m = mp;
-#pragma unroll
-      for (int u = 0; u < kVecPerThread; ++u) {
-        ep.kahan(ex2a((a[u].x - mp) * k2));
-        ep.kahan(ex2a((a[u].y - mp) * k2));
-        ep.kahan(ex2a((a[u].z - mp) * k2));
-        ep.kahan(ex2a((a[u].w - mp) * k2));
-      }
-    }
-    if (mq != -INFINITY) {
-      eq.m = mq;
-#pragma unroll
-      for (int u = 0; u < kVecPerThread; ++u) {
-        eq.kahan(ex2a((d[u].x - mq) * k2));
-        eq.kahan(ex2a((d[u].y - mq) * k2));
-        eq.kahan(ex2a((d[u].z - mq) * k2));
-        eq.kahan(ex2a((d[u].w - mq) * k2));
-      }
-    }
-  } else {
-    for (int e = lo + threadIdx.x; e < hi; e += kAcceptThreads) {
-      ep.add(__ldcs(rp + e), invT);
-      eq.add(__ldcs(rq + e), invT);
-    }
-  }
-  __shared__ float redf[kAcceptThreads / 32];
-  __shared__ float red_hi[2][kAcceptThreads / 32], red_lo[2][kAcceptThreads / 32];
-  const float Mp = block_max(ep.m, redf);
-  const float Mq = block_max(eq.m, redf);
-  // each thread's compensated sum rescaled to the block max as a double-float, then summed
-  // across the block in double-float
-  auto rescaled = [&](const OnlineExp& e, float M) {
-    if (e.m == -INFINITY) return F2{0.f, 0.f};
-    const float f = expf((e.m - M) * invT);
-    const float hi = e.s * f;
-    return F2{hi, fmaf(e.s, f, -hi) - e.comp * f};
-  };
-  const F2 sp = f2_warp_sum(rescaled(ep, Mp)), sq = f2_warp_sum(rescaled(eq, Mq));
-  const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
-    red_hi[0][warp] = sp.hi;
-    red_lo[0][warp] = sp.lo;
-    red_hi[1][warp] = sq.hi;
-    red_lo[1][warp] = sq.lo;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    F2 tp{0.f, 0.f}, tq{0.f, 0.f};
-    for (int w = 0; w < kAcceptThreads / 32; ++w) {
-      tp = f2_add(tp, F2{red_hi[0][w], red_lo[0][w]});
-      tq = f2_add(tq, F2{red_hi[1][w], red_lo[1][w]});
-    }
-    partials[(size_t)t * chunks + c] = StatPartial{Mp, Mq, tp.hi, tp.lo, tq.hi, tq.lo};
-    pdl_trigger();
-  }
-}
-
-// Statistics of one row from its chunk partials, by one warp: lane k takes chunks k,
-// k + 32, ... in order, then a fixed xor tree. Every CTA that calls it for the same row
-// gets bitwise the same result.
-__device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float invT) {
-  const int lane = threadIdx.x & 31;
-  // up to 32 chunks (vocabularies to 128K tokens): every field of the lane's chunk loaded at
-  // once and kept, one round trip to L2; more: the sum pass reloads them
-  const bool kept = chunks <= 32;
-  StatPartial mine{-INFINITY, -INFINITY, 0.f, 0.f, 0.f, 0.f};
-  if (kept && lane < chunks) {
-    const StatPartial& sp = part[lane];
-    mine = StatPartial{__ldcg(&sp.m_p), __ldcg(&sp.m_q), __ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo),
-                       __ldcg(&sp.sq_hi), __ldcg(&sp.sq_lo)};
-  }
-  float mp = mine.m_p, mq = mine.m_q;
-  if (!kept) {
-    for (int k = lane; k < chunks; k += 32) {
-      mp = fmaxf(mp, __ldcg(&part[k].m_p));
-      mq = fmaxf(mq, __ldcg(&part[k].m_q));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-    mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
-  }
-  F2 zp{0.f, 0.f}, zq{0.f, 0.f};  // double-float throughout: fp64 is slow on this part
-  auto add = [&](const StatPartial& x) {
-    if (x.m_p != -INFINITY) zp = f2_add(zp, f2_mul_f(F2{x.sp_hi, x.sp_lo}, expf((x.m_p - mp) * invT)));
-    if (x.m_q != -INFINITY) zq = f2_add(zq, f2_mul_f(F2{x.sq_hi, x.sq_lo}, expf((x.m_q - mq) * invT)));
-  };
-  if (kept) {
-    add(mine);
-  } else {
-    for (int k = lane; k < chunks; k += 32) {
-      const StatPartial& sp = part[k];
-      add(StatPartial{__ldcg(&sp.m_p), __ldcg(&sp.m_q), __ldcg(&sp.sp_hi), __ldcg(&sp.sp_lo), __ldcg(&sp.sq_hi),
-                      __ldcg(&sp.sq_lo)});
-    }
-  }
-  zp = f2_warp_sum(zp);
-  zq = f2_warp_sum(zq);
-  return NodeStats{mp, mq, f2_rcp(zp), f2_rcp(zq)};
-}
-
 // ---------------------------------------------------------------- stochastic: walk
 
 // The CTA's slice [c_lo, c_hi) of the vocabulary (a multiple of 4 tokens long, so rows
@@ -819,10 +622,14 @@ __device__ NodeStats merge_row_stats(const StatPartial* part, int chunks, float 
 constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kWalkKids = 32;  // children listed per batch
 static_assert(kMaxTreeNodes == 32 * 32, "the children bitmap is one word per lane of a warp");
+static_assert((kWalkWarps * 256) % (8 * kWalkThreads) == 0, "a staged slice is whole steps of eight");
 constexpr int kWalkStage = 24576;
 
 struct WalkShared {
-  NodeStats st;                       // statistics of the node being visited
+  float row_max[2];                   // this CTA's max of the visited row (target, draft)
+  float row_sum[4];                   // this CTA's sums of exp((x - max) / T) (hi, lo; target, draft)
+  float red[2][kWalkWarps];           // per-warp maxima
+  float red_hi[2][kWalkWarps], red_lo[2][kWalkWarps];  // per-warp sums
   float part_hi[kWalkWarps], part_lo[kWalkWarps];  // this pass's segment sums (double-float)
   float pre_hi[kWalkWarps], pre_lo[kWalkWarps];    // their exclusive prefix (bonus draw)
   float cta_hi[2], cta_lo[2];         // this CTA's pass total (double-buffered by pass parity)
@@ -885,45 +692,165 @@ __device__ __forceinline__ WalkSlice walk_slice(int vocab, int rank, float* smem
   return s;
 }
 
-// p and q of the slice into shared memory (coalesced; float4 when the rows allow it).
-__device__ void walk_stage(const WalkSlice& sl, const RowEval& ev, bool vec) {
-  if (vec) {
-    const float4* t4 = reinterpret_cast<const float4*>(ev.tl + sl.c_lo);
-    const float4* d4 = reinterpret_cast<const float4*>(ev.dl + sl.c_lo);
+// The visited row's statistics, by the cluster (every CTA gets the same bits): the max of the
+// target and of the draft logits, then their sums of exp((x - max) / T), each CTA over its
+// slice, exchanged through distributed shared memory. When the slice is staged, its logits go
+// into the staging arrays once (-inf past the slice, so no test is needed in the loops), the
+// sum pass leaves exp((x - max) / T) there and the last pass scales it into p and q (the
+// padding then holds 0). The tests' p(x) = RowEval::p gives the same bits.
+__device__ NodeStats walk_row_stats(cg::cluster_group& cl, WalkShared& sh, const WalkSlice& sl, const float* trow,
+                                    const float* drow, float invT, bool vec) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pad = kWalkWarps * sl.seg;
+  float mp = -INFINITY, mq = -INFINITY;
+  if (sl.sp != nullptr) {
+    const int n4 = sl.n >> 2, pad4 = pad >> 2;
+    const float4 neg = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4* p4 = reinterpret_cast<float4*>(sl.sp);
     float4* q4 = reinterpret_cast<float4*>(sl.sq);
-    const int n4 = sl.n >> 2;  // (n is a multiple of 4 when the vocabulary is)
-    constexpr int kU = 4;
-    for (int i0 = threadIdx.x; i0 < n4; i0 += kU * kWalkThreads) {
-      float4 a[kU], d[kU];
+    if (vec && n4 > 0) {  // (n is a multiple of 4 when the vocabulary is)
+      const float4* t4 = reinterpret_cast<const float4*>(trow + sl.c_lo);
+      const float4* d4 = reinterpret_cast<const float4*>(drow + sl.c_lo);
+      for (int i0 = threadIdx.x; i0 < pad4; i0 += 8 * kWalkThreads) {
+        float4 a[8], d[8];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kWalkThreads;
-        if (i < n4) {
-          a[u] = __ldg(t4 + i);
-          d[u] = __ldg(d4 + i);
+        for (int u = 0; u < 8; ++u) {  // every load issued (clamped into the slice), then used
+          const int i = i0 + u * kWalkThreads;
+          const int ic = i < n4 ? i : n4 - 1;
+          a[u] = __ldg(t4 + ic);
+          d[u] = __ldg(d4 + ic);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kWalkThreads;
+          if (i < pad4) {
+            const float4 x = i < n4 ? a[u] : neg, y = i < n4 ? d[u] : neg;
+            p4[i] = x;
+            q4[i] = y;
+            mp = fmaxf(mp, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+            mq = fmaxf(mq, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+          }
         }
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kWalkThreads;
-        if (i < n4) {
-          p4[i] = make_float4(ev.pv(a[u].x), ev.pv(a[u].y), ev.pv(a[u].z), ev.pv(a[u].w));
-          q4[i] = make_float4(ev.qv(d[u].x), ev.qv(d[u].y), ev.qv(d[u].z), ev.qv(d[u].w));
-        }
+    } else {
+      for (int i = threadIdx.x; i < pad; i += kWalkThreads) {
+        const float x = i < sl.n ? __ldg(trow + sl.c_lo + i) : -INFINITY;
+        const float y = i < sl.n ? __ldg(drow + sl.c_lo + i) : -INFINITY;
+        sl.sp[i] = x;
+        sl.sq[i] = y;
+        mp = fmaxf(mp, x);
+        mq = fmaxf(mq, y);
       }
     }
   } else {
     for (int i = threadIdx.x; i < sl.n; i += kWalkThreads) {
-      sl.sp[i] = ev.p(sl.c_lo + i);
-      sl.sq[i] = ev.q(sl.c_lo + i);
+      mp = fmaxf(mp, __ldg(trow + sl.c_lo + i));
+      mq = fmaxf(mq, __ldg(drow + sl.c_lo + i));
     }
   }
-  for (int i = sl.n + threadIdx.x; i < kWalkWarps * sl.seg; i += kWalkThreads) {  // padding
-    sl.sp[i] = 0.f;
-    sl.sq[i] = 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+    mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+  }
+  if (lane == 0) {
+    sh.red[0][warp] = mp;
+    sh.red[1][warp] = mq;
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = sh.red[0][0], d = sh.red[1][0];
+    for (int w = 1; w < kWalkWarps; ++w) {
+      a = fmaxf(a, sh.red[0][w]);
+      d = fmaxf(d, sh.red[1][w]);
+    }
+    sh.row_max[0] = a;
+    sh.row_max[1] = d;
+  }
+  cl.sync();  // every CTA's max is in place
+  float xm[kWalkCluster], ym[kWalkCluster];
+#pragma unroll
+  for (int r = 0; r < kWalkCluster; ++r) {
+    xm[r] = *cl.map_shared_rank(&sh.row_max[0], r);
+    ym[r] = *cl.map_shared_rank(&sh.row_max[1], r);
+  }
+  float Mp = xm[0], Mq = ym[0];
+#pragma unroll
+  for (int r = 1; r < kWalkCluster; ++r) {
+    Mp = fmaxf(Mp, xm[r]);
+    Mq = fmaxf(Mq, ym[r]);
+  }
+  // sums of exp((x - M) / T): Kahan per thread, double-float across threads, warps and CTAs
+  float sp = 0.f, cp = 0.f, sq = 0.f, cq = 0.f;
+  auto kahan = [](float e, float& sum, float& comp) {
+    const float y = e - comp, z = sum + y;
+    comp = (z - sum) - y;
+    sum = z;
+  };
+  const bool okp = Mp != -INFINITY, okq = Mq != -INFINITY;  // (a row of -inf has no mass)
+  if (sl.sp != nullptr) {  // (pad is a multiple of 8 x kWalkThreads: no bounds test)
+    for (int i0 = threadIdx.x; i0 < pad; i0 += 8 * kWalkThreads) {
+      float x[8], y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        x[u] = sl.sp[i0 + u * kWalkThreads];
+        y[u] = sl.sq[i0 + u * kWalkThreads];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float ep = okp ? expf((x[u] - Mp) * invT) : 0.f, eq = okq ? expf((y[u] - Mq) * invT) : 0.f;
+        sl.sp[i0 + u * kWalkThreads] = ep;
+        sl.sq[i0 + u * kWalkThreads] = eq;
+        kahan(ep, sp, cp);
+        kahan(eq, sq, cq);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < sl.n; i += kWalkThreads) {
+      if (okp) kahan(expf((__ldg(trow + sl.c_lo + i) - Mp) * invT), sp, cp);
+      if (okq) kahan(expf((__ldg(drow + sl.c_lo + i) - Mq) * invT), sq, cq);
+    }
+  }
+  const F2 wp = f2_warp_sum(F2{sp, -cp}), wq = f2_warp_sum(F2{sq, -cq});
+  if (lane == 0) {
+    sh.red_hi[0][warp] = wp.hi;
+    sh.red_lo[0][warp] = wp.lo;
+    sh.red_hi[1][warp] = wq.hi;
+    sh.red_lo[1][warp] = wq.lo;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    F2 tp{0.f, 0.f}, tq{0.f, 0.f};
+    for (int w = 0; w < kWalkWarps; ++w) {
+      tp = f2_add(tp, F2{sh.red_hi[0][w], sh.red_lo[0][w]});
+      tq = f2_add(tq, F2{sh.red_hi[1][w], sh.red_lo[1][w]});
+    }
+    sh.row_sum[0] = tp.hi;
+    sh.row_sum[1] = tp.lo;
+    sh.row_sum[2] = tq.hi;
+    sh.row_sum[3] = tq.lo;
+  }
+  cl.sync();  // every CTA's sums are in place
+  float zs[4][kWalkCluster];
+#pragma unroll
+  for (int r = 0; r < kWalkCluster; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) zs[k][r] = *cl.map_shared_rank(&sh.row_sum[k], r);
+  F2 Zp{0.f, 0.f}, Zq{0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < kWalkCluster; ++r) {
+    Zp = f2_add(Zp, F2{zs[0][r], zs[1][r]});
+    Zq = f2_add(Zq, F2{zs[2][r], zs[3][r]});
+  }
+  const NodeStats st{Mp, Mq, f2_rcp(Zp), f2_rcp(Zq)};
+  if (sl.sp != nullptr) {  // exp((x - M) / T) into p and q
+    for (int i = threadIdx.x; i < pad; i += kWalkThreads) {
+      sl.sp[i] *= st.inv_zp;
+      sl.sq[i] *= st.inv_zq;
+    }
+  }
+  __syncthreads();
+  return st;
 }
 
 // One pass: sum over the whole vocabulary (all CTAs of the cluster) of the residual with
@@ -995,13 +922,13 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     accept_walk_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
                        const float* __restrict__ tl, const float* __restrict__ dl,
                        const float* __restrict__ uniforms, float temperature, int vocab,
-                       const int32_t* __restrict__ qo, int path_cap, const StatPartial* partials,
-                       int chunks, int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+                       const int32_t* __restrict__ qo, int path_cap, int32_t* accept_len, int32_t* path,
+                       int32_t* out_tokens, uint8_t* flags,
                        int32_t* status, bool vec) {
   cg::cluster_group cl = cg::this_cluster();
   __shared__ WalkShared sh;
   extern __shared__ __align__(16) float walk_smem[];
-  pdl_wait();  // the statistics kernel's results
+  pdl_wait();  // stream order: the inputs may come from the kernel before
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1020,24 +947,16 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
   int v = 0, L = 0, flag = 0, bonus = 0;
   int parity = 0;
   while (true) {
-    if (threadIdx.x < 32) {  // v's statistics from its chunk partials (the load overlaps the bitmap)
-      const NodeStats m = merge_row_stats(partials + (size_t)(base + v) * chunks, chunks, invT);
-      if (threadIdx.x == 0) sh.st = m;
-    }
-    // children bitmap of v
+    // children bitmap of v (its loads in flight with the row's), then v's row statistics and,
+    // when staged, p and q of the slice
     for (int w = threadIdx.x; w < kMaxTreeNodes / 32; w += blockDim.x) sh.kids[w] = 0u;
     __syncthreads();
-    const NodeStats st = sh.st;
-    const RowEval ev{tl + (size_t)(base + v) * vocab, dl + (size_t)(base + v) * vocab, st.m_p, st.m_q, invT,
-                     st.inv_zp, st.inv_zq};
-    bool staged = false;  // p and q of v's slice in shared memory (done before v's first pass)
-    auto stage = [&]() {
-      if (!staged && sl.sp != nullptr) walk_stage(sl, ev, vec);
-      staged = true;
-    };
     for (int c = v + 1 + threadIdx.x; c < n; c += blockDim.x)
       if (__ldg(parent + base + c) == v) atomicOr(&sh.kids[c >> 5], 1u << (c & 31));
-    __syncthreads();
+    const float* trow_v = tl + (size_t)(base + v) * vocab;
+    const float* drow_v = dl + (size_t)(base + v) * vocab;
+    const NodeStats st = walk_row_stats(cl, sh, sl, trow_v, drow_v, invT, vec);  // (syncs the CTA)
+    const RowEval ev{trow_v, drow_v, st.m_p, st.m_q, invT, st.inv_zp, st.inv_zq};
     F2 cc{0.f, 0.f}, ss{1.f, 0.f};  // residual r = max(p - cc q, 0) / ss (double-float)
     int accepted = -1;
     int next_c = v + 1;  // children with ids >= next_c are not listed yet
@@ -1104,7 +1023,6 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
           accepted = c;
           break;
         }
-        stage();
         const F2 cn = f2_add(cc, ss);
         const F2 sn = walk_pass(cl, sh, sl, ev, cn.hi + cn.lo, parity, false, nullptr);
         parity ^= 1;
@@ -1135,7 +1053,6 @@ __global__ void __cluster_dims__(kWalkCluster, 1, 1) __launch_bounds__(kWalkThre
     // token whose cumulative residual exceeds u * total. The segment sums locate the
     // segment holding the threshold; its warp scans it 32 tokens at a time.
     {
-      stage();
       const float cf = cc.hi + cc.lo;
       F2 cta_pre{0.f, 0.f};
       const F2 total2 = walk_pass(cl, sh, sl, ev, cf, parity, true, &cta_pre);
@@ -1307,10 +1224,8 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   unsigned* counter = reinterpret_cast<unsigned*>(wb + w.counter);
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
                    (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
-  const dim3 grid((unsigned)(total_nodes * chunks));
   if (mode == SPEC_GREEDY) {
-    // the greedy partials (8 bytes per 4096-logit task) fit where the stochastic ones
-    // (24 bytes per 8192-logit chunk) go
+    // the partials (8 bytes per 4096-logit task) when the rows pass the slots
     ArgPartial* part = reinterpret_cast<ArgPartial*>(wb + w.partials);
     int* am = reinterpret_cast<int*>(wb + w.results);
     const int gch = greedy_chunks(vocab);
@@ -1343,13 +1258,6 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
       return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
-  StatPartial* part = reinterpret_cast<StatPartial*>(wb + w.partials);
-  const float invT = 1.0f / temperature;
-  if (vec)
-    accept_stats_kernel<true><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
-  else
-    accept_stats_kernel<false><<<grid, kAcceptThreads, 0, stream>>>(tl, dl, vocab, chunks, invT, part);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   // dynamic shared memory of the walk: each CTA's slice of p and q (when it fits)
   const size_t walk_smem = 2 * sizeof(float) * (size_t)walk_stage_floats(vocab);  // (p, then q)
   static PerDevice walk_attr;  // the raised shared-memory limit, set once per device
@@ -1361,8 +1269,8 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
       }) == 0)
     return SPEC_ERR_CUDA;
   if (launch_pdl(accept_walk_kernel, dim3(kWalkCluster, batch), dim3(kWalkThreads), walk_smem, stream, parent,
-                 tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, (const StatPartial*)part, chunks,
-                 accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
+                 tokens, tl, dl, uniforms, temperature, vocab, qo, path_cap, accept_len, path, out_tokens, flags,
+                 status, vec) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (ca.k_tree == nullptr) return SPEC_OK;
