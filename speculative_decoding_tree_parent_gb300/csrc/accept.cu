@@ -605,6 +605,146 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
   }
 }
 
+// ---------------------------------------------------------------- greedy: walk from the root
+// Greedy acceptance needs the target argmax of the nodes the walk visits only: the root, then
+// each accepted child. For many sequences of many nodes, reading just those rows beats
+// streaming every row: one 8-CTA cluster per sequence walks from the root, each CTA takes the
+// argmax of its eighth of the visited row (eight float4 loads in flight per thread), the eight
+// (max, index) pairs meet through distributed shared memory, and every CTA finds the same
+// child (the lowest id whose token is the argmax) in the sequence's staged tree. The outputs
+// are the stream kernel's bit for bit (the same (value, lower index) order). The commit, when
+// asked for, is the commit kernel's, launched after.
+constexpr int kLazyCluster = 8;
+constexpr int kLazyThreads = 512;
+
+__global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThreads, 2)
+    accept_greedy_lazy_kernel(const float* __restrict__ logits, int vocab, const int32_t* __restrict__ qo,
+                              const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens, int path_cap,
+                              int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
+                              int32_t* status, bool vec) {
+  cg::cluster_group cl = cg::this_cluster();
+  constexpr int kWarps = kLazyThreads / 32;
+  __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes];
+  __shared__ float s_wv[kWarps];
+  __shared__ int s_wi[kWarps];
+  __shared__ float s_bv[2];  // this CTA's (max, index) of the step, by step parity
+  __shared__ int s_bi[2];
+  __shared__ int s_child;
+  pdl_wait();  // stream order: the inputs may come from the kernel before
+  const int b = blockIdx.y;
+  const int rank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int base = __ldg(qo + b);
+  const int n = min(__ldg(qo + b + 1) - base, kMaxTreeNodes);
+  int32_t* prow = path + (size_t)b * path_cap;
+  int32_t* trow = out_tokens + (size_t)b * path_cap;
+  const bool writer = rank == 0 && threadIdx.x == 0;
+  if (n < 1) {  // the same in every CTA of the cluster: all leave here
+    if (writer) report(status, SPEC_ERR_CAPACITY);
+    return;
+  }
+  for (int c = threadIdx.x; c < n; c += kLazyThreads) {
+    s_par[c] = __ldg(parent + base + c);
+    s_tok[c] = __ldg(tokens + base + c);
+  }
+  const int per = ((vocab + kLazyCluster - 1) / kLazyCluster + 3) & ~3;
+  const int c_lo = rank * per;
+  const int n_sl = max(0, min(vocab, c_lo + per) - c_lo);
+  int v = 0, L = 0, bonus = 0, parity = 0;
+  if (writer) prow[0] = 0;
+  __syncthreads();
+  while (true) {
+    const float* row = logits + (size_t)(base + v) * vocab + c_lo;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (vec) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const int n4 = n_sl >> 2;  // (n_sl is a multiple of 4 when the vocabulary is)
+      for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * kLazyThreads) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // every load issued (clamped into the slice), then used
+          const int i = i0 + u * kLazyThreads;
+          x[u] = __ldcs(r4 + (i < n4 ? i : n4 - 1));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kLazyThreads;
+          if (i < n4) {
+            const int e = c_lo + 4 * i;
+            arg_better(bv, bi, x[u].x, e);
+            arg_better(bv, bi, x[u].y, e + 1);
+            arg_better(bv, bi, x[u].z, e + 2);
+            arg_better(bv, bi, x[u].w, e + 3);
+          }
+        }
+      }
+    } else {
+      for (int i = threadIdx.x; i < n_sl; i += kLazyThreads) arg_better(bv, bi, __ldcs(row + i), c_lo + i);
+    }
+    warp_arg_reduce(bv, bi);
+    if (lane == 0) {
+      s_wv[warp] = bv;
+      s_wi[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kWarps; ++w) arg_better(bv, bi, s_wv[w], s_wi[w]);
+      s_bv[parity] = bv;
+      s_bi[parity] = bi;
+      s_child = INT_MAX;
+    }
+    cl.sync();  // every CTA's (max, index) is in place
+    float ov[kLazyCluster];
+    int oi[kLazyCluster];
+#pragma unroll
+    for (int r = 0; r < kLazyCluster; ++r) {  // all sixteen loads first
+      ov[r] = *cl.map_shared_rank(&s_bv[parity], r);
+      oi[r] = *cl.map_shared_rank(&s_bi[parity], r);
+    }
+    float av = ov[0];
+    int ai = oi[0];
+#pragma unroll
+    for (int r = 1; r < kLazyCluster; ++r) arg_better(av, ai, ov[r], oi[r]);
+    const int a = ai == INT_MAX ? 0 : ai;  // (an empty or all-NaN row: token 0, as the stream kernel)
+    // the child of v whose token is a, lowest id first
+    int mine = INT_MAX;
+    for (int c = v + 1 + threadIdx.x; c < n; c += kLazyThreads)
+      if (s_par[c] == v && s_tok[c] == a && c < mine) mine = c;
+    mine = (int)__reduce_min_sync(0xffffffffu, (unsigned)mine);
+    if (lane == 0 && mine != INT_MAX) atomicMin(&s_child, mine);
+    __syncthreads();
+    const int c = s_child;
+    if (c == INT_MAX) {
+      bonus = a;
+      break;
+    }
+    if (L + 1 >= path_cap) {  // accepted path does not fit: truncate here
+      if (writer) report(status, SPEC_ERR_CAPACITY);
+      bonus = a;
+      break;
+    }
+    ++L;
+    if (writer) {
+      prow[L] = c;
+      trow[L - 1] = s_tok[c];
+    }
+    v = c;
+    parity ^= 1;
+  }
+  if (writer) {
+    trow[L] = bonus;
+    accept_len[b] = L;
+    if (flags != nullptr) flags[b] = 0;
+  }
+  if (rank == 0)
+    for (int k = L + 1 + threadIdx.x; k < path_cap; k += kLazyThreads) {
+      prow[k] = -1;
+      trow[k] = -1;
+    }
+  cl.sync();  // no CTA leaves while another may still read its shared memory
+}
+
 // ---------------------------------------------------------------- stochastic: walk
 
 // The CTA's slice [c_lo, c_hi) of the vocabulary (a multiple of 4 tokens long, so rows
@@ -1224,6 +1364,33 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   unsigned* counter = reinterpret_cast<unsigned*>(wb + w.counter);
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
                    (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
+  if (mode == SPEC_GREEDY && vec && batch <= kMaxGridYZ) {
+    // The walk from the root reads at most path_cap rows per sequence, one after another; the
+    // stream reads every row at the copy rate. A model of both (per-step latency of a cluster
+    // reading an eighth of a row; ~6 TB/s and a ~3.5 us tail for the stream) picks the walk
+    // only where it is clearly cheaper: many rows per sequence, several sequences.
+    static PerDevice sm_walk;
+    const int sms = per_device(sm_walk, [](int dev) {
+      int v = 0;
+      return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
+    });
+    if (sms == 0) return SPEC_ERR_CUDA;
+    const double stream_us = (double)total_nodes * vocab * 4.0 / 6.0e6 + 3.5;
+    const long clusters = (sms * 2L) / kLazyCluster > 0 ? (sms * 2L) / kLazyCluster : 1;
+    const long waves = (batch + clusters - 1) / clusters;
+    const double step_us = 1.5 + (double)vocab * 4.0 / kLazyCluster / 50.0e3;
+    const double walk_us = (double)waves * path_cap * step_us;
+    if (walk_us < stream_us) {
+      if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
+                     qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+      if (ca.k_tree == nullptr) return SPEC_OK;
+      return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
+                              ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
+                              ca.v_pool, batch, ca.hkv, ca.d, status, stream, ca.ins);
+    }
+  }
   if (mode == SPEC_GREEDY) {
     // the partials (8 bytes per 4096-logit task) when the rows pass the slots
     ArgPartial* part = reinterpret_cast<ArgPartial*>(wb + w.partials);
