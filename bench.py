@@ -96,6 +96,12 @@ def job_throughput(tokens_all_ranks, max_rank_ms):
 
 # ----------------------------------------------------------------------------- work counts
 
+def _sm_count():
+    """The current GPU's SM count (152 on a GB300), for the acceptance read plan."""
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+
+
 def work_counts(inp, accept_len=None, mode="greedy"):
     """Algorithmic FLOPs and bytes of one step's kernels (per launch)."""
     import numpy as np
@@ -120,13 +126,20 @@ def work_counts(inp, accept_len=None, mode="greedy"):
                      + inp.total_nodes * inp.mask_words * 8)
     # FP8 cache: one byte per prefix K/V element (the tree K/V, Q and O stay bf16)
     attn_bytes_fp8kv = attn_bytes - int(P.sum() * inp.hkv * inp.d * (esz - 1) * 2)
-    # greedy: one pass over every node's logits; stochastic: the target and draft rows of the
-    # nodes the walk visits (the root and each accepted node, accept_len + 1 per sequence),
-    # the only rows the method reads (all rows while the accepted lengths are not known yet)
-    if mode == "stochastic" and accept_len is not None:
-        accept_bytes = int((np.asarray(accept_len, np.int64) + 1).sum() * inp.vocab * 4 * 2)
+    # the logits rows the acceptance reads: every node's (greedy, when it streams), or only the
+    # rows of the nodes the walk visits (the root and each accepted node, accept_len + 1 per
+    # sequence: stochastic always, greedy when spec_accept_plan says so) -- target rows, and
+    # draft rows too for stochastic acceptance (all rows while the accepted lengths are unknown)
+    rows_per_node = 2 if mode == "stochastic" else 1
+    walk = 1
+    if mode != "stochastic":
+        from speculative_decoding_tree_parent_gb300 import binding as _B
+        walk = _B.spec_accept_plan(_B.SPEC_GREEDY, inp.batch, inp.total_nodes, inp.vocab, inp.path_cap,
+                                   _sm_count())
+    if walk and accept_len is not None:
+        accept_bytes = int((np.asarray(accept_len, np.int64) + 1).sum() * inp.vocab * 4 * rows_per_node)
     else:
-        accept_bytes = int(inp.total_nodes * inp.vocab * 4 * (2 if mode == "stochastic" else 1))
+        accept_bytes = int(inp.total_nodes * inp.vocab * 4 * rows_per_node)
     commit_bytes = 0
     if accept_len is not None:
         commit_bytes = int(((np.asarray(accept_len) + 1) * inp.hkv * inp.d * esz * 2 * 2).sum())

@@ -122,6 +122,17 @@ size_t spec_workspace_size(int op, int batch, int total_nodes, int max_nodes, in
 int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, int page_size,
                    int max_prefix, int* splits, int* tensor_cores);
 
+/* Read plan spec_accept uses for these sizes (informational; the pages have no
+ * counterpart): *walk = 1 when the call reads only the rows of the nodes its walk visits
+ * (the root and each accepted node) -- always for SPEC_STOCHASTIC; for SPEC_GREEDY when a
+ * model of the two ways (a walk from the root, one 8-CTA cluster per sequence, at most
+ * path_cap rows each, against streaming every row at the copy rate) finds the walk
+ * cheaper, which needs many rows per sequence -- and 0 when it streams every row. The
+ * results are the same either way. sm_count: the GPU's SMs (0: the current device's).
+ * Assumes 16-byte aligned logits rows (the walk needs them). Returns SPEC_OK,
+ * SPEC_ERR_ARG, or SPEC_ERR_CUDA when sm_count is 0 and no device answers. */
+int spec_accept_plan(int mode, int batch, int total_nodes, int vocab, int path_cap, int sm_count, int* walk);
+
 /* Static, NUL-terminated description of a spec_status value. */
 const char* spec_status_string(int status);
 

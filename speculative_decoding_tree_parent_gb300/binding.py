@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
            "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
            "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8",
-           "spec_tree_verify_attn_parents", "spec_tree_expand_multi")
+           "spec_tree_verify_attn_parents", "spec_tree_expand_multi", "spec_accept_plan")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -35,6 +35,7 @@ _SIGS = {
     "spec_status_string": (ctypes.c_char_p, [_I]),
     "spec_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "spec_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "spec_accept_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "spec_build_tree_mask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "spec_tree_verify_attn": (_I, [_I, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                    _I, _F, _P, _P, _P, _Z, _P, _P]),
@@ -131,6 +132,16 @@ def spec_attn_plan(dtype, batch, max_nodes, hq, hkv, d, page_size, max_prefix):
                                ctypes.addressof(s), ctypes.addressof(tc))
     _check(st, "spec_attn_plan")
     return s.value, tc.value
+
+
+def spec_accept_plan(mode, batch, total_nodes, vocab, path_cap, sm_count=0):
+    """1 when spec_accept reads only the visited nodes' rows (the walk), 0 when it streams
+    every row (greedy only); sm_count 0: the current device's."""
+    w = ctypes.c_int(0)
+    st = load().spec_accept_plan(int(mode), int(batch), int(total_nodes), int(vocab), int(path_cap), int(sm_count),
+                                 ctypes.addressof(w))
+    _check(st, "spec_accept_plan")
+    return w.value
 
 
 def spec_build_tree_mask(parent, qo_indptr, max_nodes, mask, depth=None, dev_status=None, stream=None):

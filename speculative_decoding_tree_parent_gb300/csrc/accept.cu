@@ -617,6 +617,20 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
 constexpr int kLazyCluster = 8;
 constexpr int kLazyThreads = 512;
 
+// Whether greedy acceptance walks from the root (true) or streams every row. The walk reads
+// at most path_cap rows per sequence, one after another; the stream reads every row at the
+// copy rate. A model of both (a step: ~1.5 us of latency plus an eighth of a row at ~50 GB/s
+// per SM, two clusters' CTAs per SM; the stream: ~6 TB/s and a ~3.5 us tail) picks the walk
+// only where it is clearly cheaper: many rows per sequence, several sequences.
+bool greedy_walks(int batch, int total_nodes, int vocab, int path_cap, int sms) {
+  if (batch > kMaxGridYZ || sms <= 0) return false;
+  const double stream_us = (double)total_nodes * vocab * 4.0 / 6.0e6 + 3.5;
+  const long clusters = (sms * 2L) / kLazyCluster > 0 ? (sms * 2L) / kLazyCluster : 1;
+  const long waves = (batch + clusters - 1) / clusters;
+  const double step_us = 1.5 + (double)vocab * 4.0 / kLazyCluster / 50.0e3;
+  return (double)waves * path_cap * step_us < stream_us;
+}
+
 __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThreads, 2)
     accept_greedy_lazy_kernel(const float* __restrict__ logits, int vocab, const int32_t* __restrict__ qo,
                               const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens, int path_cap,
@@ -1365,22 +1379,13 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
                    (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
   if (mode == SPEC_GREEDY && vec && batch <= kMaxGridYZ) {
-    // The walk from the root reads at most path_cap rows per sequence, one after another; the
-    // stream reads every row at the copy rate. A model of both (per-step latency of a cluster
-    // reading an eighth of a row; ~6 TB/s and a ~3.5 us tail for the stream) picks the walk
-    // only where it is clearly cheaper: many rows per sequence, several sequences.
     static PerDevice sm_walk;
     const int sms = per_device(sm_walk, [](int dev) {
       int v = 0;
       return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
     });
     if (sms == 0) return SPEC_ERR_CUDA;
-    const double stream_us = (double)total_nodes * vocab * 4.0 / 6.0e6 + 3.5;
-    const long clusters = (sms * 2L) / kLazyCluster > 0 ? (sms * 2L) / kLazyCluster : 1;
-    const long waves = (batch + clusters - 1) / clusters;
-    const double step_us = 1.5 + (double)vocab * 4.0 / kLazyCluster / 50.0e3;
-    const double walk_us = (double)waves * path_cap * step_us;
-    if (walk_us < stream_us) {
+    if (greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
       if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
                      qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
         return SPEC_ERR_CUDA;

@@ -4,6 +4,7 @@
 #include "draft_tree.cuh"
 
 namespace specv {
+bool greedy_walks(int batch, int total_nodes, int vocab, int path_cap, int sms);
 int launch_tree_mask(const int32_t* parent, const int32_t* qo, int batch, int total_nodes, int max_nodes,
                      uint64_t* mask, int32_t* depth, int32_t* status, cudaStream_t stream);
 int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,
@@ -105,6 +106,24 @@ int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, 
   *tensor_cores = tc ? 1 : 0;
   *splits = tc ? attn_splits_tc(batch, max_nodes, hq, hkv, max_prefix)
                : attn_splits_simt(batch, max_nodes, hq, hkv, max_prefix);
+  return SPEC_OK;
+}
+
+int spec_accept_plan(int mode, int batch, int total_nodes, int vocab, int path_cap, int sm_count, int* walk) {
+  if (mode != SPEC_GREEDY && mode != SPEC_STOCHASTIC) return SPEC_ERR_ARG;
+  if (batch < 0 || total_nodes < batch || vocab <= 0 || path_cap < 1 || sm_count < 0 || !walk) return SPEC_ERR_ARG;
+  if (mode == SPEC_STOCHASTIC) {
+    *walk = 1;
+    return SPEC_OK;
+  }
+  int sms = sm_count;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return SPEC_ERR_CUDA;
+  }
+  *walk = (vocab % 4 == 0 && greedy_walks(batch, total_nodes, vocab, path_cap, sms)) ? 1 : 0;
   return SPEC_OK;
 }
 

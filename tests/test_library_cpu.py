@@ -156,3 +156,17 @@ def test_batches_past_a_launch_grid_are_refused(lib):
     st = lib.spec_tree_expand_multi(fake, 1000, 1000, 1000, 65536, 64, 8, 4, 4, 0.0, fake, 1 << 40, fake, fake,
                                     fake, fake, fake, fake, fake, None, None, None)
     assert st == -6
+
+
+def test_accept_plan(lib):
+    """The read plan of spec_accept (host model only, given an SM count): the single-sequence
+    64-node verify streams every row; 32 sequences of 64 nodes walk; stochastic always walks;
+    an odd vocabulary (no 16-byte rows) streams."""
+    G, S = binding.SPEC_GREEDY, binding.SPEC_STOCHASTIC
+    assert binding.spec_accept_plan(G, 1, 64, 128256, 9, 152) == 0
+    assert binding.spec_accept_plan(G, 32, 2048, 128256, 9, 152) == 1
+    assert binding.spec_accept_plan(G, 128, 704, 128256, 9, 152) == 0    # short chains: the stream
+    assert binding.spec_accept_plan(G, 32, 2048, 128255, 9, 152) == 0
+    assert binding.spec_accept_plan(S, 1, 64, 128256, 9, 152) == 1
+    with pytest.raises(binding.SpecError):
+        binding.spec_accept_plan(G, 4, 3, 1000, 9, 152)   # fewer nodes than sequences
