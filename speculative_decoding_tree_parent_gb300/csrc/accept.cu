@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kAcceptThreads, 5) accept_greedy_kernel(
 // (max, index) pairs meet through distributed shared memory, and every CTA finds the same
 // child (the lowest id whose token is the argmax) in the sequence's staged tree. The outputs
 // are the stream kernel's bit for bit (the same (value, lower index) order). The commit, when
-// asked for, is the commit kernel's, launched after.
+// asked for, follows in the same launch: rank 0 of each cluster copies its sequence's path.
 constexpr int kLazyCluster = 8;
 constexpr int kLazyThreads = 512;
 
@@ -635,7 +635,7 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     accept_greedy_lazy_kernel(const float* __restrict__ logits, int vocab, const int32_t* __restrict__ qo,
                               const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens, int path_cap,
                               int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
-                              int32_t* status, bool vec) {
+                              int32_t* status, bool vec, const CommitArgs ca) {
   cg::cluster_group cl = cg::this_cluster();
   constexpr int kWarps = kLazyThreads / 32;
   __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes];
@@ -757,6 +757,13 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
       trow[k] = -1;
     }
   cl.sync();  // no CTA leaves while another may still read its shared memory
+  if (ca.k_tree != nullptr && rank == 0) {  // the commit of this sequence's path (the whole CTA)
+    __syncthreads();  // (the path and tokens written above are visible to the CTA)
+    if (ca.ins.token_buf != nullptr)
+      commit_sequence<true, true>(ca, b, base, n, L, nullptr, prow, path_cap, status);
+    else
+      commit_sequence<true, false>(ca, b, base, n, L, nullptr, prow, path_cap, status);
+  }
 }
 
 // ---------------------------------------------------------------- stochastic: walk
@@ -1361,6 +1368,23 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
                   cudaStream_t stream, const CommitArgs* commit) {
   CommitArgs ca = {};
   if (commit != nullptr) ca = *commit;
+  const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
+                   (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
+  if (mode == SPEC_GREEDY && vec && batch <= kMaxGridYZ) {  // the walk from the root, commit fused
+    static PerDevice sm_walk;
+    const int sms = per_device(sm_walk, [](int dev) {
+      int v = 0;
+      return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
+    });
+    if (sms == 0) return SPEC_ERR_CUDA;
+    if (greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
+      if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
+                     qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec, ca) !=
+          cudaSuccess)
+        return SPEC_ERR_CUDA;
+      return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    }
+  }
   // Greedy commits inside the acceptance kernel only for a few sequences: its final CTA does
   // them one after another. More sequences are committed by the commit kernel (one CTA per
   // sequence, launched to start as the acceptance grid drains), like the stochastic path.
@@ -1376,26 +1400,6 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   const AcceptWs w = AcceptWs::make(batch, total_nodes, chunks);
   uint8_t* wb = static_cast<uint8_t*>(ws);
   unsigned* counter = reinterpret_cast<unsigned*>(wb + w.counter);
-  const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
-                   (dl == nullptr || (reinterpret_cast<uintptr_t>(dl) & 15) == 0);
-  if (mode == SPEC_GREEDY && vec && batch <= kMaxGridYZ) {
-    static PerDevice sm_walk;
-    const int sms = per_device(sm_walk, [](int dev) {
-      int v = 0;
-      return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
-    });
-    if (sms == 0) return SPEC_ERR_CUDA;
-    if (greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
-      if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
-                     qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-      if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-      if (ca.k_tree == nullptr) return SPEC_OK;
-      return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
-                              ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,
-                              ca.v_pool, batch, ca.hkv, ca.d, status, stream, ca.ins);
-    }
-  }
   if (mode == SPEC_GREEDY) {
     // the partials (8 bytes per 4096-logit task) when the rows pass the slots
     ArgPartial* part = reinterpret_cast<ArgPartial*>(wb + w.partials);
