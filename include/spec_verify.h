@@ -70,9 +70,9 @@
  *     kernel between the two. Kernels that never signal early (the usual
  *     case) need nothing. Of this library's kernels, the ones that signal
  *     early write only mask and depth (spec_build_tree_mask), out, lse and
- *     the workspace (the attention and its split merge), the workspace (the
- *     stochastic statistics) and the acceptance results (greedy spec_accept);
- *     the commit kernels, which write the pool, never do.
+ *     the workspace (the attention and its split merge) and the acceptance
+ *     results (greedy spec_accept when it streams every row); the commit
+ *     kernels and the acceptance walks, which may write the pool, never do.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -221,13 +221,20 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
  *   uniforms[c][0] < r(x) / q_v(x); a rejection replaces r by
  *   max(r - q_v, 0) normalised; if no child is accepted the bonus is the
  *   inverse-CDF draw from r with uniforms[v][1].
+ *   Rows read: both modes need the logits of the nodes the walk visits only (the
+ *   root and each accepted node). Stochastic acceptance always reads just those;
+ *   greedy acceptance either streams every row (one wave of CTAs, a last-CTA walk)
+ *   or walks from the root reading just those, whichever spec_accept_plan's model
+ *   finds cheaper for the sizes. The results are the same either way.
  *
  *   parent, draft_tokens  int32 [total_nodes]  (root's token = last accepted token)
  *   target_logits  float [total_nodes][vocab]
  *   draft_logits   float [total_nodes][vocab]  (stochastic only; NULL for greedy)
  *   uniforms       float [total_nodes][2]      (stochastic only) (u_accept, u_bonus) in [0,1)
  *   temperature    > 0 (stochastic only)
- *   path_cap       row length of path / out_tokens (>= deepest accepted path + 1).
+ *   path_cap       row length of path / out_tokens (>= deepest accepted path + 1; the
+ *                  trees' depth + 1 always suffices). It also bounds the greedy walk's
+ *                  rows per sequence in spec_accept_plan's model.
  *   accept_len int32 [batch] (out)  L = accepted draft nodes (root excluded).
  *   path       int32 [batch][path_cap] (out)  root (0) then the accepted node ids; -1 after.
  *   out_tokens int32 [batch][path_cap] (out)  the L accepted tokens, then the bonus; -1 after.
