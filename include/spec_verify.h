@@ -61,10 +61,12 @@
  *     serialization, so a call may begin while the kernel enqueued before it
  *     is still running. Every kernel waits for that predecessor before it
  *     writes anything and before it reads what the predecessor may write,
- *     with one exception: spec_tree_verify_attn (and its _kv8 and _parents
+ *     with two exceptions: spec_tree_verify_attn (and its _kv8 and _parents
  *     forms) reads q, k_pool, v_pool, k_tree, v_tree, page_table, prefix_len,
  *     qo_indptr and kv_scale (everything but the mask or parent array)
- *     before that wait. If the kernel enqueued just before it
+ *     before that wait, and greedy spec_accept (and spec_accept_commit), when
+ *     it walks from the root (spec_accept_plan), reads parent, draft_tokens,
+ *     target_logits and qo_indptr before it. If the kernel enqueued just before it
  *     writes one of those and signals its dependents early (the
  *     griddepcontrol.launch_dependents instruction), put an event or another
  *     kernel between the two. Kernels that never signal early (the usual

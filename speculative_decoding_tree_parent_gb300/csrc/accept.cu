@@ -644,7 +644,10 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
   __shared__ float s_bv[2];  // this CTA's (max, index) of the step, by step parity
   __shared__ int s_bi[2];
   __shared__ int s_child;
-  pdl_wait();  // stream order: the inputs may come from the kernel before
+  __shared__ int s_path[kMaxTreeNodes];  // the accepted nodes, written out after the wait below
+  // The walk reads inputs only (the tree, the logits, qo_indptr): it runs before the grid
+  // dependency wait, which comes before its first write -- so its reads overlap the tail of
+  // the kernel enqueued before it (the attention's merge, in a verification step).
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -654,6 +657,7 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
   int32_t* trow = out_tokens + (size_t)b * path_cap;
   const bool writer = rank == 0 && threadIdx.x == 0;
   if (n < 1) {  // the same in every CTA of the cluster: all leave here
+    pdl_wait();
     if (writer) report(status, SPEC_ERR_CAPACITY);
     return;
   }
@@ -665,7 +669,7 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
   const int c_lo = rank * per;
   const int n_sl = max(0, min(vocab, c_lo + per) - c_lo);
   int v = 0, L = 0, bonus = 0, parity = 0;
-  if (writer) prow[0] = 0;
+  bool truncated = false;
   __syncthreads();
   while (true) {
     const float* row = logits + (size_t)(base + v) * vocab + c_lo;
@@ -734,28 +738,29 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
       break;
     }
     if (L + 1 >= path_cap) {  // accepted path does not fit: truncate here
-      if (writer) report(status, SPEC_ERR_CAPACITY);
+      truncated = true;
       bonus = a;
       break;
     }
     ++L;
-    if (writer) {
-      prow[L] = c;
-      trow[L - 1] = s_tok[c];
-    }
+    if (threadIdx.x == 0) s_path[L] = c;  // (L < n: the path visits distinct nodes)
     v = c;
     parity ^= 1;
   }
-  if (writer) {
-    trow[L] = bonus;
-    accept_len[b] = L;
-    if (flags != nullptr) flags[b] = 0;
-  }
-  if (rank == 0)
-    for (int k = L + 1 + threadIdx.x; k < path_cap; k += kLazyThreads) {
-      prow[k] = -1;
-      trow[k] = -1;
+  pdl_wait();  // the kernel before has finished: the outputs may be written
+  __syncthreads();  // (s_path complete)
+  if (rank == 0) {
+    for (int k = threadIdx.x; k < path_cap; k += kLazyThreads) {
+      const int node = k == 0 ? 0 : k <= L ? s_path[k] : -1;
+      prow[k] = node;
+      trow[k] = k < L ? s_tok[s_path[k + 1]] : k == L ? bonus : -1;
     }
+    if (threadIdx.x == 0) {
+      accept_len[b] = L;
+      if (flags != nullptr) flags[b] = 0;
+      if (truncated) report(status, SPEC_ERR_CAPACITY);
+    }
+  }
   cl.sync();  // no CTA leaves while another may still read its shared memory
   if (ca.k_tree != nullptr && rank == 0) {  // the commit of this sequence's path (the whole CTA)
     __syncthreads();  // (the path and tokens written above are visible to the CTA)
