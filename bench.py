@@ -415,6 +415,14 @@ def run_ours(args):
     # the step: mask, attention, fused acceptance + commit. The attention that builds the
     # mask itself (spec_tree_verify_attn_parents) is timed per call beside it; in a step the
     # separate mask kernel overlaps the attention's prologue and is the faster of the two.
+    # The step's inputs are resident: no kernel in it writes what the attention or the
+    # greedy walk reads, so both may read before their grid-dependency wait
+    # (spec_set_early_reads, on for every graph from here). The same step with the
+    # library's default (every kernel waits first) is timed beside it.
+    from speculative_decoding_tree_parent_gb300 import binding as BIND
+    with BIND.early_reads(False):
+        g_step_default = capture(lambda: [rep.step(mode) for rep in reps])
+    BIND.spec_set_early_reads(1)
     g_step = capture(lambda: [rep.step(mode) for rep in reps])
     g_calls = {"mask": capture(over_reps("build_mask")), "attention": capture(over_reps("attention")),
                "accept": capture(over_reps("accept")), "commit": capture(over_reps("commit")),
@@ -463,7 +471,7 @@ def run_ours(args):
         return ev
 
     # warm-up
-    timed_replays([g_step] + list(g_calls.values()), max(args.warmup, 3))
+    timed_replays([g_step, g_step_default] + list(g_calls.values()), max(args.warmup, 3))
     torch.cuda.synchronize()
 
     # ---- timed region: K steps = K / R replays of the R-step graph --------------------
@@ -473,12 +481,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ev_step = timed_replays([g_step], n_rep)
+        ev_default = timed_replays([g_step_default], n_rep)
         ev_calls = timed_replays(list(g_calls.values()), n_rep)
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) / R for ((a, b),) in ev_step]
+    step_default_us = statistics.mean(a.elapsed_time(b) / R for ((a, b),) in ev_default) * 1e3
     call_ms = {name: [ev_calls[r][i][0].elapsed_time(ev_calls[r][i][1]) / R for r in range(n_rep)]
                for i, name in enumerate(g_calls)}
     total_ms = reduce_over_ranks(sum(step_ms) * R, "max", ws, dev)
@@ -687,6 +697,9 @@ def run_ours(args):
                          f"(a 256 MB buffer written, then read back, so no dirty flush lines remain)",
                    "timing": f"CUDA-graph replay of {R} steps, CUDA events on the launching stream",
                    "step": "mask, attention, acceptance + KV commit",
+                   "early_reads": "on (spec_set_early_reads): the step's inputs are resident, and no "
+                                  "kernel in it writes what the attention or the greedy walk reads "
+                                  "before its grid-dependency wait",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
         "attn": {"tokens_per_s": wc["tokens"] / t_attn, "tflops": attn_tflops, "gbs": attn_gbs,
                  "roofline_frac": attn_roof, "us": t_attn * 1e6, "flops": wc["attn_flops"],
@@ -695,6 +708,7 @@ def run_ours(args):
                           "accept_us": t_acc * 1e6, "commit_us": t_com * 1e6,
                           "separate_us": (t_acc + t_com) * 1e6, "gbs": accom_gbs, "hbm_frac": accom_gbs / hbm,
                           "bytes": wc["accept_bytes"] + wc["commit_bytes"]},
+        "step_us_early_reads_off": step_default_us,
         "mask_us": statistics.mean(call_ms["mask"]) * 1e3,
         "attn_with_mask_us": statistics.mean(call_ms["attention_parents"]) * 1e3 if with_parents else None,
         "attn_fp8kv": attn8,
@@ -702,8 +716,9 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": job_throughput(tokens_all, e2e_total), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_total / args.steps},
-        # launches in the timed region: full-step replays + per-call replays, R steps each
-        "gpu_launches": (launches + call_launches) * args.steps,
+        # launches in the timed region: full-step replays (early reads on, then off) +
+        # per-call replays, R steps each
+        "gpu_launches": (2 * launches + call_launches) * args.steps,
         "clocks": clk.summary(),
     }
     line.update(extras)

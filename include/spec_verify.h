@@ -59,22 +59,25 @@
  *     that may run concurrently.
  *   - Early start: the kernels are launched with programmatic stream
  *     serialization, so a call may begin while the kernel enqueued before it
- *     is still running. Every kernel waits for that predecessor before it
- *     writes anything and before it reads what the predecessor may write,
- *     with two exceptions: spec_tree_verify_attn (and its _kv8 and _parents
- *     forms) reads q, k_pool, v_pool, k_tree, v_tree, page_table, prefix_len,
- *     qo_indptr and kv_scale (everything but the mask or parent array)
- *     before that wait, and greedy spec_accept (and spec_accept_commit), when
- *     it walks from the root (spec_accept_plan), reads parent, draft_tokens,
- *     target_logits and qo_indptr before it. If the kernel enqueued just before it
- *     writes one of those and signals its dependents early (the
- *     griddepcontrol.launch_dependents instruction), put an event or another
- *     kernel between the two. Kernels that never signal early (the usual
- *     case) need nothing. Of this library's kernels, the ones that signal
- *     early write only mask and depth (spec_build_tree_mask), out, lse and
- *     the workspace (the attention and its split merge) and the acceptance
- *     results (greedy spec_accept when it streams every row); the commit
- *     kernels and the acceptance walks, which may write the pool, never do.
+ *     is still running. By default every kernel waits for that predecessor
+ *     before it reads or writes anything (a predecessor's writes are visible
+ *     only after that wait, whether or not it signals early). A caller whose
+ *     preceding kernel writes none of the inputs listed below can let two
+ *     kernels read them before the wait with spec_set_early_reads(1):
+ *     spec_tree_verify_attn (and its _kv8 and _parents forms) then reads q,
+ *     k_pool, v_pool, k_tree, v_tree, page_table, prefix_len, qo_indptr and
+ *     kv_scale (everything but the mask or parent array) before it waits, and
+ *     greedy spec_accept (and spec_accept_commit), when it walks from the root
+ *     (spec_accept_plan), reads parent, draft_tokens, target_logits and
+ *     qo_indptr before it waits; both still wait before their first write.
+ *     (In a target model's forward pass the kernel before the attention
+ *     writes q and the tree's K/V, and the one before the acceptance writes
+ *     the logits: keep the switch off there, or put an event between.) Of
+ *     this library's kernels, the ones that signal early write only mask and
+ *     depth (spec_build_tree_mask), out, lse and the workspace (the attention
+ *     and its split merge) and the acceptance results (greedy spec_accept when
+ *     it streams every row); the commit kernels and the acceptance walks,
+ *     which may write the pool, never do.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -134,6 +137,13 @@ int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, 
  * Assumes 16-byte aligned logits rows (the walk needs them). Returns SPEC_OK,
  * SPEC_ERR_ARG, or SPEC_ERR_CUDA when sm_count is 0 and no device answers. */
 int spec_accept_plan(int mode, int batch, int total_nodes, int vocab, int path_cap, int sm_count, int* walk);
+
+/* Whether the attention and the greedy walk may read their inputs before waiting for
+ * the kernel enqueued just before them (the early-start rule above). enable != 0 turns
+ * it on for the whole process, 0 (the default) off; each later call reads the setting
+ * when it is made (a captured CUDA graph keeps the setting it was captured with).
+ * Thread-safe. Results do not depend on it. Returns the previous setting (0 or 1). */
+int spec_set_early_reads(int enable);
 
 /* Static, NUL-terminated description of a spec_status value. */
 const char* spec_status_string(int status);

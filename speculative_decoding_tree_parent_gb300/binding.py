@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("spec_version", "spec_status_string", "spec_workspace_size", "spec_attn_plan", "spec_build_tree_mask",
            "spec_tree_verify_attn", "spec_accept", "spec_kv_commit", "spec_accept_commit", "spec_accept_noalloc",
            "spec_tree_init", "spec_tree_expand", "spec_tree_verify_attn_kv8", "spec_kv_commit_kv8",
-           "spec_tree_verify_attn_parents", "spec_tree_expand_multi", "spec_accept_plan")
+           "spec_tree_verify_attn_parents", "spec_tree_expand_multi", "spec_accept_plan", "spec_set_early_reads")
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -36,6 +36,7 @@ _SIGS = {
     "spec_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "spec_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "spec_accept_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
+    "spec_set_early_reads": (_I, [_I]),
     "spec_build_tree_mask": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "spec_tree_verify_attn": (_I, [_I, _P, _P, _P, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                    _I, _F, _P, _P, _P, _Z, _P, _P]),
@@ -142,6 +143,28 @@ def spec_accept_plan(mode, batch, total_nodes, vocab, path_cap, sm_count=0):
                                  ctypes.addressof(w))
     _check(st, "spec_accept_plan")
     return w.value
+
+
+def spec_set_early_reads(enable):
+    """Let the attention and the greedy walk read their inputs before waiting for the kernel
+    enqueued just before them (only where that kernel writes none of them); returns the
+    previous setting. Off by default."""
+    return int(load().spec_set_early_reads(1 if enable else 0))
+
+
+class early_reads:
+    """Context manager: spec_set_early_reads(enable) inside, the previous setting after."""
+
+    def __init__(self, enable=True):
+        self.enable = enable
+
+    def __enter__(self):
+        self.prev = spec_set_early_reads(self.enable)
+        return self
+
+    def __exit__(self, *exc):
+        spec_set_early_reads(self.prev)
+        return False
 
 
 def spec_build_tree_mask(parent, qo_indptr, max_nodes, mask, depth=None, dev_status=None, stream=None):

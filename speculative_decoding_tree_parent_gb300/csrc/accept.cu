@@ -635,7 +635,7 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     accept_greedy_lazy_kernel(const float* __restrict__ logits, int vocab, const int32_t* __restrict__ qo,
                               const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens, int path_cap,
                               int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
-                              int32_t* status, bool vec, const CommitArgs ca) {
+                              int32_t* status, bool vec, bool early, const CommitArgs ca) {
   cg::cluster_group cl = cg::this_cluster();
   constexpr int kWarps = kLazyThreads / 32;
   __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes];
@@ -645,9 +645,11 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
   __shared__ int s_bi[2];
   __shared__ int s_child;
   __shared__ int s_path[kMaxTreeNodes];  // the accepted nodes, written out after the wait below
-  // The walk reads inputs only (the tree, the logits, qo_indptr): it runs before the grid
-  // dependency wait, which comes before its first write -- so its reads overlap the tail of
-  // the kernel enqueued before it (the attention's merge, in a verification step).
+  // The walk reads inputs only (the tree, the logits, qo_indptr). Where the caller has
+  // declared that the kernel enqueued before this one writes none of them (early), it runs
+  // before the grid-dependency wait, which then comes just before its first write, so its
+  // reads overlap that kernel's tail; otherwise it waits first.
+  if (!early) pdl_wait();
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1384,7 +1386,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
     if (sms == 0) return SPEC_ERR_CUDA;
     if (greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
       if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
-                     qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec, ca) !=
+                     qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec, early_reads(), ca) !=
           cudaSuccess)
         return SPEC_ERR_CUDA;
       return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

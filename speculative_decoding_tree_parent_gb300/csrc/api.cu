@@ -1,5 +1,7 @@
 // C ABI of libspecverify: argument checks on the host, then kernel dispatch.
 // Every entry point is asynchronous on the caller's stream and allocates nothing.
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "draft_tree.cuh"
 
@@ -50,13 +52,18 @@ static bool attn_wants_tc(int dtype, int d) { return dtype == SPEC_BF16 && d == 
 // Grids put (sequence, KV head) pairs, or sequences, on a launch's y or z dimension.
 static bool grid_fits(long n) { return n <= kMaxGridYZ; }
 
+static std::atomic<int> g_early_reads{0};
+bool early_reads() { return g_early_reads.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace specv
 
 using namespace specv;
 
 extern "C" {
 
-int spec_version(void) { return 111; }
+int spec_version(void) { return 112; }
+
+int spec_set_early_reads(int enable) { return g_early_reads.exchange(enable ? 1 : 0); }
 
 const char* spec_status_string(int status) {
   switch (status) {

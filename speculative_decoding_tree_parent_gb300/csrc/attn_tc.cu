@@ -118,6 +118,7 @@ struct TcParams {
   const float* kv_scale;  // FP8 cache: [2][Hkv] K then V scales (unused with a bf16 cache)
   int32_t* status;
   int batch;
+  int early_reads;  // the inputs may be read before the grid-dependency wait (spec_set_early_reads)
 };
 
 // Longest-first order (kLpt instances) applies to unsplit launches of 2 .. kLptMax sequences
@@ -254,6 +255,9 @@ __global__ void __launch_bounds__(TcCfg<kFp8, kPar>::kThreads, 1)
     tc::prefetch_tmap(&tm_kt);
     tc::prefetch_tmap(&tm_vt);
   }
+  // Unless the caller has declared that the kernel enqueued before this one writes none of
+  // the inputs (everything but the mask or parent array), nothing is read before it ends.
+  if (!p.early_reads) pdl_wait();
   const int G = p.G;
   int b = bg / p.hkv;
   const int g = bg - b * p.hkv;
@@ -294,7 +298,10 @@ __global__ void __launch_bounds__(TcCfg<kFp8, kPar>::kThreads, 1)
   // the two exits below are taken by every split CTA of a tile alike (they depend on b, g, pair)
   if (node0 >= N) return;  // this pair of M-tiles is past the sequence's tree
   if (N > p.mask_words * 64 || P < 0 || P > p.max_pages * 16) {
-    if (threadIdx.x == 0 && split == 0) report(p.status, SPEC_ERR_CAPACITY);
+    if (threadIdx.x == 0 && split == 0) {
+      pdl_wait();  // (the status word is written in stream order)
+      report(p.status, SPEC_ERR_CAPACITY);
+    }
     return;
   }
   const TcSplit sr = tc_split(P, N, p.splits, split);
@@ -1072,6 +1079,7 @@ int launch_attn_tc(const void* q, const void* k_pool, const void* v_pool, int nu
   prm.kv_scale = kv_scale;
   prm.status = status;
   prm.batch = batch;
+  prm.early_reads = early_reads() ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(splits, ceil_div(mtiles, kTiles), batch * hkv);
   cfg.blockDim = dim3(fp8 ? TcCfg<true>::kThreads : TcCfg<false>::kThreads);

@@ -42,9 +42,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while its predecessor in the stream still runs; it must
 // call pdl_wait() before reading anything the predecessor writes. pdl_trigger() lets
-// the successor be scheduled early.
+// the successor be scheduled early. A predecessor's writes are visible only after
+// pdl_wait(), whether or not it signals early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The process-wide choice of spec_set_early_reads, taken when a call is made: whether the
+// attention and the greedy walk may read their inputs before pdl_wait() (off: they wait first).
+bool early_reads();
 
 // Device-side insert of a step's tokens into each sequence's token buffer (the next step's
 // input, no host round trip): out_tokens[b][0 .. L] (the L accepted tokens, then the bonus,

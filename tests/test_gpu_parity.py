@@ -794,3 +794,73 @@ def test_accept_commit_token_insert_short_row(inputs, cfg):
             page, row = inp.page_table[b, (P + i) // inp.page_size], (P + i) % inp.page_size
             assert np.array_equal(kp[page, :, row], kb[page, :, row])
             assert np.array_equal(vp[page, :, row], vb[page, :, row])
+
+
+# ----------------------------------------------------------------------------- early reads
+
+_STEP_OUT = ("mask", "out", "lse", "accept_len", "path", "out_tokens", "seq_len", "k_pool", "v_pool")
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_step_early_reads_same_results(inputs, cfg):
+    """A step (mask, attention, greedy accept + commit, the greedy walk on these shapes) with
+    spec_set_early_reads on gives bit for bit the step with the default (every kernel waits
+    for its predecessor first), run eagerly and from a CUDA graph, and the oracle's paths."""
+    inp = inputs(cfg)
+    walk = B.spec_accept_plan(B.SPEC_GREEDY, inp.batch, inp.total_nodes, inp.vocab, inp.path_cap)
+    assert walk == 1
+    runs = {}
+    for early in (False, True):
+        with B.early_reads(early):
+            eager = DeviceBatch(inp, mode="greedy")
+            eager.step("greedy")
+            graphed = DeviceBatch(inp, mode="greedy")
+            s = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                graphed.step("greedy", stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+        assert _status(eager) == 0 and _status(graphed) == 0
+        for name in _STEP_OUT:
+            assert torch.equal(getattr(eager, name), getattr(graphed, name)), (early, name)
+        runs[early] = eager
+        del g
+    for name in _STEP_OUT:
+        assert torch.equal(getattr(runs[False], name), getattr(runs[True], name)), name
+    ref = _oracle_accept(inp, "greedy")
+    assert _accept_compare(runs[True], ref) == 0
+
+
+def test_accept_default_sees_logits_written_just_before(inputs):
+    """With the default (early reads off) the greedy walk may follow, in the same stream, the
+    kernel that writes its logits: a copy replaces them right before the call, and the walk
+    must take the new rows' argmax (the oracle on the new logits), not the old ones."""
+    inp = inputs(2)
+    assert B.spec_set_early_reads(0) == 0
+    rng = np.random.default_rng(11)
+    new = rng.standard_normal(inp.target_logits.shape).astype(np.float32)
+    qo = np.asarray(inp.qo_indptr)
+    par = np.asarray(inp.parent)
+    toks = np.asarray(inp.draft_tokens)
+    for v in range(1, int(qo[1])):                 # plant a path two levels deep in the new rows
+        if par[v] == 0:
+            new[0, :] = new[0].min() - 1.0
+            new[0, toks[v]] = 5.0
+            kids = [c for c in range(v + 1, int(qo[1])) if par[c] == v]
+            if kids:
+                new[v, :] = new[v].min() - 1.0
+                new[v, toks[kids[0]]] = 5.0
+            break
+    db = DeviceBatch(inp, mode="greedy")
+    src = torch.from_numpy(new).cuda()
+    torch.cuda.synchronize()
+    db.target_logits.copy_(src)     # the kernel just before the acceptance writes its logits
+    db.accept_commit("greedy")
+    torch.cuda.synchronize()
+    assert _status(db) == 0
+    ref = oracle.greedy_accept(inp.parent, inp.draft_tokens, new, inp.qo_indptr, inp.path_cap)
+    assert np.array_equal(db.accept_len.cpu().numpy(), ref.accept_len)
+    assert np.array_equal(db.path.cpu().numpy(), ref.path)
+    assert np.array_equal(db.out_tokens.cpu().numpy(), ref.out_tokens)
+    assert int(ref.accept_len[0]) >= 1

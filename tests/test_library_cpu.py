@@ -170,3 +170,15 @@ def test_accept_plan(lib):
     assert binding.spec_accept_plan(S, 1, 64, 128256, 9, 152) == 1
     with pytest.raises(binding.SpecError):
         binding.spec_accept_plan(G, 4, 3, 1000, 9, 152)   # fewer nodes than sequences
+
+
+def test_early_reads_switch(lib):
+    """spec_set_early_reads is host state only: off by default, returns the previous
+    setting, and the context manager restores it."""
+    assert binding.spec_set_early_reads(0) == 0      # the default is off
+    assert binding.spec_set_early_reads(5) == 0      # any non-zero turns it on
+    assert binding.spec_set_early_reads(1) == 1
+    assert binding.spec_set_early_reads(0) == 1
+    with binding.early_reads(True):
+        assert binding.spec_set_early_reads(1) == 1
+    assert binding.spec_set_early_reads(0) == 0
