@@ -69,7 +69,9 @@
  *     kv_scale (everything but the mask or parent array) before it waits, and
  *     greedy spec_accept (and spec_accept_commit), when it walks from the root
  *     (spec_accept_plan), reads parent, draft_tokens, target_logits and
- *     qo_indptr before it waits; both still wait before their first write.
+ *     qo_indptr before it waits (spec_accept_commit also the commit's k_tree,
+ *     v_tree, page_table and prefix_len); both still wait before their first
+ *     write.
  *     (In a target model's forward pass the kernel before the attention
  *     writes q and the tree's K/V, and the one before the acceptance writes
  *     the logits: keep the switch off there, or put an event between.) Of

@@ -326,6 +326,116 @@ __device__ void commit_sequence(const CommitArgs& ca, int b, int base, int n, in
   if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
 }
 
+// The same commit in two halves, for the walk from the root (the whole CTA, rows 0 .. L).
+// walk_commit_load reads inputs only: the first rows' K/V (their sources need only the
+// path, so they load alongside the prefix length), then every slot's page entry, checked;
+// two dependent memory round trips in all, and the walk may run it before its
+// grid-dependency wait. walk_commit_store votes (a sequence with an error is reported and
+// left unwritten) and writes.
+constexpr int kCommitPer = 1;  // 16-byte pieces of the rows a thread holds in registers
+struct CommitLoad {
+  int P, code, total;
+  uint4 kb[kCommitPer], vb[kCommitPer];
+  size_t dst[kCommitPer];
+};
+
+__device__ __forceinline__ void walk_commit_load(const CommitArgs& ca, int b, int base, int n, int L,
+                                                 const int* spath, int path_cap, CommitLoad& c) {
+  const int rank = threadIdx.x, size = blockDim.x;
+  const int row_bytes = ca.d * ca.elem_bytes;
+  const int vecs = row_bytes >> 4;
+  const bool shape_ok = L >= 0 && L < path_cap && L < n;
+  const int total = shape_ok ? (L + 1) * ca.hkv * vecs : 0;
+  int slot_i[kCommitPer];
+#pragma unroll
+  for (int u = 0; u < kCommitPer; ++u) {  // the rows: addressed by the path alone
+    const int e = rank + u * size;
+    slot_i[u] = -1;
+    if (e < total) {
+      const int r = e / vecs, vi = e - (e / vecs) * vecs;
+      const int i = r / ca.hkv, g = r - (r / ca.hkv) * ca.hkv;
+      const int node = spath[i];
+      if (node >= 0 && node < n) {
+        const size_t src = ((size_t)(base + node) * ca.hkv + g) * row_bytes + ((size_t)vi << 4);
+        c.kb[u] = __ldg(reinterpret_cast<const uint4*>(ca.k_tree + src));
+        c.vb[u] = __ldg(reinterpret_cast<const uint4*>(ca.v_tree + src));
+        slot_i[u] = i;
+        c.dst[u] = (size_t)g * ca.page_size * row_bytes + ((size_t)vi << 4);  // + the page and slot below
+      }
+    }
+  }
+  const int P = __ldg(ca.prefix_len + b);
+  const int32_t* prow_pt = ca.page_table + (size_t)b * ca.max_pages;
+  int code = 0;
+  if (!shape_ok || P < 0) {
+    code = SPEC_ERR_INDEX;
+  } else if (ca.ins.token_buf != nullptr && P + L + 1 >= ca.ins.token_stride) {
+    code = SPEC_ERR_CAPACITY;  // the token row has no room for L + 1 tokens after P
+  } else {
+    for (int i = rank; i <= L; i += size) {
+      const int node = spath[i];
+      const int lp = (P + i) / ca.page_size;
+      const int page = lp < ca.max_pages ? __ldg(prow_pt + lp) : -1;
+      int cc = 0;
+      if (node < 0 || node >= n || (i == 0 && node != 0)) cc = SPEC_ERR_INDEX;
+      else if (lp >= ca.max_pages) cc = SPEC_ERR_CAPACITY;
+      else if (page < 0 || page >= ca.num_pages) cc = SPEC_ERR_PAGE;
+      if (code == 0) code = cc;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kCommitPer; ++u) {  // each held piece's destination (used once the vote passes)
+    if (slot_i[u] >= 0 && code == 0) {
+      const int slot = P + slot_i[u];
+      const int lp = slot / ca.page_size;
+      const int page = lp < ca.max_pages ? __ldg(prow_pt + lp) : 0;
+      c.dst[u] += (((size_t)page * ca.hkv) * ca.page_size + (slot % ca.page_size)) * row_bytes;
+    }
+  }
+  c.P = P;
+  c.code = code;
+  c.total = code == 0 ? total : 0;
+}
+
+template <bool kIns>
+__device__ __forceinline__ void walk_commit_store(const CommitArgs& ca, int b, int base, int L, const int* spath,
+                                                  int path_cap, int32_t* status, const CommitLoad& c) {
+  const int rank = threadIdx.x, size = blockDim.x;
+  if (__syncthreads_or(c.code != 0)) {
+    if (c.code != 0) report(status, c.code);
+    return;
+  }
+  // every slot and node checked above is valid from here on
+#pragma unroll
+  for (int u = 0; u < kCommitPer; ++u) {
+    if (rank + u * size < c.total) {
+      *reinterpret_cast<uint4*>(ca.k_pool + c.dst[u]) = c.kb[u];
+      *reinterpret_cast<uint4*>(ca.v_pool + c.dst[u]) = c.vb[u];
+    }
+  }
+  const int P = c.P;
+  const int row_bytes = ca.d * ca.elem_bytes;
+  const int vecs = row_bytes >> 4;
+  const int32_t* prow_pt = ca.page_table + (size_t)b * ca.max_pages;
+  for (int e = rank + kCommitPer * size; e < c.total; e += size) {  // long paths: the rest
+    const int r = e / vecs, vi = e - (e / vecs) * vecs;
+    const int i = r / ca.hkv, g = r - (r / ca.hkv) * ca.hkv;
+    const int slot = P + i;
+    const int page = __ldg(prow_pt + slot / ca.page_size);
+    const size_t src = ((size_t)(base + spath[i]) * ca.hkv + g) * row_bytes + ((size_t)vi << 4);
+    const size_t dst =
+        (((size_t)page * ca.hkv + g) * ca.page_size + (slot % ca.page_size)) * row_bytes + ((size_t)vi << 4);
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(ca.k_tree + src));
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(ca.v_tree + src));
+    *reinterpret_cast<uint4*>(ca.k_pool + dst) = kv;
+    *reinterpret_cast<uint4*>(ca.v_pool + dst) = vv;
+  }
+  if (kIns)  // the accepted tokens and the bonus after the root
+    for (int i = rank; i <= L; i += size)
+      ca.ins.token_buf[(size_t)b * ca.ins.token_stride + P + 1 + i] = ca.ins.out_tokens[(size_t)b * path_cap + i];
+  if (rank == 0 && ca.seq_len_out != nullptr) ca.seq_len_out[b] = P + L + 1;
+}
+
 // ---- the root row committed while the walk runs (fused greedy commit, few sequences)
 // The root (node 0, the last accepted token) always goes to slot P, whatever the walk
 // decides; only rows 1 .. L wait for it. One warp of the final CTA stages the root rows
@@ -667,6 +777,7 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     s_par[c] = __ldg(parent + base + c);
     s_tok[c] = __ldg(tokens + base + c);
   }
+  if (threadIdx.x == 0) s_path[0] = 0;  // the root
   const int per = ((vocab + kLazyCluster - 1) / kLazyCluster + 3) & ~3;
   const int c_lo = rank * per;
   const int n_sl = max(0, min(vocab, c_lo + per) - c_lo);
@@ -749,6 +860,14 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     v = c;
     parity ^= 1;
   }
+  // The commit's reads (the path's K/V rows, the prefix length, the slots' page entries) are
+  // inputs too: with early reads they go out before the wait, and only stores follow it.
+  const bool commit = ca.k_tree != nullptr && rank == 0;
+  CommitLoad pre;
+  if (commit && early) {
+    __syncthreads();  // (s_path complete)
+    walk_commit_load(ca, b, base, n, L, s_path, path_cap, pre);
+  }
   pdl_wait();  // the kernel before has finished: the outputs may be written
   __syncthreads();  // (s_path complete)
   if (rank == 0) {
@@ -764,12 +883,13 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     }
   }
   cl.sync();  // no CTA leaves while another may still read its shared memory
-  if (ca.k_tree != nullptr && rank == 0) {  // the commit of this sequence's path (the whole CTA)
+  if (commit) {  // the commit of this sequence's path (the whole CTA)
     __syncthreads();  // (the path and tokens written above are visible to the CTA)
+    if (!early) walk_commit_load(ca, b, base, n, L, s_path, path_cap, pre);
     if (ca.ins.token_buf != nullptr)
-      commit_sequence<true, true>(ca, b, base, n, L, nullptr, prow, path_cap, status);
+      walk_commit_store<true>(ca, b, base, L, s_path, path_cap, status, pre);
     else
-      commit_sequence<true, false>(ca, b, base, n, L, nullptr, prow, path_cap, status);
+      walk_commit_store<false>(ca, b, base, L, s_path, path_cap, status, pre);
   }
 }
 

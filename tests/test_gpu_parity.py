@@ -529,17 +529,19 @@ def test_accept_commit_fused(inputs, cfg, mode):
     assert np.array_equal(fused.seq_len.cpu().numpy(), seq_len)
 
 
-@pytest.mark.parametrize("cfg", [1, 3])
-def test_accept_commit_fused_bad_page(inputs, cfg):
+@pytest.mark.parametrize("cfg,early", [(1, False), (3, False), (3, True)])
+def test_accept_commit_fused_bad_page(inputs, cfg, early):
     """A page id outside the pool at a commit slot: SPEC_ERR_PAGE, that sequence left
-    unwritten, the acceptance results still those of the oracle."""
+    unwritten, the acceptance results still those of the oracle (also with early reads,
+    where the walk's commit checks the slots before its grid-dependency wait)."""
     inp = inputs(cfg)
     db = DeviceBatch(inp)
     # sequence 0: every page-table entry from its prefix end on points outside the pool
     P0 = int(inp.prefix_len[0])
     db.page_table[0, P0 // inp.page_size:] = inp.num_pages + 7
     before_k, before_v = db.k_pool.clone(), db.v_pool.clone()
-    db.accept_commit("greedy")
+    with B.early_reads(early):
+        db.accept_commit("greedy")
     torch.cuda.synchronize()
     assert _status(db) == -3   # SPEC_ERR_PAGE
     ref = _oracle_accept(inp, "greedy")
@@ -721,9 +723,10 @@ def _deep_tokens(inp):
     return replace(inp, draft_tokens=tokens)
 
 
-@pytest.mark.parametrize("cfg,mode,deep", [(1, "greedy", False), (1, "greedy", True), (3, "greedy", False),
-                                           (5, "stochastic", False)])
-def test_accept_commit_token_insert(inputs, cfg, mode, deep):
+@pytest.mark.parametrize("cfg,mode,deep,early", [(1, "greedy", False, False), (1, "greedy", True, False),
+                                                 (3, "greedy", False, False), (3, "greedy", True, True),
+                                                 (5, "stochastic", False, False)])
+def test_accept_commit_token_insert(inputs, cfg, mode, deep, early):
     """spec_accept_commit with a token buffer: after the call each row holds the old tokens
     up to the root, then the step's accepted tokens and the bonus (the next root), and is
     unchanged elsewhere -- the oracle's token_insert of the oracle's acceptance -- while the
@@ -736,12 +739,14 @@ def test_accept_commit_token_insert(inputs, cfg, mode, deep):
     rng = np.random.default_rng(cfg)
     buf0 = rng.integers(0, inp.vocab, (inp.batch, stride)).astype(np.int32)
     buf = torch.from_numpy(buf0).cuda()
-    B.spec_accept_commit(B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY, db.parent, db.tokens,
-                         db.target_logits, db.qo, db.max_nodes, db.accept_len, db.path, db.out_tokens, db.acc_ws,
-                         db.k_tree, db.v_tree, db.page_table, db.prefix_len, db.k_pool, db.v_pool,
-                         seq_len_out=db.seq_len, draft_logits=db.draft_logits if mode == "stochastic" else None,
-                         uniforms=db.uniforms if mode == "stochastic" else None, temperature=inp.temperature,
-                         flags=db.flags, dev_status=db.status, token_buf=buf)
+    torch.cuda.synchronize()
+    with B.early_reads(early):
+        B.spec_accept_commit(B.SPEC_STOCHASTIC if mode == "stochastic" else B.SPEC_GREEDY, db.parent, db.tokens,
+                             db.target_logits, db.qo, db.max_nodes, db.accept_len, db.path, db.out_tokens,
+                             db.acc_ws, db.k_tree, db.v_tree, db.page_table, db.prefix_len, db.k_pool, db.v_pool,
+                             seq_len_out=db.seq_len, draft_logits=db.draft_logits if mode == "stochastic" else None,
+                             uniforms=db.uniforms if mode == "stochastic" else None, temperature=inp.temperature,
+                             flags=db.flags, dev_status=db.status, token_buf=buf)
     torch.cuda.synchronize()
     assert _status(db) == 0
     ref = _oracle_accept(inp, mode)
