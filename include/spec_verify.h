@@ -134,8 +134,9 @@ int spec_attn_plan(int dtype, int batch, int max_nodes, int hq, int hkv, int d, 
  * (the root and each accepted node) -- always for SPEC_STOCHASTIC; for SPEC_GREEDY when a
  * model of the two ways (a walk from the root, one 8-CTA cluster per sequence, at most
  * path_cap rows each, against streaming every row at the copy rate) finds the walk
- * cheaper, which needs many rows per sequence -- and 0 when it streams every row. The
- * results are the same either way. sm_count: the GPU's SMs (0: the current device's).
+ * cheaper, which needs many rows per sequence -- and 0 when it streams every row (logits
+ * in host memory always walk, whatever this says). The results are the same either way.
+ * sm_count: the GPU's SMs (0: the current device's).
  * Assumes 16-byte aligned logits rows (the walk needs them). Returns SPEC_OK,
  * SPEC_ERR_ARG, or SPEC_ERR_CUDA when sm_count is 0 and no device answers. */
 int spec_accept_plan(int mode, int batch, int total_nodes, int vocab, int path_cap, int sm_count, int* walk);
@@ -244,6 +245,13 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
  *   parent, draft_tokens  int32 [total_nodes]  (root's token = last accepted token)
  *   target_logits  float [total_nodes][vocab]
  *   draft_logits   float [total_nodes][vocab]  (stochastic only; NULL for greedy)
+ *                  Either may sit in device memory or in pinned host memory the
+ *                  device reads at the same address (cudaHostAlloc, or
+ *                  cudaHostRegister, under unified addressing). From host memory
+ *                  only the visited rows cross the host link (NVLink-C2C on a
+ *                  Grace-Blackwell part): greedy acceptance then always walks from
+ *                  the root. Any other pointer (pageable host memory, pinned
+ *                  memory mapped elsewhere) returns SPEC_ERR_ARG.
  *   uniforms       float [total_nodes][2]      (stochastic only) (u_accept, u_bonus) in [0,1)
  *   temperature    > 0 (stochastic only)
  *   path_cap       row length of path / out_tokens (>= deepest accepted path + 1; the

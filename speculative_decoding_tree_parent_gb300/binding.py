@@ -117,6 +117,18 @@ def _dtype(t) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+def _logits_ptr(t) -> int | None:
+    """Logits may be a device tensor or a pinned host tensor (the library checks that the
+    device reads it at the same address; the acceptance then reads only the rows it visits)."""
+    if t is None:
+        return None
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("device tensor or pinned host tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
 def _need(t, dtype, what):
     if t.dtype != dtype:
         raise ValueError(f"{what}: {dtype} expected, got {t.dtype}")
@@ -195,7 +207,8 @@ def spec_accept(mode, parent, draft_tokens, target_logits, qo_indptr, max_nodes,
                 ws, draft_logits=None, uniforms=None, temperature=1.0, flags=None, dev_status=None, stream=None):
     T, V = target_logits.shape
     st = load().spec_accept(
-        int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+        int(mode), _ptr(parent), _ptr(draft_tokens), _logits_ptr(target_logits), _logits_ptr(draft_logits),
+        _ptr(uniforms),
         float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
         _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(dev_status), _stream(stream))
@@ -225,7 +238,8 @@ def spec_accept_commit(mode, parent, draft_tokens, target_logits, qo_indptr, max
     num_pages, _, ps, _ = k_pool.shape
     stride = token_buf.shape[1] if token_buf is not None else 0
     st = load().spec_accept_commit(
-        int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+        int(mode), _ptr(parent), _ptr(draft_tokens), _logits_ptr(target_logits), _logits_ptr(draft_logits),
+        _ptr(uniforms),
         float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
         _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _dtype(k_tree), _ptr(k_tree), _ptr(v_tree),
         _ptr(page_table), page_table.shape[1], num_pages, ps, _ptr(prefix_len), _ptr(seq_len_out), _ptr(k_pool),
@@ -241,7 +255,8 @@ def spec_accept_noalloc(mode, parent, draft_tokens, target_logits, qo_indptr, ma
     memory; the scratch is a fixed array inside the library (see include/spec_verify.h)."""
     T, V = target_logits.shape
     st = load().spec_accept_noalloc(
-        int(mode), _ptr(parent), _ptr(draft_tokens), _ptr(target_logits), _ptr(draft_logits), _ptr(uniforms),
+        int(mode), _ptr(parent), _ptr(draft_tokens), _logits_ptr(target_logits), _logits_ptr(draft_logits),
+        _ptr(uniforms),
         float(temperature), V, _ptr(qo_indptr), qo_indptr.numel() - 1, T, int(max_nodes), path.shape[1],
         _ptr(accept_len), _ptr(path), _ptr(out_tokens), _ptr(flags), _ptr(dev_status), _stream(stream))
     return _check(st, "spec_accept_noalloc")

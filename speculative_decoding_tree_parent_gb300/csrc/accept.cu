@@ -1492,7 +1492,7 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
                   const float* dl, const float* uniforms, float temperature, int vocab,
                   const int32_t* qo, int batch, int total_nodes, int path_cap, int32_t* accept_len,
                   int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws, int32_t* status,
-                  cudaStream_t stream, const CommitArgs* commit) {
+                  cudaStream_t stream, const CommitArgs* commit, bool host_logits) {
   CommitArgs ca = {};
   if (commit != nullptr) ca = *commit;
   const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(tl) & 15) == 0) &&
@@ -1504,7 +1504,8 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
       return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 0;
     });
     if (sms == 0) return SPEC_ERR_CUDA;
-    if (greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
+    // logits in host memory: the walk, whose reads cross the host link for the visited rows only
+    if (host_logits || greedy_walks(batch, total_nodes, vocab, path_cap, sms)) {
       if (launch_pdl(accept_greedy_lazy_kernel, dim3(kLazyCluster, batch), dim3(kLazyThreads), 0, stream, tl, vocab,
                      qo, parent, tokens, path_cap, accept_len, path, out_tokens, flags, status, vec, early_reads(), ca) !=
           cudaSuccess)
@@ -1517,7 +1518,8 @@ int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const 
   // sequence, launched to start as the acceptance grid drains), like the stochastic path.
   if (mode == SPEC_GREEDY && ca.k_tree != nullptr && batch > kCommitCta) {
     const int e = launch_accept(mode, parent, tokens, tl, dl, uniforms, temperature, vocab, qo, batch, total_nodes,
-                                path_cap, accept_len, path, out_tokens, flags, ws, status, stream, nullptr);
+                                path_cap, accept_len, path, out_tokens, flags, ws, status, stream, nullptr,
+                                host_logits);
     if (e != SPEC_OK) return e;
     return launch_kv_commit(ca.elem_bytes, ca.k_tree, ca.v_tree, path, path_cap, accept_len, qo, ca.page_table,
                             ca.max_pages, ca.num_pages, ca.page_size, ca.prefix_len, ca.seq_len_out, ca.k_pool,

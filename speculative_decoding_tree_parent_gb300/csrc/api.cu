@@ -17,7 +17,8 @@ int launch_kv_commit(int elem_bytes, const void* k_tree, const void* v_tree, con
 int launch_accept(int mode, const int32_t* parent, const int32_t* tokens, const float* tl, const float* dl,
                   const float* uniforms, float temperature, int vocab, const int32_t* qo, int batch,
                   int total_nodes, int path_cap, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
-                  uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream, const CommitArgs* commit);
+                  uint8_t* flags, void* ws, int32_t* status, cudaStream_t stream, const CommitArgs* commit,
+                  bool host_logits);
 size_t accept_ws_bytes(int batch, int total_nodes, int vocab);
 int accept_noalloc_scratch(int batch, int total_nodes, int vocab, cudaStream_t stream, void** ws);
 int launch_attn_simt(int dtype, const void* q, const void* k_pool, const void* v_pool, int num_pages, int ps,
@@ -184,6 +185,28 @@ int spec_tree_verify_attn(int dtype, const void* q, const void* k_pool, const vo
 
 // Host checks of spec_accept's arguments other than the workspace (SPEC_OK when they pass);
 // spec_accept_noalloc makes the same checks.
+// Where logits live: device memory, or host memory the device reads at the same address
+// (pinned by cudaHostAlloc or cudaHostRegister under unified addressing; on a Grace-Blackwell
+// part the rows then cross NVLink-C2C as the kernels read them). Anything else -- pageable or
+// unregistered host memory, or pinned memory the device sees at another address -- is refused,
+// so no kernel is handed an address it cannot read.
+static int logits_where(const void* p, bool* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SPEC_ERR_ARG;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *host = false;
+    return SPEC_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == p) {
+    *host = true;
+    return SPEC_OK;
+  }
+  return SPEC_ERR_ARG;
+}
+
 static int check_accept_args(int mode, const int32_t* parent, const int32_t* draft_tokens,
                              const float* target_logits, const float* draft_logits, const float* uniforms,
                              float temperature, int vocab, const int32_t* qo_indptr, int batch, int total_nodes,
@@ -199,6 +222,15 @@ static int check_accept_args(int mode, const int32_t* parent, const int32_t* dra
   if (mode == SPEC_STOCHASTIC && (!draft_logits || !uniforms || !(temperature > 0.f))) return SPEC_ERR_ARG;
   if (mode == SPEC_STOCHASTIC && !grid_fits(batch)) return SPEC_ERR_UNSUPPORTED;  // one cluster row each
   return SPEC_OK;
+}
+
+// The last host check of an acceptance call (after every other): where its logits live.
+static int accept_logits_where(int mode, const float* target_logits, const float* draft_logits, bool* host) {
+  bool ht = false, hd = false;
+  int rc = logits_where(target_logits, &ht);
+  if (rc == SPEC_OK && mode == SPEC_STOCHASTIC) rc = logits_where(draft_logits, &hd);
+  *host = ht || hd;
+  return rc;
 }
 
 // Host checks of spec_accept's arguments (SPEC_OK when they pass).
@@ -239,13 +271,16 @@ int spec_accept(int mode, const int32_t* parent, const int32_t* draft_tokens, co
                 const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
                 int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags, void* ws,
                 size_t ws_bytes, int32_t* dev_status, void* stream) {
-  const int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
-                              qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws,
-                              ws_bytes);
+  bool host = false;
+  int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
+                        qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws,
+                        ws_bytes);
   if (rc != SPEC_OK || batch == 0) return rc;
+  rc = accept_logits_where(mode, target_logits, draft_logits, &host);
+  if (rc != SPEC_OK) return rc;
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, static_cast<cudaStream_t>(stream), nullptr);
+                       dev_status, static_cast<cudaStream_t>(stream), nullptr, host);
 }
 
 int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
@@ -253,16 +288,19 @@ int spec_accept_noalloc(int mode, const int32_t* parent, const int32_t* draft_to
                         const int32_t* qo_indptr, int batch, int total_nodes, int max_nodes, int path_cap,
                         int32_t* accept_len, int32_t* path, int32_t* out_tokens, uint8_t* flags,
                         int32_t* dev_status, void* stream) {
+  bool host = false;
   int rc = check_accept_args(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                              qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens);
   if (rc != SPEC_OK || batch == 0) return rc;
+  rc = accept_logits_where(mode, target_logits, draft_logits, &host);
+  if (rc != SPEC_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   rc = accept_noalloc_scratch(batch, total_nodes, vocab, st, &ws);
   if (rc != SPEC_OK) return rc;
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, st, nullptr);
+                       dev_status, st, nullptr, host);
 }
 
 int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tokens, const float* target_logits,
@@ -273,6 +311,7 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
                        int num_pages, int page_size, const int32_t* prefix_len, int32_t* seq_len_out, void* k_pool,
                        void* v_pool, int hkv, int d, int32_t* token_buf, int token_stride, void* ws,
                        size_t ws_bytes, int32_t* dev_status, void* stream) {
+  bool host = false;
   int rc = check_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                         qo_indptr, batch, total_nodes, max_nodes, path_cap, accept_len, path, out_tokens, ws, ws_bytes);
   if (rc != SPEC_OK) return rc;
@@ -280,6 +319,8 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
                     page_size, prefix_len, k_pool, v_pool, batch, total_nodes, hkv, d);
   if (rc != SPEC_OK || batch == 0) return rc;
   if (token_buf != nullptr && token_stride < 1) return SPEC_ERR_ARG;
+  rc = accept_logits_where(mode, target_logits, draft_logits, &host);
+  if (rc != SPEC_OK) return rc;
   CommitArgs ca;
   ca.k_tree = static_cast<const uint8_t*>(k_tree);
   ca.v_tree = static_cast<const uint8_t*>(v_tree);
@@ -297,7 +338,7 @@ int spec_accept_commit(int mode, const int32_t* parent, const int32_t* draft_tok
   ca.ins = TokenInsert{out_tokens, token_buf, token_stride};
   return launch_accept(mode, parent, draft_tokens, target_logits, draft_logits, uniforms, temperature, vocab,
                        qo_indptr, batch, total_nodes, path_cap, accept_len, path, out_tokens, flags, ws,
-                       dev_status, static_cast<cudaStream_t>(stream), &ca);
+                       dev_status, static_cast<cudaStream_t>(stream), &ca, host);
 }
 
 int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int32_t* path, int path_cap,

@@ -111,3 +111,56 @@ def test_greedy_walk_truncates_at_path_cap():
         assert np.array_equal(out[b, :L], full.out_tokens[b, :L])
         last = int(full.path[b, L])
         assert out[b, L] == int(np.argmax(tl[qo[b] + last]))   # the bonus at the last kept node
+
+
+def test_greedy_walk_reads_pinned_host_logits():
+    """Logits in pinned host memory (read in place, only the visited rows): the same
+    results as from device memory and the oracle's, for spec_accept and spec_accept_noalloc."""
+    parent, tokens, tl, qo = _inputs(3)
+    dev = "cuda"
+    i32 = dict(dtype=torch.int32, device=dev)
+    T = tl.shape[0]
+    ref = oracle.greedy_accept(parent, tokens, tl, qo, 9)
+    host = torch.from_numpy(tl).pin_memory()
+    par, tok, qo_d = (torch.from_numpy(x).to(dev) for x in (parent, tokens, qo))
+    for noalloc in (False, True):
+        acc, path, out = torch.empty(NB, **i32), torch.empty((NB, 9), **i32), torch.empty((NB, 9), **i32)
+        status = torch.zeros(1, **i32)
+        if noalloc:
+            B.spec_accept_noalloc(B.SPEC_GREEDY, par, tok, host, qo_d, N, acc, path, out, dev_status=status)
+        else:
+            ws = torch.zeros(B.spec_workspace_size(B.SPEC_OP_ACCEPT, NB, T, N, 0, 0, 0, 0, V), dtype=torch.uint8,
+                             device=dev)
+            B.spec_accept(B.SPEC_GREEDY, par, tok, host, qo_d, N, acc, path, out, ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(acc.cpu().numpy(), ref.accept_len)
+        assert np.array_equal(path.cpu().numpy(), ref.path)
+        assert np.array_equal(out.cpu().numpy(), ref.out_tokens)
+
+
+def test_accept_refuses_pageable_host_logits():
+    """Logits in pageable host memory (not addressable by the device at that pointer): the
+    host check answers SPEC_ERR_ARG before any launch; nothing is written."""
+    import ctypes
+
+    parent, tokens, tl, qo = _inputs(4)
+    dev = "cuda"
+    i32 = dict(dtype=torch.int32, device=dev)
+    T = tl.shape[0]
+    par, tok, qo_d = (torch.from_numpy(x).to(dev) for x in (parent, tokens, qo))
+    acc = torch.full((NB,), -7, **i32)
+    path, out = torch.empty((NB, 9), **i32), torch.empty((NB, 9), **i32)
+    ws = torch.zeros(B.spec_workspace_size(B.SPEC_OP_ACCEPT, NB, T, N, 0, 0, 0, 0, V), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, **i32)
+    pageable = np.ascontiguousarray(tl)                 # plain numpy memory: never registered
+    lib = B.load()
+    rc = lib.spec_accept(B.SPEC_GREEDY, par.data_ptr(), tok.data_ptr(), pageable.ctypes.data, None, None,
+                         ctypes.c_float(1.0), V, qo_d.data_ptr(), NB, T, N, 9, acc.data_ptr(), path.data_ptr(),
+                         out.data_ptr(), None, ws.data_ptr(), ws.numel(), status.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == -1   # SPEC_ERR_ARG
+    assert (acc.cpu() == -7).all() and int(status.item()) == 0
+    with pytest.raises(ValueError):
+        B.spec_accept(B.SPEC_GREEDY, par, tok, torch.from_numpy(pageable), qo_d, N, acc, path, out, ws)

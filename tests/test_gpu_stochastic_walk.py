@@ -27,7 +27,7 @@ if not torch.cuda.is_available():  # collected on CPU machines, skipped there
     pytest.skip("needs a GPU", allow_module_level=True)
 
 
-def _run(parent, toks, tl, dl, u, qo, path_cap, temperature=1.0):
+def _run(parent, toks, tl, dl, u, qo, path_cap, temperature=1.0, host_logits=False):
     dev = "cuda"
     T, V = tl.shape
     Bn = len(qo) - 1
@@ -41,9 +41,10 @@ def _run(parent, toks, tl, dl, u, qo, path_cap, temperature=1.0):
     flags = torch.empty(Bn, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, **i32)
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    logits = (lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).pin_memory()) if host_logits else f32
     B.spec_accept(B.SPEC_STOCHASTIC, torch.from_numpy(np.asarray(parent, np.int32)).to(dev),
-                  torch.from_numpy(np.asarray(toks, np.int32)).to(dev), f32(tl), torch.from_numpy(
-                      np.asarray(qo, np.int32)).to(dev), max_nodes, acc, path, out, ws, draft_logits=f32(dl),
+                  torch.from_numpy(np.asarray(toks, np.int32)).to(dev), logits(tl), torch.from_numpy(
+                      np.asarray(qo, np.int32)).to(dev), max_nodes, acc, path, out, ws, draft_logits=logits(dl),
                   uniforms=f32(u), temperature=temperature, flags=flags, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -68,6 +69,10 @@ def test_stochastic_wide_nodes(V, seed):
     parent = np.concatenate(parents).astype(np.int32)
     path_cap = 8
     got = _run(parent, toks, tl, dl, u, qo, path_cap)
+    if V == 4096:  # the same from pinned host logits, read in place: bit for bit
+        got_h = _run(parent, toks, tl, dl, u, qo, path_cap, host_logits=True)
+        for x, y in zip(got, got_h):
+            assert np.array_equal(x, y)
     ref = oracle.stochastic_accept(parent, toks, tl, dl, u, 1.0, np.asarray(qo), path_cap)
     keep = ref.flags == 0
     assert keep.sum() >= len(keep) - 2
