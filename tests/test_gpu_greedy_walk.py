@@ -164,3 +164,33 @@ def test_accept_refuses_pageable_host_logits():
     assert (acc.cpu() == -7).all() and int(status.item()) == 0
     with pytest.raises(ValueError):
         B.spec_accept(B.SPEC_GREEDY, par, tok, torch.from_numpy(pageable), qo_d, N, acc, path, out, ws)
+
+
+def test_stream_reads_pinned_host_logits_unaligned_rows():
+    """A 1001-token vocabulary (rows not 16-byte aligned, so the walk is unavailable): the
+    streaming kernel reads every row from pinned host memory, with the oracle's results."""
+    rng = np.random.default_rng(5)
+    Vs, nb, n = 1001, 6, 10
+    parent = np.concatenate([[-1] + [int(rng.integers(0, i)) for i in range(1, n)] for _ in range(nb)]).astype(np.int32)
+    tokens = rng.integers(0, Vs, nb * n).astype(np.int32)
+    tl = rng.standard_normal((nb * n, Vs)).astype(np.float32)
+    qo = (np.arange(nb + 1) * n).astype(np.int32)
+    for b in range(nb):                                  # a child's token at the root's argmax
+        kids = [c for c in range(1, n) if parent[b * n + c] == 0]
+        tl[b * n, tokens[b * n + kids[0]]] = 9.0
+    ref = oracle.greedy_accept(parent, tokens, tl, qo, n)
+    dev = "cuda"
+    i32 = dict(dtype=torch.int32, device=dev)
+    acc, path, out = torch.empty(nb, **i32), torch.empty((nb, n), **i32), torch.empty((nb, n), **i32)
+    status = torch.zeros(1, **i32)
+    ws = torch.zeros(B.spec_workspace_size(B.SPEC_OP_ACCEPT, nb, nb * n, n, 0, 0, 0, 0, Vs), dtype=torch.uint8,
+                     device=dev)
+    host = torch.from_numpy(tl).pin_memory()
+    B.spec_accept(B.SPEC_GREEDY, torch.from_numpy(parent).to(dev), torch.from_numpy(tokens).to(dev), host,
+                  torch.from_numpy(qo).to(dev), n, acc, path, out, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(acc.cpu().numpy(), ref.accept_len)
+    assert np.array_equal(path.cpu().numpy(), ref.path)
+    assert np.array_equal(out.cpu().numpy(), ref.out_tokens)
+    assert (ref.accept_len >= 1).all()
