@@ -301,6 +301,48 @@ def time_graph(fn, stream, flush_l2, warmup, n):
     return statistics.median(ts)
 
 
+def accept_depth_table(inp, mode, dev, stream, flush_l2, warmup, n):
+    """The verification step of `inp` with its target logits planted so that the walk accepts
+    d = 0, 1, ... nodes in every sequence: along lowest-id children, each row's argmax moved to
+    the next child's token, and at the last node no child holding the argmax. Median µs of the
+    step and of the fused acceptance + commit (one replay per timing, L2 flushed), with the
+    accepted lengths the device reports."""
+    import dataclasses
+
+    import numpy as np
+
+    from speculative_decoding_tree_parent_gb300.step import DeviceBatch
+
+    par, tok, qo = (np.asarray(x) for x in (inp.parent, inp.draft_tokens, inp.qo_indptr))
+    rows = []
+    for d in range(inp.path_cap):
+        tl = np.array(inp.target_logits, copy=True)
+        for b in range(inp.batch):
+            a, e = int(qo[b]), int(qo[b + 1])
+            v = 0
+            for _ in range(d):
+                kids = [c for c in range(v + 1, e - a) if par[a + c] == v]
+                if not kids:
+                    break
+                tl[a + v, tok[a + kids[0]]] = tl[a + v].max() + 8.0
+                v = kids[0]
+            held = {int(tok[a + c]) for c in range(v + 1, e - a) if par[a + c] == v}
+            row = tl[a + v]
+            while int(row.argmax()) in held:
+                row[int(row.argmax())] = row.min() - 1.0
+        db = DeviceBatch(dataclasses.replace(inp, target_logits=tl), device=dev, mode=mode)
+        step = time_graph(lambda: db.step(mode), stream, flush_l2, warmup, n)
+        acc = time_graph(lambda: db.accept_commit(mode), stream, flush_l2, warmup, n)
+        assert db.device_status() == 0
+        got = db.accept_len.cpu()
+        rows.append({"accepted_max": int(got.max()), "accepted_mean": float(got.float().mean()),
+                     "step_us": step, "accept_commit_us": acc})
+        del db
+        if int(got.max()) < d:  # no sequence reaches this depth
+            break
+    return rows
+
+
 def workload_calls(idx, dev, stream, flush_l2, warmup, n):
     """Per-call times of workload idx at full size (one replica; its inputs exceed the L2):
     attention (bf16 cache and FP8 cache) with its % of roofline, and the fused acceptance +
@@ -675,6 +717,10 @@ def run_ours(args):
         extras["tree_sweep"] = {"config": "Llama-3-8B heads, prefix 2048 (shuffled pages), EAGLE-2 trees, vocab "
                                           "128256, mask + attention + greedy accept + commit, median step µs",
                                 "table": tree_sweep_table(dev, stream, flush_l2, 3, nrep, batches=(1, 32, 64, 128))}
+        if mode == "greedy":
+            extras["accept_depth"] = {"config": "this workload with the target logits planted so the walk accepts "
+                                                "d nodes; one step / one fused accept + commit per replay, median µs",
+                                      "table": accept_depth_table(inp, mode, dev, stream, flush_l2, 3, nrep)}
 
     # ---- figures ------------------------------------------------------------------------
     wc = work_counts(inp, db.accept_len.cpu().numpy(), mode)
