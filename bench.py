@@ -301,35 +301,43 @@ def time_graph(fn, stream, flush_l2, warmup, n):
     return statistics.median(ts)
 
 
-def accept_depth_table(inp, mode, dev, stream, flush_l2, warmup, n):
-    """The verification step of `inp` with its target logits planted so that the walk accepts
-    d = 0, 1, ... nodes in every sequence: along lowest-id children, each row's argmax moved to
-    the next child's token, and at the last node no child holding the argmax. Median µs of the
-    step and of the fused acceptance + commit (one replay per timing, L2 flushed), with the
-    accepted lengths the device reports."""
-    import dataclasses
-
+def plant_accept_depth(inp, d):
+    """Target logits of `inp` changed so that greedy acceptance takes d nodes in every sequence
+    whose tree reaches that deep (fewer where it does not): from the root along lowest-id
+    children, each row's maximum raised onto the next child's token; at the last node, no
+    child's token keeps the maximum."""
     import numpy as np
+
+    par, tok, qo = (np.asarray(x) for x in (inp.parent, inp.draft_tokens, inp.qo_indptr))
+    tl = np.array(inp.target_logits, copy=True)
+    for b in range(inp.batch):
+        a, e = int(qo[b]), int(qo[b + 1])
+        v = 0
+        for _ in range(d):
+            kids = [c for c in range(v + 1, e - a) if par[a + c] == v]
+            if not kids:
+                break
+            tl[a + v, tok[a + kids[0]]] = tl[a + v].max() + 8.0
+            v = kids[0]
+        held = {int(tok[a + c]) for c in range(v + 1, e - a) if par[a + c] == v}
+        row = tl[a + v]
+        while int(row.argmax()) in held:
+            row[int(row.argmax())] = row.min() - 1.0
+    return tl
+
+
+def accept_depth_table(inp, mode, dev, stream, flush_l2, warmup, n):
+    """The verification step of `inp` with its target logits planted (plant_accept_depth) so
+    that the walk accepts d = 0, 1, ... nodes. Median µs of the step and of the fused
+    acceptance + commit (one replay per timing, L2 flushed), with the accepted lengths the
+    device reports."""
+    import dataclasses
 
     from speculative_decoding_tree_parent_gb300.step import DeviceBatch
 
-    par, tok, qo = (np.asarray(x) for x in (inp.parent, inp.draft_tokens, inp.qo_indptr))
     rows = []
     for d in range(inp.path_cap):
-        tl = np.array(inp.target_logits, copy=True)
-        for b in range(inp.batch):
-            a, e = int(qo[b]), int(qo[b + 1])
-            v = 0
-            for _ in range(d):
-                kids = [c for c in range(v + 1, e - a) if par[a + c] == v]
-                if not kids:
-                    break
-                tl[a + v, tok[a + kids[0]]] = tl[a + v].max() + 8.0
-                v = kids[0]
-            held = {int(tok[a + c]) for c in range(v + 1, e - a) if par[a + c] == v}
-            row = tl[a + v]
-            while int(row.argmax()) in held:
-                row[int(row.argmax())] = row.min() - 1.0
+        tl = plant_accept_depth(inp, d)
         db = DeviceBatch(dataclasses.replace(inp, target_logits=tl), device=dev, mode=mode)
         step = time_graph(lambda: db.step(mode), stream, flush_l2, warmup, n)
         acc = time_graph(lambda: db.accept_commit(mode), stream, flush_l2, warmup, n)
