@@ -749,11 +749,8 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
   cg::cluster_group cl = cg::this_cluster();
   constexpr int kWarps = kLazyThreads / 32;
   __shared__ int s_par[kMaxTreeNodes], s_tok[kMaxTreeNodes];
-  __shared__ float s_wv[kWarps];
-  __shared__ int s_wi[kWarps];
-  __shared__ float s_bv[2];  // this CTA's (max, index) of the step, by step parity
-  __shared__ int s_bi[2];
-  __shared__ int s_child;
+  __shared__ float s_wv[2][kWarps];  // each warp's (max, index) of the step, by step parity
+  __shared__ int s_wi[2][kWarps];
   __shared__ int s_path[kMaxTreeNodes];  // the accepted nodes, written out after the wait below
   // The walk reads inputs only (the tree, the logits, qo_indptr). Where the caller has
   // declared that the kernel enqueued before this one writes none of them (early), it runs
@@ -815,37 +812,40 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kLazyThre
     }
     warp_arg_reduce(bv, bi);
     if (lane == 0) {
-      s_wv[warp] = bv;
-      s_wi[warp] = bi;
+      s_wv[parity][warp] = bv;
+      s_wi[parity][warp] = bi;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kWarps; ++w) arg_better(bv, bi, s_wv[w], s_wi[w]);
-      s_bv[parity] = bv;
-      s_bi[parity] = bi;
-      s_child = INT_MAX;
-    }
-    cl.sync();  // every CTA's (max, index) is in place
-    float ov[kLazyCluster];
-    int oi[kLazyCluster];
+    // One barrier per step: every warp of every CTA publishes its pair, then every warp reads
+    // all kLazyCluster x kWarps pairs itself (kPer per lane, every load issued first) and finds
+    // the child on its own, so no block barrier follows. (A pair of this parity is written
+    // again two steps on, after the next step's barrier, which no thread passes before it has
+    // finished reading this step's pairs.)
+    cl.sync();
+    constexpr int kPairs = kLazyCluster * kWarps, kPer = kPairs / 32;
+    static_assert(kPairs % 32 == 0, "the pairs split evenly over a warp's lanes");
+    float ov[kPer];
+    int oi[kPer];
 #pragma unroll
-    for (int r = 0; r < kLazyCluster; ++r) {  // all sixteen loads first
-      ov[r] = *cl.map_shared_rank(&s_bv[parity], r);
-      oi[r] = *cl.map_shared_rank(&s_bi[parity], r);
+    for (int k = 0; k < kPer; ++k) {
+      const int e = lane + 32 * k, r = e / kWarps, w = e - r * kWarps;
+      ov[k] = *cl.map_shared_rank(&s_wv[parity][w], r);
+      oi[k] = *cl.map_shared_rank(&s_wi[parity][w], r);
     }
     float av = ov[0];
     int ai = oi[0];
 #pragma unroll
-    for (int r = 1; r < kLazyCluster; ++r) arg_better(av, ai, ov[r], oi[r]);
+    for (int k = 1; k < kPer; ++k) arg_better(av, ai, ov[k], oi[k]);
+    warp_arg_reduce(av, ai);  // (a total order: every warp of every CTA gets the same pair)
     const int a = ai == INT_MAX ? 0 : ai;  // (an empty or all-NaN row: token 0, as the stream kernel)
-    // the child of v whose token is a, lowest id first
+    // the child of v whose token is a, lowest id first: each lane's first match, then the
+    // warp's minimum
     int mine = INT_MAX;
-    for (int c = v + 1 + threadIdx.x; c < n; c += kLazyThreads)
-      if (s_par[c] == v && s_tok[c] == a && c < mine) mine = c;
-    mine = (int)__reduce_min_sync(0xffffffffu, (unsigned)mine);
-    if (lane == 0 && mine != INT_MAX) atomicMin(&s_child, mine);
-    __syncthreads();
-    const int c = s_child;
+    for (int c = v + 1 + lane; c < n; c += 32)
+      if (s_par[c] == v && s_tok[c] == a) {
+        mine = c;
+        break;
+      }
+    const int c = (int)__reduce_min_sync(0xffffffffu, (unsigned)mine);
     if (c == INT_MAX) {
       bonus = a;
       break;
