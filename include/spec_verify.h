@@ -307,9 +307,11 @@ int spec_kv_commit(int dtype, const void* k_tree, const void* v_tree, const int3
  * spec_accept_commit — spec_accept, then spec_kv_commit of the paths it accepted, in one
  *   call: the results (accept_len, path, out_tokens, flags, the written pool rows,
  *   seq_len_out, device errors) are those of the two calls made back to back on
- *   `stream`. Greedy with up to 4 sequences runs the commit inside the acceptance kernel
- *   (its last CTA, right after the walk); more sequences, and stochastic acceptance, launch
- *   the commit kernel after the acceptance kernels.
+ *   `stream`. Greedy acceptance commits inside its own kernel where it can: walking from
+ *   the root (spec_accept_plan), each sequence's cluster commits that sequence after its
+ *   walk; streaming every row, the last CTA commits up to 4 sequences right after its
+ *   walk. More sequences when streaming, and stochastic acceptance, launch the commit
+ *   kernel after the acceptance kernels.
  *   Arguments: those of spec_accept (mode ... flags, ws, ws_bytes) and of spec_kv_commit
  *   (dtype ... d); path_cap, path and accept_len serve both. The same host errors, the
  *   same layouts; ws as for spec_accept.
