@@ -182,3 +182,16 @@ def test_early_reads_switch(lib):
     with binding.early_reads(True):
         assert binding.spec_set_early_reads(1) == 1
     assert binding.spec_set_early_reads(0) == 0
+
+
+def test_logits_marshalling_refuses_pageable_host_tensors():
+    """The binding passes logits as device tensors or pinned host tensors only; a pageable
+    host tensor is refused before the library is called (the library refuses it too, with
+    SPEC_ERR_ARG, where a device can answer the pointer query)."""
+    import torch
+
+    assert binding._logits_ptr(None) is None
+    with pytest.raises(ValueError):
+        binding._logits_ptr(torch.zeros((4, 8), dtype=torch.float32))
+    with pytest.raises(ValueError):
+        binding._ptr(torch.zeros(4, dtype=torch.int32))   # every other argument: device only
