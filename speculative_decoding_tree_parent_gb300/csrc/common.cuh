@@ -97,11 +97,6 @@ __device__ __forceinline__ F2 f2_warp_sum(F2 x) {
   return x;
 }
 
-__device__ __forceinline__ double f2_to_d(F2 x) { return (double)x.hi + (double)x.lo; }
-__device__ __forceinline__ F2 d_to_f2(double x) {
-  const float hi = (float)x;
-  return F2{hi, (float)(x - (double)hi)};
-}
 // a > b for normalised double-float values (|lo| at most half an ulp of hi).
 __device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 // a * b for a double-float a and an fp32 b: the product of the high parts exactly (fma), the
