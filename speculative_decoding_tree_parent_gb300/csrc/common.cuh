@@ -82,7 +82,7 @@ struct F2 {
 };
 // Double-float sum. Its first step is exact (two-sum), so a + b and b + a give the same
 // bits: every lane of a butterfly ends with the same total.
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+__host__ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
   const float s = a.hi + b.hi;
   const float v = s - a.hi;
   float e = (a.hi - (s - v)) + (b.hi - v);
@@ -98,10 +98,10 @@ __device__ __forceinline__ F2 f2_warp_sum(F2 x) {
 }
 
 // a > b for normalised double-float values (|lo| at most half an ulp of hi).
-__device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__host__ __device__ __forceinline__ bool f2_gt(F2 a, F2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 // a * b for a double-float a and an fp32 b: the product of the high parts exactly (fma), the
 // low part's product added, renormalised.
-__device__ __forceinline__ F2 f2_mul_f(F2 a, float b) {
+__host__ __device__ __forceinline__ F2 f2_mul_f(F2 a, float b) {
   const float p = a.hi * b;
   const float e = fmaf(a.lo, b, fmaf(a.hi, b, -p));
   const float hi = p + e;
@@ -109,7 +109,7 @@ __device__ __forceinline__ F2 f2_mul_f(F2 a, float b) {
 }
 // 1 / (hi + lo) in fp32: the fp32 reciprocal of hi refined once with the residual of both
 // parts (Newton's step r + r (1 - x r)); 0 for a zero or negative input.
-__device__ __forceinline__ float f2_rcp(F2 x) {
+__host__ __device__ __forceinline__ float f2_rcp(F2 x) {
   if (!(x.hi > 0.f)) return 0.f;
   const float r = 1.0f / x.hi;
   const float e = fmaf(-x.hi, r, 1.0f) - x.lo * r;
